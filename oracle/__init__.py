@@ -1,0 +1,120 @@
+"""CPU FP64 oracle for the dense tiled GEMM: test infrastructure only.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+and reference legs may import this package. The CUDA product path
+(``dense_tiled_gemm_gb300``) never imports it, and this package imports
+nothing from there. The two meet only in the seeded input generator
+(``workloads.py``), which holds no GEMM arithmetic.
+
+``gemm_ref`` is a ctypes wrapper around ``gemm_oracle.c``. It implements the
+plain definition C[i][j] = sum_k a[i][k]*b[k][j] in FP64 over the exact
+FP16/BF16 operand values (k ascending), plus C_abs[i][j] = sum_k |a·b|.
+It follows "Two Waves, One Stage Apart" (opening paragraph: a tiled GEMM
+sums operand-tile products) and counts 2·M·N·K flops as in that page's
+Table 1 caption.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemm_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F16, BF16 = 0, 1
+K_MAJOR, MN_MAJOR = 0, 1
+_DTYPE = {"f16": F16, "bf16": BF16}
+_LAYOUT = {"k": K_MAJOR, "mn": MN_MAJOR}
+
+
+def build(force: bool = False) -> str:
+    """Compile gemm_oracle.c with gcc into liboracle.so (next to the source)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-pthread", "-D_POSIX_C_SOURCE=200809L",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def load_library(path: str):
+    """Open a compiled oracle library and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    i64, dp, u16p = ctypes.c_int64, ctypes.POINTER(ctypes.c_double), ctypes.c_void_p
+    lib.oracle_gemm.restype = ctypes.c_int
+    lib.oracle_gemm.argtypes = [u16p, u16p, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_void_p, i64, dp, dp, ctypes.c_int]
+    lib.oracle_decode_f16.restype = ctypes.c_double
+    lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
+    lib.oracle_decode_bf16.restype = ctypes.c_double
+    lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = load_library(build())
+    return _lib
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def decode(bits, dtype: str, lib=None) -> np.ndarray:
+    """Decode 16-bit FP16/BF16 patterns to FP64 with the oracle's own decoder."""
+    lib = lib or _load()
+    fn = lib.oracle_decode_bf16 if dtype == "bf16" else lib.oracle_decode_f16
+    flat = np.asarray(bits, dtype=np.uint16).ravel()
+    return np.array([fn(int(b)) for b in flat], dtype=np.float64).reshape(np.shape(bits))
+
+
+def gemm_ref(A_bits: np.ndarray, B_bits: np.ndarray, M: int, N: int, K: int,
+             dtype_in: str, layout_b: str, rows=None, threads: int | None = None,
+             lib=None):
+    """FP64 reference rows of C = A·B and of C_abs = sum_k |a·b|.
+
+    A_bits: uint16 M×K (row-major). B_bits: uint16 N×K for layout_b="k",
+    K×N for layout_b="mn". ``rows``: output rows to compute (None = all).
+    Returns (C, C_abs), each len(rows)×N (or M×N) float64. ``lib`` selects
+    another compiled copy of the oracle (the tests' planted-mistake checks).
+    """
+    lib = lib or _load()
+    A = np.ascontiguousarray(A_bits, dtype=np.uint16)
+    B = np.ascontiguousarray(B_bits, dtype=np.uint16)
+    if A.size != M * K or B.size != N * K:
+        raise ValueError("operand sizes do not match M, N, K")
+    if rows is None:
+        rows_arr, n_rows, rows_ptr = None, M, None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n_rows = int(rows_arr.size)
+        rows_ptr = rows_arr.ctypes.data_as(ctypes.c_void_p)
+    C = np.empty((n_rows, N), dtype=np.float64)
+    C_abs = np.empty((n_rows, N), dtype=np.float64)
+    if n_rows == 0:
+        return C, C_abs
+    dp = ctypes.POINTER(ctypes.c_double)
+    rc = lib.oracle_gemm(A.ctypes.data_as(ctypes.c_void_p), B.ctypes.data_as(ctypes.c_void_p),
+                         M, N, K, _DTYPE[dtype_in], _LAYOUT[layout_b], rows_ptr, n_rows,
+                         C.ctypes.data_as(dp), C_abs.ctypes.data_as(dp),
+                         int(threads or host_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm failed with code {rc}")
+    return C, C_abs

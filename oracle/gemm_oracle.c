@@ -1,0 +1,239 @@
+/*
+ * CPU FP64 oracle for the dense tiled GEMM C = A·B: test infrastructure only.
+ *
+ * Only the tests, the package's smoke check and the benchmark's CPU-baseline
+ * leg use this file. The product path never links or calls it.
+ *
+ * It computes the definition the tiled kernel computes. "Two Waves, One Stage
+ * Apart: Warp-Pipelining Triton GEMMs on AMD Instinct" (opening paragraph)
+ * defines tiled GEMM as computing on one pair of operand tiles after another,
+ * with each output tile the sum over K of A-tile·B-tile products. Summed over
+ * all tiles, that is
+ *
+ *     C[i][j] = sum_{k=0}^{K-1} a[i][k] * b[k][j]
+ *
+ * and the oracle evaluates it in FP64, with k ascending, over the exact
+ * values of the FP16/BF16 operands. It also returns
+ *
+ *     C_abs[i][j] = sum_k |a[i][k] * b[k][j]|
+ *
+ * which the acceptance bound uses. Every product of two FP16 values (11-bit
+ * significands) or two BF16 values (8-bit significands) is exact in FP64, so
+ * the only rounding is in the FP64 running sum. No blocking or reordering:
+ * one plain i-k-j loop per output row, with rows shared among threads.
+ *
+ * Operand storage (the reading taken for the "K-major" wording of the pages'
+ * kernels, whose B operand is passed transposed, "B_T"):
+ *   A       : M x K row-major, a[i][k] at A[i*K + k]
+ *   B k-major : N x K, K contiguous, b[k][j] at B[j*K + k]
+ *   B mn-major: K x N, N contiguous, b[k][j] at B[k*N + j]
+ *
+ * Build: plain C99, gcc -O2 -ffp-contract=off (no fused multiply-add, so
+ * x86 and Arm hosts give identical bits), -pthread.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_K_MAJOR = 0, ORACLE_MN_MAJOR = 1 };
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ * Normal:    (1024 + f) * 2^(e - 15 - 10)
+ * Subnormal: f * 2^(1 - 15 - 10) = f * 2^-24                                */
+double oracle_decode_f16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);
+    else if (e == 0x1f)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + f), e - 25);
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper half of an IEEE binary32: 1 sign bit, 8 exponent bits
+ * (bias 127), 7 fraction bits.
+ * Normal:    (128 + f) * 2^(e - 127 - 7)
+ * Subnormal: f * 2^(1 - 127 - 7) = f * 2^-133                               */
+double oracle_decode_bf16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xff;
+    int f = h & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);
+    else if (e == 0xff)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + f), e - 134);
+    return sign ? -v : v;
+}
+
+static double decode(uint16_t h, int dtype)
+{
+    return dtype == ORACLE_BF16 ? oracle_decode_bf16(h) : oracle_decode_f16(h);
+}
+
+typedef struct {
+    /* shared */
+    const uint16_t *A;
+    const double *Bd;      /* decoded b[k][j], K x N row-major */
+    const uint16_t *B;     /* raw B, for the decode phase */
+    int64_t M, N, K;
+    int dtype, layout_b;
+    const int64_t *rows;
+    int64_t n_rows;
+    double *C, *C_abs;
+    /* per thread */
+    int64_t lo, hi;        /* range of output rows (decode: range of k) */
+    int phase;             /* 0: decode B, 1: rows of C */
+} job_t;
+
+static void decode_b_rows(const job_t *j)
+{
+    double *Bd = (double *)j->Bd;
+    for (int64_t k = j->lo; k < j->hi; ++k)
+        for (int64_t c = 0; c < j->N; ++c) {
+            uint16_t bits = j->layout_b == ORACLE_K_MAJOR ? j->B[c * j->K + k]
+                                                          : j->B[k * j->N + c];
+            Bd[k * j->N + c] = decode(bits, j->dtype);
+        }
+}
+
+static void gemm_rows(const job_t *j)
+{
+    const int64_t N = j->N, K = j->K;
+    for (int64_t r = j->lo; r < j->hi; ++r) {
+        const int64_t i = j->rows ? j->rows[r] : r;
+        double *c = j->C + r * N;
+        double *cabs = j->C_abs + r * N;
+        for (int64_t col = 0; col < N; ++col) {
+            c[col] = 0.0;
+            cabs[col] = 0.0;
+        }
+        for (int64_t k = 0; k < K; ++k) {
+            const double a = decode(j->A[i * K + k], j->dtype);
+            const double *b = j->Bd + k * N;
+            for (int64_t col = 0; col < N; ++col) {
+                const double p = a * b[col];
+                c[col] += p;
+                cabs[col] += fabs(p);
+            }
+        }
+    }
+}
+
+static void *worker(void *arg)
+{
+    const job_t *j = (const job_t *)arg;
+    if (j->phase == 0)
+        decode_b_rows(j);
+    else
+        gemm_rows(j);
+    return NULL;
+}
+
+static int run_threads(job_t *base, int64_t count, int n_threads)
+{
+    if (count <= 0)
+        return 0;
+    if (n_threads > count)
+        n_threads = (int)count;
+    pthread_t *tid = (pthread_t *)calloc((size_t)n_threads, sizeof(pthread_t));
+    char *started = (char *)calloc((size_t)n_threads, 1);
+    job_t *jobs = (job_t *)calloc((size_t)n_threads, sizeof(job_t));
+    if (!tid || !jobs || !started) {
+        free(tid);
+        free(started);
+        free(jobs);
+        return -2;
+    }
+    for (int t = 0; t < n_threads; ++t) {
+        jobs[t] = *base;
+        jobs[t].lo = count * t / n_threads;
+        jobs[t].hi = count * (t + 1) / n_threads;
+        if (t == n_threads - 1)
+            worker(&jobs[t]);   /* the calling thread takes the last share */
+        else if (pthread_create(&tid[t], NULL, worker, &jobs[t]) == 0)
+            started[t] = 1;
+        else
+            worker(&jobs[t]);   /* no thread available: do the share inline */
+    }
+    for (int t = 0; t < n_threads - 1; ++t)
+        if (started[t])
+            pthread_join(tid[t], NULL);
+    free(tid);
+    free(started);
+    free(jobs);
+    return 0;
+}
+
+/*
+ * Compute selected rows of C = A·B in FP64.
+ *   A, B      : raw 16-bit operand patterns, layouts as described above
+ *   dtype     : ORACLE_F16 or ORACLE_BF16 (both operands)
+ *   layout_b  : ORACLE_K_MAJOR or ORACLE_MN_MAJOR
+ *   rows      : indices of the output rows to compute, or NULL for all M
+ *   n_rows    : number of entries in rows (ignored when rows is NULL)
+ *   C, C_abs  : n_rows x N (or M x N) row-major outputs
+ *   n_threads : worker threads (<= 0: all online CPUs)
+ * Returns 0 on success, -1 for invalid arguments, -2 when memory runs out.
+ */
+int oracle_gemm(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K,
+                int dtype, int layout_b, const int64_t *rows, int64_t n_rows,
+                double *C, double *C_abs, int n_threads)
+{
+    if (!A || !B || !C || !C_abs || M <= 0 || N <= 0 || K <= 0)
+        return -1;
+    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16)
+        return -1;
+    if (layout_b != ORACLE_K_MAJOR && layout_b != ORACLE_MN_MAJOR)
+        return -1;
+    if (rows) {
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (rows[r] < 0 || rows[r] >= M)
+                return -1;
+    } else {
+        n_rows = M;
+    }
+    if (n_threads <= 0) {
+        long n = sysconf(_SC_NPROCESSORS_ONLN);
+        n_threads = n > 0 ? (int)n : 1;
+    }
+    double *Bd = (double *)malloc((size_t)K * (size_t)N * sizeof(double));
+    if (!Bd)
+        return -2;
+    job_t base;
+    memset(&base, 0, sizeof(base));
+    base.A = A;
+    base.B = B;
+    base.Bd = Bd;
+    base.M = M;
+    base.N = N;
+    base.K = K;
+    base.dtype = dtype;
+    base.layout_b = layout_b;
+    base.rows = rows;
+    base.n_rows = n_rows;
+    base.C = C;
+    base.C_abs = C_abs;
+
+    /* phase 0 decodes b[k][j] into FP64 once; phase 1 runs the row loops */
+    base.phase = 0;
+    int rc = run_threads(&base, K, n_threads);
+    if (rc == 0) {
+        base.phase = 1;
+        rc = run_threads(&base, n_rows, n_threads);
+    }
+    free(Bd);
+    return rc;
+}

@@ -1,0 +1,389 @@
+"""Pins for the CPU FP64 oracle (no GPU).
+
+The oracle is checked against things other than itself: the IEEE/bfloat16
+format definitions (hand-written fixtures), numpy's and torch's own FP16/BF16
+conversions, exact rational arithmetic (``fractions``) on tiny shapes, closed
+forms (identity, all-ones, rank-1), exact integer arithmetic, and
+``torch.matmul`` in float64. ``test_planted_mistakes`` compiles copies of the
+oracle with one deliberate bug each and requires every copy to fail at least
+one of these pins.
+"""
+from __future__ import annotations
+
+import math
+import os
+import subprocess
+import tempfile
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import tolerance
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+U = 2.0 ** -53
+
+
+# ---------------------------------------------------------------- helpers
+def f16_bits(vals) -> np.ndarray:
+    return np.asarray(vals, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def bf16_bits(vals) -> np.ndarray:
+    t = torch.tensor(np.asarray(vals, dtype=np.float64), dtype=torch.float64).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_of(vals, dtype):
+    return f16_bits(vals) if dtype == "f16" else bf16_bits(vals)
+
+
+def exact_value(bits: int, dtype: str) -> float:
+    """FP64 value of a pattern via numpy/torch conversions (not the oracle's decoder)."""
+    if dtype == "f16":
+        return float(np.array([bits], dtype=np.uint16).view(np.float16)[0])
+    return float(np.array([bits << 16], dtype=np.uint32).view(np.float32)[0])
+
+
+def random_finite_bits(rng: np.random.Generator, n: int, dtype: str) -> np.ndarray:
+    """Finite patterns with every exponent represented, subnormals included."""
+    if dtype == "f16":
+        e = rng.integers(0, 31, n)
+        f = rng.integers(0, 1024, n)
+        word = (e << 10) | f
+    else:
+        e = rng.integers(0, 255, n)
+        f = rng.integers(0, 128, n)
+        word = (e << 7) | f
+    sign = rng.integers(0, 2, n) << 15
+    return (word | sign).astype(np.uint16)
+
+
+def b_storage(Bkn: np.ndarray, layout_b: str) -> np.ndarray:
+    """Store a K×N matrix of patterns in the requested B layout."""
+    return np.ascontiguousarray(Bkn.T if layout_b == "k" else Bkn)
+
+
+def gamma(K: int) -> float:
+    """Bound on FP64 sequential-summation error relative to sum |terms|."""
+    return K * U / (1 - K * U)
+
+
+# ---------------------------------------------------------------- pin battery
+def _pin_decoders(lib):
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    out = []
+    for dtype in ("f16", "bf16"):
+        mine = oracle.decode(allbits, dtype, lib=lib)
+        if dtype == "f16":
+            ref = allbits.view(np.float16).astype(np.float64)
+        else:
+            with np.errstate(invalid="ignore"):
+                ref = (allbits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        same = (mine == ref) | (np.isnan(mine) & np.isnan(ref))
+        if not same.all():
+            out.append(f"decoder_{dtype}")
+    return out
+
+
+def _parse_format_fixture(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as fh:
+        for line in fh:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            bits, mant, expo = line.split()[:3]
+            if mant in ("inf", "-inf"):
+                val = float(mant)
+            else:
+                val = math.ldexp(float(int(mant)), int(expo))
+            rows.append((int(bits, 16), val))
+    return rows
+
+
+def _pin_format_fixtures(lib):
+    out = []
+    for name, dtype in (("binary16_values.txt", "f16"), ("bfloat16_values.txt", "bf16")):
+        for bits, val in _parse_format_fixture(name):
+            got = float(oracle.decode(np.array([bits], dtype=np.uint16), dtype, lib=lib)[0])
+            if got != val:
+                out.append(f"fixture_{dtype}_{bits:#06x}")
+    return out
+
+
+def _parse_gemm_fixture():
+    cases, cur, key = [], None, None
+    with open(os.path.join(GOLDEN, "gemm_hand_2x2.txt")) as fh:
+        for line in fh:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            tok = line.split()
+            if tok[0] == "case":
+                cur = {"name": tok[1]}
+                cases.append(cur)
+            elif tok[0] in ("A", "B", "C", "C_abs"):
+                key = tok[0]
+                cur[key] = []
+            else:
+                cur[key].append([float(t) for t in tok])
+    return [{k: (np.array(v) if k != "name" else v) for k, v in c.items()} for c in cases]
+
+
+def _pin_hand_gemm(lib):
+    out = []
+    for case in _parse_gemm_fixture():
+        A, Bkn, C, Cabs = case["A"], case["B"], case["C"], case["C_abs"]
+        M, K = A.shape
+        N = Bkn.shape[1]
+        for dtype in ("f16", "bf16"):
+            for lay in ("k", "mn"):
+                got, gabs = oracle.gemm_ref(bits_of(A, dtype), b_storage(bits_of(Bkn, dtype), lay),
+                                            M, N, K, dtype, lay, lib=lib)
+                if not (np.array_equal(got, C) and np.array_equal(gabs, Cabs)):
+                    out.append(f"hand_{case['name']}_{dtype}_{lay}")
+    return out
+
+
+def _pin_brute_force(lib):
+    out = []
+    rng = np.random.default_rng(1234)
+    for (M, N, K) in ((1, 1, 1), (2, 3, 4), (5, 7, 3), (17, 9, 33)):
+        for dtype in ("f16", "bf16"):
+            for lay in ("k", "mn"):
+                Ab = random_finite_bits(rng, M * K, dtype).reshape(M, K)
+                Bkn = random_finite_bits(rng, K * N, dtype).reshape(K, N)
+                got, gabs = oracle.gemm_ref(Ab, b_storage(Bkn, lay), M, N, K, dtype, lay, lib=lib)
+                av = [[Fraction(exact_value(int(x), dtype)) for x in row] for row in Ab]
+                bv = [[Fraction(exact_value(int(x), dtype)) for x in row] for row in Bkn]
+                for i in range(M):
+                    for j in range(N):
+                        terms = [av[i][k] * bv[k][j] for k in range(K)]
+                        ex = sum(terms)
+                        ea = sum(abs(t) for t in terms)
+                        lim = gamma(K) * float(ea)
+                        if abs(Fraction(got[i, j]) - ex) > Fraction(lim):
+                            out.append(f"brute_{M}x{N}x{K}_{dtype}_{lay}")
+                            break
+                        if abs(Fraction(gabs[i, j]) - ea) > Fraction(lim):
+                            out.append(f"brute_abs_{M}x{N}x{K}_{dtype}_{lay}")
+                            break
+                    else:
+                        continue
+                    break
+    return out
+
+
+def _pin_closed_forms(lib):
+    out = []
+    rng = np.random.default_rng(7)
+    for dtype in ("f16", "bf16"):
+        for lay in ("k", "mn"):
+            # identity B (N = K): C = A exactly
+            M, K = 13, 24
+            Ab = random_finite_bits(rng, M * K, dtype).reshape(M, K)
+            eye = bits_of(np.eye(K), dtype)
+            got, _ = oracle.gemm_ref(Ab, b_storage(eye, lay), M, K, K, dtype, lay, lib=lib)
+            ref = np.vectorize(lambda b: exact_value(int(b), dtype))(Ab)
+            if not np.array_equal(got, ref):
+                out.append(f"identity_{dtype}_{lay}")
+            # all-ones A: C[i][j] = column sum of B (math.fsum is correctly rounded)
+            M, N, K = 3, 11, 40
+            vals = rng.uniform(-4, 4, (K, N))
+            Bkn = bits_of(vals, dtype)
+            ones = bits_of(np.ones((M, K)), dtype)
+            got, gabs = oracle.gemm_ref(ones, b_storage(Bkn, lay), M, N, K, dtype, lay, lib=lib)
+            bv = np.vectorize(lambda b: exact_value(int(b), dtype))(Bkn)
+            for j in range(N):
+                col = math.fsum(bv[:, j])
+                lim = 2 * gamma(K) * float(np.abs(bv[:, j]).sum())
+                if np.any(np.abs(got[:, j] - col) > lim):
+                    out.append(f"ones_{dtype}_{lay}")
+                    break
+            # rank-1: a[i][k] = u_i, b[k][j] = v_j gives K * u_i * v_j exactly
+            M, N, K = 6, 5, 37
+            u = bits_of(rng.uniform(-3, 3, M), dtype)
+            v = bits_of(rng.uniform(-3, 3, N), dtype)
+            Ab = np.repeat(u[:, None], K, axis=1)
+            Bkn = np.repeat(v[None, :], K, axis=0)
+            got, _ = oracle.gemm_ref(Ab, b_storage(Bkn, lay), M, N, K, dtype, lay, lib=lib)
+            uv = np.array([exact_value(int(b), dtype) for b in u])
+            vv = np.array([exact_value(int(b), dtype) for b in v])
+            if not np.array_equal(got, K * np.outer(uv, vv)):
+                out.append(f"rank1_{dtype}_{lay}")
+    return out
+
+
+def _pin_integers(lib):
+    """Small integers: every partial sum is exact, so C equals int64 matmul."""
+    out = []
+    rng = np.random.default_rng(11)
+    for dtype in ("f16", "bf16"):
+        for lay in ("k", "mn"):
+            M, N, K = 19, 23, 300
+            Ai = rng.integers(-3, 4, (M, K))
+            Bi = rng.integers(-3, 4, (K, N))
+            got, gabs = oracle.gemm_ref(bits_of(Ai, dtype), b_storage(bits_of(Bi, dtype), lay),
+                                        M, N, K, dtype, lay, lib=lib)
+            if not (np.array_equal(got, (Ai @ Bi).astype(np.float64))
+                    and np.array_equal(gabs, (np.abs(Ai) @ np.abs(Bi)).astype(np.float64))):
+                out.append(f"integer_{dtype}_{lay}")
+    return out
+
+
+def _pin_torch_matmul(lib):
+    out = []
+    g = torch.Generator().manual_seed(5)
+    for dtype, tdt in (("f16", torch.float16), ("bf16", torch.bfloat16)):
+        for lay in ("k", "mn"):
+            M, N, K = 40, 33, 200
+            A = torch.randn(M, K, generator=g).to(tdt)
+            Bkn = torch.randn(K, N, generator=g).to(tdt)
+            ref = (A.double() @ Bkn.double()).numpy()
+            refabs = (A.double().abs() @ Bkn.double().abs()).numpy()
+            Ab = A.view(torch.int16).numpy().view(np.uint16)
+            Bb = Bkn.contiguous().view(torch.int16).numpy().view(np.uint16)
+            got, gabs = oracle.gemm_ref(Ab, b_storage(Bb, lay), M, N, K, dtype, lay, lib=lib)
+            lim = 2 * gamma(K) * refabs
+            if np.any(np.abs(got - ref) > lim) or np.any(np.abs(gabs - refabs) > lim):
+                out.append(f"torch_{dtype}_{lay}")
+    return out
+
+
+def _pin_row_subset(lib):
+    out = []
+    rng = np.random.default_rng(3)
+    M, N, K = 21, 10, 17
+    for dtype in ("f16", "bf16"):
+        Ab = random_finite_bits(rng, M * K, dtype).reshape(M, K)
+        Bb = random_finite_bits(rng, K * N, dtype).reshape(N, K)
+        full, fabs_ = oracle.gemm_ref(Ab, Bb, M, N, K, dtype, "k", lib=lib)
+        rows = [20, 0, 7, 7, 13]
+        part, pabs = oracle.gemm_ref(Ab, Bb, M, N, K, dtype, "k", rows=rows, lib=lib)
+        same = (part == full[rows]) | (np.isnan(part) & np.isnan(full[rows]))
+        if not same.all() or not np.array_equal(pabs, fabs_[rows]):
+            out.append(f"rows_{dtype}")
+    return out
+
+
+PINS = [_pin_decoders, _pin_format_fixtures, _pin_hand_gemm, _pin_brute_force,
+        _pin_closed_forms, _pin_integers, _pin_torch_matmul, _pin_row_subset]
+
+
+def pin_battery(lib):
+    failed = []
+    for pin in PINS:
+        try:
+            failed += pin(lib)
+        except Exception as exc:  # a crash in a mutant counts as a caught mistake
+            failed.append(f"{pin.__name__}: {type(exc).__name__}")
+    return failed
+
+
+# ---------------------------------------------------------------- tests
+@pytest.fixture(scope="module")
+def lib():
+    return oracle._load()
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__[5:])
+def test_pin(lib, pin):
+    assert pin(lib) == []
+
+
+def test_argument_errors(lib):
+    import ctypes
+    dp = ctypes.POINTER(ctypes.c_double)
+    a = np.zeros(4, dtype=np.uint16)
+    c = np.zeros(4)
+    args = (a.ctypes.data_as(ctypes.c_void_p), a.ctypes.data_as(ctypes.c_void_p))
+    out = (c.ctypes.data_as(dp), c.ctypes.data_as(dp))
+    assert lib.oracle_gemm(*args, 0, 2, 2, 0, 0, None, 0, *out, 1) == -1       # M = 0
+    assert lib.oracle_gemm(*args, 2, 2, 2, 5, 0, None, 0, *out, 1) == -1       # bad dtype
+    assert lib.oracle_gemm(*args, 2, 2, 2, 0, 9, None, 0, *out, 1) == -1       # bad layout
+    bad_rows = np.array([2], dtype=np.int64)                                     # row >= M
+    assert lib.oracle_gemm(*args, 2, 2, 2, 0, 0, bad_rows.ctypes.data_as(ctypes.c_void_p),
+                           1, *out, 1) == -1
+
+
+def test_threads_do_not_change_bits(lib):
+    rng = np.random.default_rng(9)
+    M, N, K = 37, 29, 64
+    Ab = random_finite_bits(rng, M * K, "f16").reshape(M, K)
+    Bb = random_finite_bits(rng, K * N, "f16").reshape(N, K)
+    c1, a1 = oracle.gemm_ref(Ab, Bb, M, N, K, "f16", "k", threads=1)
+    c8, a8 = oracle.gemm_ref(Ab, Bb, M, N, K, "f16", "k", threads=8)
+    assert np.array_equal(np.nan_to_num(c1), np.nan_to_num(c8)) and np.array_equal(a1, a8)
+
+
+# Each entry plants one plausible mistake in a copy of the oracle's source.
+MUTANTS = {
+    "dropped_term": ("for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = 1; k < K; ++k) {"),
+    "transposed_b": ("j->B[c * j->K + k]", "j->B[k * j->N + c]"),
+    "wrong_sign": ("c[col] += p;", "c[col] -= p;"),
+    "f16_bias": ("e - 25", "e - 24"),
+    "f16_subnormal": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
+    "bf16_bias": ("e - 134", "e - 133"),
+    "bf16_hidden_bit": ("(double)(128 + f)", "(double)(f)"),
+    "abs_dropped": ("cabs[col] += fabs(p);", "cabs[col] += p;"),
+    "row_map_ignored": ("j->rows ? j->rows[r] : r", "r"),
+    "a_index_reversed": ("j->A[i * K + k]", "j->A[i * K + (K - 1 - k)]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistakes(name, tmp_path):
+    src = open(oracle._SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    path = tmp_path / "mutant.c"
+    path.write_text(src.replace(old, new))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+                    "-pthread", "-D_POSIX_C_SOURCE=200809L", "-o", str(so), str(path), "-lm"],
+                   check=True)
+    mutant = oracle.load_library(str(so))
+    assert pin_battery(mutant), f"no pin caught the planted mistake {name}"
+
+
+# ---------------------------------------------------------------- tolerance
+def test_ulp_matches_numpy_spacing():
+    rng = np.random.default_rng(2)
+    # below 2^15, where numpy's next FP16 value is still finite
+    x16 = np.concatenate([rng.uniform(-32000, 32000, 2000), rng.uniform(-1e-4, 1e-4, 2000),
+                          [1.0, 2.0, 2.0 ** -14, 2.0 ** -24]]).astype(np.float16)
+    assert np.array_equal(tolerance.ulp_out(x16.astype(np.float64), "f16"),
+                          np.spacing(np.abs(x16)).astype(np.float64))
+    # in the top binade [2^15, 65504] the spacing is 2^(15-10)
+    assert tolerance.ulp_out(np.array([65504.0, 32768.0]), "f16").tolist() == [32.0, 32.0]
+    x32 = np.concatenate([rng.standard_normal(2000) * 1e3, [1.0, 2.0 ** -126, 2.0 ** -140]]
+                         ).astype(np.float32)
+    assert np.array_equal(tolerance.ulp_out(x32.astype(np.float64), "f32"),
+                          np.spacing(np.abs(x32)).astype(np.float64))
+
+
+def test_ulp_bf16_against_neighbouring_pattern():
+    rng = np.random.default_rng(4)
+    bits = rng.integers(0x0001, 0x7F7F, 3000).astype(np.uint32)
+    x = (bits << 16).view(np.float32).astype(np.float64)
+    nxt = ((bits + 1) << 16).view(np.float32).astype(np.float64)
+    assert np.array_equal(tolerance.ulp_out(x, "bf16"), nxt - x)
+    assert tolerance.ulp_out(np.array([1.0]), "bf16")[0] == 2.0 ** -7
+
+
+def test_check_flags_errors():
+    ref = np.array([[1.0, -2.0], [100.0, 0.0]])
+    cabs = np.array([[1.0, 2.0], [100.0, 0.0]])
+    ok, *_ = tolerance.check(ref, ref, cabs, "f16")
+    assert ok
+    bad = ref.copy()
+    bad[1, 0] += 0.3 + 2e-3 * 100      # beyond 2e-3*C_abs + ulp(100) = 0.2 + 0.0625
+    ok, ratio, n_bad, first = tolerance.check(bad, ref, cabs, "f16")
+    assert not ok and n_bad == 1 and first == (1, 0) and ratio > 1
+    nan = ref.copy()
+    nan[0, 0] = np.nan
+    assert not tolerance.check(nan, ref, cabs, "f32")[0]

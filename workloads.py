@@ -1,0 +1,129 @@
+"""Seeded synthetic inputs for the dense GEMM C = A·B.
+
+This module only draws random operands: it holds none of the GEMM's
+arithmetic, so both the CPU oracle (``oracle/``) and the CUDA path
+(``dense_tiled_gemm_gb300``) can be fed from it without sharing code.
+
+Recipe (the pages fix no generator; this is the plain reading):
+  * one CPU ``torch.Generator`` seeded with the workload's seed;
+  * FP32 draws, A first and then B, each in its own storage order
+    (A: M×K row-major; B K-major: N×K, K contiguous; B MN-major: K×N,
+    N contiguous);
+  * uniform[a, b] = a + (b − a)·rand, normal(0, σ) = σ·randn;
+  * rounded to FP16/BF16 with round-to-nearest-even (``Tensor.to``).
+
+The workloads are the five GEMM shapes the tiled-GEMM pages measure or that
+exercise the method's edge paths (a small 256³ check, the compute-bound
+4096×4096×8192 FP16 shape of "Two Waves, One Stage Apart", §"MI350 Series",
+a BF16 8192³ shape, a ragged 3000×5000×2050 shape with N-contiguous B, and
+a square FP16 sweep).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    dtype_in: str          # "f16" | "bf16"
+    dtype_out: str         # "f16" | "bf16" | "f32"
+    layout_b: str          # "k": B stored N×K (K contiguous); "mn": B stored K×N
+    dist: tuple            # ("uniform", lo, hi) | ("normal", sigma) | ("int", lo, hi)
+    seed: int
+    note: str = field(default="", compare=False)
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+
+def _sweep():
+    out = []
+    for i, n in enumerate((1024, 2048, 4096, 8192, 16384)):
+        out.append(Workload(f"square_f16_{n}", n, n, n, "f16", "f16", "k",
+                            ("normal", 1.0), 4 + i, "square FP16 sweep"))
+    return out
+
+
+WORKLOADS = {w.name: w for w in [
+    Workload("gemm_256_f16_f32", 256, 256, 256, "f16", "f32", "k",
+             ("uniform", -1.0, 1.0), 0, "small check"),
+    Workload("gemm_4096x4096x8192_f16", 4096, 4096, 8192, "f16", "f16", "k",
+             ("normal", 1.0), 1, "compute-bound headline shape"),
+    Workload("gemm_8192_bf16", 8192, 8192, 8192, "bf16", "bf16", "k",
+             ("normal", 1.0 / math.sqrt(8192)), 2, "BF16 square"),
+    Workload("gemm_3000x5000x2050_bf16_f32_bmn", 3000, 5000, 2050, "bf16", "f32", "mn",
+             ("uniform", -2.0, 2.0), 3, "ragged tails, N-contiguous B"),
+] + _sweep()}
+
+HEADLINE = "gemm_4096x4096x8192_f16"
+
+
+def _draw(gen: torch.Generator, n: int, dist: tuple) -> torch.Tensor:
+    kind = dist[0]
+    if kind == "uniform":
+        lo, hi = dist[1], dist[2]
+        return lo + (hi - lo) * torch.rand(n, generator=gen, dtype=torch.float32)
+    if kind == "normal":
+        return dist[1] * torch.randn(n, generator=gen, dtype=torch.float32)
+    if kind == "int":
+        lo, hi = dist[1], dist[2]
+        return torch.randint(lo, hi + 1, (n,), generator=gen).to(torch.float32)
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def b_shape(M: int, N: int, K: int, layout_b: str) -> tuple:
+    """Storage shape of B for a layout: (N, K) when K-major, (K, N) when MN-major."""
+    if layout_b == "k":
+        return (N, K)
+    if layout_b == "mn":
+        return (K, N)
+    raise ValueError(f"layout_b must be 'k' or 'mn', got {layout_b!r}")
+
+
+def make_operands(M: int, N: int, K: int, dtype_in: str, layout_b: str,
+                  dist: tuple, seed: int) -> tuple[torch.Tensor, torch.Tensor]:
+    """Return CPU tensors (A, B) in storage layout, rounded to ``dtype_in``."""
+    gen = torch.Generator().manual_seed(int(seed))
+    dt = DTYPES[dtype_in]
+    A = _draw(gen, M * K, dist).to(dt).reshape(M, K)
+    B = _draw(gen, N * K, dist).to(dt).reshape(b_shape(M, N, K, layout_b))
+    return A, B
+
+
+def workload_operands(w: Workload) -> tuple[torch.Tensor, torch.Tensor]:
+    return make_operands(w.M, w.N, w.K, w.dtype_in, w.layout_b, w.dist, w.seed)
+
+
+def as_bits(t: torch.Tensor):
+    """Raw 16-bit patterns of an FP16/BF16 CPU tensor as a numpy uint16 array."""
+    import numpy as np
+    assert t.dtype in (torch.float16, torch.bfloat16) and t.device.type == "cpu"
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def sample_rows(M: int, count: int, seed: int, tile: int = 128) -> list[int]:
+    """Rows to check at full size: both edges of every ``tile``-row block
+    (up to ``count``), the last row, and seeded random rows."""
+    g = torch.Generator().manual_seed(10_000 + int(seed))
+    rows = {0, M - 1}
+    for b in range(0, M, tile):
+        rows.add(b)
+        rows.add(min(M - 1, b + tile - 1))
+        if len(rows) >= count // 2:
+            break
+    extra = torch.randint(0, M, (count,), generator=g).tolist()
+    for r in extra:
+        if len(rows) >= count:
+            break
+        rows.add(int(r))
+    return sorted(rows)
