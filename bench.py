@@ -1,0 +1,379 @@
+#!/usr/bin/env python
+"""Benchmark of the dense tiled GEMM on GB300.
+
+One step = one GEMM call (the whole hot path) on the 4096 x 4096 x 8192
+FP16-in / FP16-out workload (FP32 accumulation), the compute-bound shape of
+"Two Waves, One Stage Apart" (section "MI350 Series"). Throughput is
+2*M*N*K / elapsed, as in that page's Table 1 caption.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timing: W untimed warm-up steps, then exactly K steps between a barrier and
+torch.cuda.synchronize() on both sides. CUDA events are recorded on the
+launching stream around every launch. Operands rotate over enough
+(A, B, C) sets to exceed twice the L2 size, so every step reads from HBM.
+SM clocks are sampled with nvidia-smi during the timed region.
+Under torchrun (N > 1) every rank runs its own replica; the time is the
+maximum over ranks, and rank 0 prints one JSON line.
+
+--impl reference times the CPU FP64 oracle on this host instead, on a
+bounded sample of rows of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "GEMM TFLOP/s at 4096x4096x8192 FP16 and % of GB300 dense tensor peak"
+PAGES_REFERENCE_TFLOPS = 1437.0   # MI355X, 8-wave warp-pipelined Triton, same shape (context only)
+FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_DENSE_TFLOPS = 2250.0     # GB300 dense FP16/BF16 tensor peak, nominal
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------- helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "dense_tiled_gemm_gb300", "csrc", "*"))):
+        with open(p, "rb") as fh:
+            h.update(os.path.basename(p).encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return json.load(fh), "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now; otherwise None."""
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        with open(path) as fh:
+            text = fh.read()
+        wl = re.search(r"^workload:\s*(\S+)", text, re.M)
+        src = re.search(r"^source_sha256:\s*(\S+)", text, re.M)
+        tr = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        if wl and src and tr and wl.group(1) == workload and src.group(1) == source_hash():
+            return float(tr.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: str):
+        self.gpu = gpu
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        with open(self.tmp.name) as fh:
+            lines = [ln.strip() for ln in fh if ln.strip()]
+        os.unlink(self.tmp.name)
+        sm, sm_max, power, reasons = [], 0.0, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                sm_max = max(sm_max, float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        loaded = [s for s, p in zip(sm, power) if p > 300.0] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": sm_max,
+                "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(loaded),
+                "power_w_max": max(power) if power else None}
+
+
+def oracle_sample(w, rows_total: int, threads: int):
+    """Time the oracle on `rows_total` output rows of workload w (FP64, host cores)."""
+    import oracle
+    A, B = workloads.workload_operands(w)
+    Ab, Bb = workloads.as_bits(A), workloads.as_bits(B)
+    rows = list(range(0, w.M, max(1, w.M // rows_total)))[:rows_total]
+    t0 = time.perf_counter()
+    oracle.gemm_ref(Ab, Bb, w.M, w.N, w.K, w.dtype_in, w.layout_b, rows=rows, threads=threads)
+    return time.perf_counter() - t0, len(rows)
+
+
+def cpu_baseline(w, target_s: float) -> dict:
+    import oracle
+    threads = oracle.host_threads()
+    t1, r1 = oracle_sample(w, threads, threads)            # one row per thread: calibration
+    rows = max(threads, min(w.M, int(r1 * target_s / max(t1, 1e-3))))
+    rows = max(threads, rows // threads * threads)
+    t, r = oracle_sample(w, rows, threads)
+    flops = 2.0 * r * w.N * w.K
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{r} of {w.M} output rows (all {w.N} columns, K={w.K}), FP64 i-k-j loop, "
+                      f"{t:.1f} s wall including the FP64 decode of B",
+            "seconds": t}
+
+
+# ---------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    w = workloads.WORKLOADS[args.workload]
+    threads = oracle.host_threads()
+    A, B = workloads.workload_operands(w)
+    Ab, Bb = workloads.as_bits(A), workloads.as_bits(B)
+    # calibrate: one oracle call with one row per thread
+    t0 = time.perf_counter()
+    oracle.gemm_ref(Ab, Bb, w.M, w.N, w.K, w.dtype_in, w.layout_b, rows=list(range(threads)),
+                    threads=threads)
+    t_cal = time.perf_counter() - t0
+    budget = 150.0   # seconds for the whole warm-up + timed run
+    per_step = budget / max(1, args.steps + args.warmup)
+    rows = max(1, min(4 * threads, int(threads * per_step / max(t_cal, 1e-3))))
+    stride = max(1, w.M // rows)
+    samples = [list(range((s * 7) % stride, w.M, stride))[:rows] for s in range(args.steps + args.warmup)]
+    for s in range(args.warmup):
+        oracle.gemm_ref(Ab, Bb, w.M, w.N, w.K, w.dtype_in, w.layout_b, rows=samples[s], threads=threads)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        oracle.gemm_ref(Ab, Bb, w.M, w.N, w.K, w.dtype_in, w.layout_b,
+                        rows=samples[args.warmup + s], threads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / PAGES_REFERENCE_TFLOPS, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype_in": w.dtype_in,
+                   "dtype_out": w.dtype_out, "layout_b": w.layout_b,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} of {w.M} output rows per step, all {w.N} columns"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- our arm
+def run_ours(args):
+    world, rank, local = dist_env()
+    import dense_tiled_gemm_gb300 as dtg
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    w = workloads.WORKLOADS[args.workload]
+    out_dt = workloads.DTYPES[w.dtype_out]
+    A0, B0 = workloads.workload_operands(w)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = (A0.numel() + B0.numel()) * 2 + w.M * w.N * torch.finfo(out_dt).bits // 8
+    n_sets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+    As, Bs, Cs = [], [], []
+    for i in range(n_sets):
+        As.append(A0.to(dev) if i == 0 else A0.to(dev).roll(i, 0))
+        Bs.append(B0.to(dev) if i == 0 else B0.to(dev).roll(i, 0))
+        Cs.append(torch.empty((w.M, w.N), dtype=out_dt, device=dev))
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        j = i % n_sets
+        dtg.gemm(As[j], Bs[j], Cs[j], layout_b=w.layout_b, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    status, detail = dtg.gemm_last_device_status(stream)
+    if status != dtg.GEMM_OK:
+        raise RuntimeError(f"device status {dtg.gemm_status_string(status)} site {detail:#x}")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    try:
+        smi_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # noqa: BLE001  (older torch: fall back to the CUDA index)
+        smi_id = str(local)
+    sampler = ClockSampler(smi_id)
+    sampler.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = dtg.gemm_launch_count()
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(args.warmup + i)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    launches = dtg.gemm_launch_count() - launches0
+    clocks = sampler.stop()
+    status, detail = dtg.gemm_last_device_status(stream)
+    if status != dtg.GEMM_OK:
+        raise RuntimeError(f"device status {dtg.gemm_status_string(status)} site {detail:#x}")
+
+    region_ms = starts[0].elapsed_time(ends[-1])
+    kernel_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if pg:
+        t = torch.tensor([region_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        region_ms = float(t.item())
+    flops_step = float(w.flops)
+    value = world * flops_step * args.steps / (region_ms * 1e-3) / 1e12
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))  # FP16 and BF16 share the dense rate
+    achieved = flops_step / (kernel_ms * 1e-3) / 1e12
+    plan = dtg.gemm_plan(w.M, w.N, w.K, dtype_in=workloads.DTYPES[w.dtype_in], dtype_out=out_dt,
+                         layout_b=w.layout_b, a_ptr=As[0].data_ptr(), b_ptr=Bs[0].data_ptr(),
+                         c_ptr=Cs[0].data_ptr())
+
+    e2e = None
+    if not args.no_e2e:
+        Ah = A0.pin_memory()
+        Bh = B0.pin_memory()
+        Ch = torch.empty((w.M, w.N), dtype=out_dt).pin_memory()
+        dtg.gemm_from_host(Ah, Bh, Ch, layout_b=w.layout_b, stream=stream)   # grows the workspace
+        n = max(1, args.e2e_steps)
+        if pg:
+            pg.barrier()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            dtg.gemm_from_host(Ah, Bh, Ch, layout_b=w.layout_b, stream=stream)
+        dt = time.perf_counter() - t0
+        if pg:
+            t = torch.tensor([dt], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            dt = float(t.item())
+        dtg.gemm_release_workspace()
+        e2e = {"value": world * flops_step * n / dt / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": (Ah.numel() + Bh.numel()) * 2,
+               "d2h_bytes_per_step": Ch.numel() * Ch.element_size(),
+               "steps": n, "api": "gemm_from_host (pinned host buffers, synchronous)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": region_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": value / world / PAGES_REFERENCE_TFLOPS if w.name == workloads.HEADLINE else None,
+            "vs_baseline_ref": "1437 TFLOP/s: MI355X 8-wave warp-pipelined Triton, same shape (context)",
+            "dtype": "f16" if w.dtype_in == "f16" else "bf16", "accumulate": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype_in": w.dtype_in,
+                       "dtype_out": w.dtype_out, "layout_b": w.layout_b,
+                       "l2": f"rotating {n_sets} operand sets "
+                             f"({n_sets * set_bytes / 1e6:.0f} MB > 2 x {l2 / 1e6:.0f} MB L2)",
+                       "parallelism": f"replicas x{world}", "plan": plan},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                         "peak_source": f"{peak_src} bf16_tflops (burst); FP16 dense rate = BF16",
+                         "kernel_ms": kernel_ms},
+            "clocks": clocks,
+            "gpu_launches": launches,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        line["roofline"]["frac_of_nominal"] = achieved / NOMINAL_DENSE_TFLOPS
+        if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+            line["roofline"]["frac_of_nominal_at_measured_clock"] = achieved / (
+                NOMINAL_DENSE_TFLOPS * clocks["sm_mhz"] / clocks["sm_max_mhz"])
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,164 @@
+"""Dense tiled GEMM for GB300 (sm_103a): C = A·B with FP16/BF16 operands,
+FP32 accumulation and a cast-on-store epilogue.
+
+Every function here has the name of a C-ABI entry point in include/gemm.h and
+only marshals arguments: torch tensors become device pointers and sizes, and
+torch's current stream is passed as the CUDA stream. The GEMM runs in the
+library's own kernels (``libdtgemm.so``). Importing this package fails when
+that library is not built, and every error status is raised as GemmError.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import binding
+from .binding import (GEMM_BF16, GEMM_F16, GEMM_F32, GEMM_K_MAJOR, GEMM_MN_MAJOR, GEMM_OK,
+                      GEMM_ERR_TIMEOUT, GemmError, GemmOptions, GemmPlan, STATUS_NAMES)
+
+__all__ = ["gemm", "gemm_ex", "gemm_plan", "gemm_from_host", "gemm_release_workspace",
+           "gemm_last_device_status", "gemm_selftest_wait_timeout", "gemm_status_string",
+           "gemm_launch_count", "GemmError", "GemmOptions", "GemmPlan"]
+
+_DT_IN = {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16}
+_DT_OUT = {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16, torch.float32: GEMM_F32}
+_LAYOUT = {"k": GEMM_K_MAJOR, "mn": GEMM_MN_MAJOR}
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _options(options) -> GemmOptions | None:
+    if options is None or isinstance(options, GemmOptions):
+        return options
+    o = GemmOptions()
+    for key, val in dict(options).items():
+        setattr(o, key, int(val))
+    return o
+
+
+def _shapes(A: torch.Tensor, B: torch.Tensor, layout_b: str):
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D")
+    M, K = A.shape
+    if layout_b == "k":
+        N, Kb = B.shape
+    elif layout_b == "mn":
+        Kb, N = B.shape
+    else:
+        raise ValueError("layout_b must be 'k' (B is N x K) or 'mn' (B is K x N)")
+    if Kb != K:
+        raise ValueError(f"K mismatch: A has {K}, B has {Kb}")
+    return int(M), int(N), int(K)
+
+
+def _check(status: int, what: str):
+    if status != GEMM_OK:
+        raise GemmError(status, what)
+
+
+def _prepare(A, B, C, layout_b, out_dtype, device_kind):
+    for name, t in (("A", A), ("B", B)):
+        if t.dtype not in _DT_IN:
+            raise TypeError(f"{name} must be float16 or bfloat16, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device.type != device_kind:
+            raise ValueError(f"{name} must be a {device_kind} tensor")
+    if A.dtype != B.dtype:
+        raise TypeError("A and B must have the same dtype")
+    M, N, K = _shapes(A, B, layout_b)
+    if C is None:
+        C = torch.empty((M, N), dtype=out_dtype or A.dtype, device=A.device,
+                        pin_memory=(device_kind == "cpu" and torch.cuda.is_available()))
+    if C.dtype not in _DT_OUT or tuple(C.shape) != (M, N) or not C.is_contiguous():
+        raise ValueError("C must be a contiguous (M, N) float16/bfloat16/float32 tensor")
+    if C.device.type != device_kind:
+        raise ValueError(f"C must be a {device_kind} tensor")
+    return M, N, K, C
+
+
+def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *,
+         layout_b: str = "k", out_dtype: torch.dtype | None = None, stream=None,
+         options=None) -> torch.Tensor:
+    """C = A·B on A's CUDA device, asynchronously on ``stream`` (default: torch's current).
+
+    A: (M, K). B: (N, K) for layout_b="k", (K, N) for layout_b="mn".
+    C: (M, N) of ``out_dtype`` (default A.dtype), allocated when not given.
+    ``options``: dict or GemmOptions of gemm_ex overrides.
+    """
+    M, N, K, C = _prepare(A, B, C, layout_b, out_dtype, "cuda")
+    opts = _options(options)
+    args = (A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _DT_IN[A.dtype],
+            _DT_OUT[C.dtype], GEMM_K_MAJOR, _LAYOUT[layout_b])
+    with torch.cuda.device(A.device):
+        if opts is None:
+            _check(binding.lib.gemm(*args, _stream_ptr(stream)), "gemm")
+        else:
+            _check(binding.lib.gemm_ex(*args, ctypes.byref(opts), _stream_ptr(stream)), "gemm_ex")
+    return C
+
+
+def gemm_ex(A, B, C=None, *, options=None, **kw) -> torch.Tensor:
+    """gemm with gemm_ex overrides (cta_group, block_n, max_clusters, group_m, timeout_ms)."""
+    return gemm(A, B, C, options=options if options is not None else GemmOptions(), **kw)
+
+
+def gemm_plan(M: int, N: int, K: int, *, dtype_in=torch.float16, dtype_out=torch.float16,
+              layout_b: str = "k", a_ptr: int = 256, b_ptr: int = 256, c_ptr: int = 256,
+              options=None, device=None) -> dict:
+    """The launch gemm_ex would make (tile, grid, realign/direct-store paths), as a dict.
+    The pointers only matter for their alignment."""
+    plan = GemmPlan()
+    opts = _options(options)
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _check(binding.lib.gemm_plan(M, N, K, _DT_IN[dtype_in], _DT_OUT[dtype_out], GEMM_K_MAJOR,
+                                     _LAYOUT[layout_b], a_ptr, b_ptr, c_ptr,
+                                     ctypes.byref(opts) if opts is not None else None,
+                                     ctypes.byref(plan)), "gemm_plan")
+    return plan.as_dict()
+
+
+def gemm_from_host(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *,
+                   layout_b: str = "k", out_dtype: torch.dtype | None = None, stream=None,
+                   device=None) -> torch.Tensor:
+    """C = A·B with host (CPU) tensors; copies in, computes and copies out on the current
+    CUDA device, and returns when C is complete."""
+    M, N, K, C = _prepare(A, B, C, layout_b, out_dtype, "cpu")
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _check(binding.lib.gemm_from_host(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                                          _DT_IN[A.dtype], _DT_OUT[C.dtype], GEMM_K_MAJOR,
+                                          _LAYOUT[layout_b], _stream_ptr(stream)),
+               "gemm_from_host")
+    return C
+
+
+def gemm_release_workspace() -> None:
+    _check(binding.lib.gemm_release_workspace(), "gemm_release_workspace")
+
+
+def gemm_last_device_status(stream=None) -> tuple[int, int]:
+    """Synchronise the stream, then read and clear the device status word.
+    Returns (status, detail); status GEMM_ERR_TIMEOUT means a kernel wait timed out."""
+    detail = ctypes.c_uint32(0)
+    st = binding.lib.gemm_last_device_status(_stream_ptr(stream), ctypes.byref(detail))
+    return int(st), int(detail.value)
+
+
+def gemm_selftest_wait_timeout(timeout_ms: int = 50, stream=None) -> None:
+    _check(binding.lib.gemm_selftest_wait_timeout(int(timeout_ms), _stream_ptr(stream)),
+           "gemm_selftest_wait_timeout")
+
+
+def gemm_status_string(status: int) -> str:
+    return binding.lib.gemm_status_string(int(status)).decode()
+
+
+def gemm_launch_count() -> int:
+    return int(binding.lib.gemm_launch_count())

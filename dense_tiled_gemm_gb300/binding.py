@@ -1,0 +1,86 @@
+"""ctypes binding to libdtgemm.so (the C ABI in include/gemm.h).
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels. There is no fallback of any kind. If the library is missing, the
+import fails; if it returns an error, a GemmError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+GEMM_F16, GEMM_BF16, GEMM_F32 = 0, 1, 2
+GEMM_K_MAJOR, GEMM_MN_MAJOR = 0, 1
+STATUS_NAMES = {
+    0: "GEMM_OK",
+    1: "GEMM_ERR_INVALID_ARG",
+    2: "GEMM_ERR_UNSUPPORTED",
+    3: "GEMM_ERR_CUDA",
+    4: "GEMM_ERR_TIMEOUT",
+    5: "GEMM_ERR_NO_DEVICE",
+    6: "GEMM_ERR_OUT_OF_MEMORY",
+}
+GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_CUDA = 0, 1, 2, 3
+GEMM_ERR_TIMEOUT, GEMM_ERR_NO_DEVICE, GEMM_ERR_OUT_OF_MEMORY = 4, 5, 6
+
+
+class GemmOptions(ctypes.Structure):
+    _fields_ = [("cta_group", ctypes.c_int32), ("block_n", ctypes.c_int32),
+                ("max_clusters", ctypes.c_int32), ("group_m", ctypes.c_int32),
+                ("timeout_ms", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+
+
+class GemmPlan(ctypes.Structure):
+    _fields_ = [("cta_group", ctypes.c_int32), ("block_m", ctypes.c_int32),
+                ("block_n", ctypes.c_int32), ("block_k", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("num_tiles", ctypes.c_int32),
+                ("grid_ctas", ctypes.c_int32), ("group_m", ctypes.c_int32),
+                ("realign_a", ctypes.c_int32), ("realign_b", ctypes.c_int32),
+                ("direct_store", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        super().__init__(f"{what}: {STATUS_NAMES.get(self.status, self.status)}")
+
+
+def _declare(lib):
+    vp, i64, i32, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+    gemm_args = [vp, vp, vp, i64, i64, i64, c_int, c_int, c_int, c_int]
+    lib.gemm.restype = c_int
+    lib.gemm.argtypes = gemm_args + [vp]
+    lib.gemm_ex.restype = c_int
+    lib.gemm_ex.argtypes = gemm_args + [ctypes.POINTER(GemmOptions), vp]
+    lib.gemm_plan.restype = c_int
+    lib.gemm_plan.argtypes = [i64, i64, i64, c_int, c_int, c_int, c_int, vp, vp, vp,
+                              ctypes.POINTER(GemmOptions), ctypes.POINTER(GemmPlan)]
+    lib.gemm_from_host.restype = c_int
+    lib.gemm_from_host.argtypes = gemm_args + [vp]
+    lib.gemm_release_workspace.restype = c_int
+    lib.gemm_release_workspace.argtypes = []
+    lib.gemm_last_device_status.restype = c_int
+    lib.gemm_last_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.gemm_selftest_wait_timeout.restype = c_int
+    lib.gemm_selftest_wait_timeout.argtypes = [i32, vp]
+    lib.gemm_status_string.restype = ctypes.c_char_p
+    lib.gemm_status_string.argtypes = [c_int]
+    lib.gemm_launch_count.restype = ctypes.c_uint64
+    lib.gemm_launch_count.argtypes = []
+    return lib
+
+
+def load(path: str = LIB_PATH):
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built; call dense_tiled_gemm_gb300.build.build() "
+                          "(needs nvcc) before importing the package")
+    return _declare(ctypes.CDLL(path))
+
+
+lib = load()

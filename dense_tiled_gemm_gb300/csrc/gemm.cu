@@ -1,0 +1,567 @@
+// gemm.cu: host side of the C ABI declared in gemm.h.
+//
+// One call validates its arguments, picks a tile plan, builds three TMA
+// tensor maps (A, B, C), optionally re-pitches an operand that the TMA engine
+// cannot describe, and launches one persistent kernel on the caller's
+// stream. Nothing is allocated per call on the common path. The launcher of
+// "Porting High-Performance HIP Kernels to FlyDSL" (section "Structure of a
+// FlyDSL Kernel") is the model for the interface: prebuilt code, caller's
+// stream, no stream created per call.
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cstring>
+#include <mutex>
+
+#include "gemm.h"
+#include "gemm_kernel.cuh"
+
+using namespace dtg;
+
+// Device status word of this library, one copy per device:
+// [0] id of the first launch that timed out since the host last read it,
+// [1] the wait site of the latest timeout, [2] id of the latest timed-out launch.
+static __device__ unsigned long long g_status[4];
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+constexpr uint64_t DEFAULT_TIMEOUT_MS = 2000;
+
+struct Variant {
+    int cg;
+    int bn;
+    int stages;
+    int smem;
+    const void *fn;
+    bool b_mn_ok;   // MN-major B needs 64-column TMA boxes per CTA
+};
+
+const Variant kVariants[] = {
+    {2, 256, TileConfig<2, 256>::STAGES, TileConfig<2, 256>::SMEM_BYTES,
+     reinterpret_cast<const void *>(&gemm_tcgen05_kernel<2, 256>), true},
+    {2, 224, TileConfig<2, 224>::STAGES, TileConfig<2, 224>::SMEM_BYTES,
+     reinterpret_cast<const void *>(&gemm_tcgen05_kernel<2, 224>), false},
+    {1, 256, TileConfig<1, 256>::STAGES, TileConfig<1, 256>::SMEM_BYTES,
+     reinterpret_cast<const void *>(&gemm_tcgen05_kernel<1, 256>), true},
+};
+constexpr int NUM_VARIANTS = sizeof(kVariants) / sizeof(kVariants[0]);
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    unsigned long long *status = nullptr;
+    int max_units[NUM_VARIANTS] = {};   // co-resident CTAs (cg 1) or CTA pairs (cg 2)
+    std::mutex ws_mu;
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[MAX_DEVICES];
+std::atomic<uint64_t> g_launches{0};
+std::atomic<unsigned long long> g_next_id{1};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int esize(int dtype) { return dtype == GEMM_F32 ? 4 : 2; }
+
+gemm_status_t device_state(DeviceState **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_NO_DEVICE;
+        }
+        if (major != 10 || minor != 3)   // the library holds sm_103a code only
+            return GEMM_ERR_NO_DEVICE;
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        void *status = nullptr;
+        if (cudaGetSymbolAddress(&status, g_status) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        d.status = static_cast<unsigned long long *>(status);
+        for (int v = 0; v < NUM_VARIANTS; ++v) {
+            const Variant &var = kVariants[v];
+            if (cudaFuncSetAttribute(var.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, var.smem) !=
+                cudaSuccess)
+                return GEMM_ERR_CUDA;
+            if (var.cg == 1) {
+                int per_sm = 0;
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, var.fn, NUM_THREADS,
+                                                                  var.smem) != cudaSuccess)
+                    return GEMM_ERR_CUDA;
+                d.max_units[v] = per_sm * d.sms;
+            } else {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(2 * d.sms);
+                cfg.blockDim = dim3(NUM_THREADS);
+                cfg.dynamicSmemBytes = var.smem;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 2;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                int clusters = 0;
+                if (cudaOccupancyMaxActiveClusters(&clusters, var.fn, &cfg) != cudaSuccess)
+                    return GEMM_ERR_CUDA;
+                d.max_units[v] = clusters;
+            }
+        }
+        if (!g_encode) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                                 &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return GEMM_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return GEMM_OK;
+}
+
+gemm_status_t validate(const void *A, const void *B, const void *C, int64_t M, int64_t N, int64_t K,
+                       int dtype_in, int dtype_out, int layoutA, int layoutB, const gemm_options_t *o)
+{
+    if (!A || !B || !C)
+        return GEMM_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 1 || M > INT_MAX || N > INT_MAX || K > INT_MAX)
+        return GEMM_ERR_INVALID_ARG;
+    if (dtype_in != GEMM_F16 && dtype_in != GEMM_BF16)
+        return dtype_in == GEMM_F32 ? GEMM_ERR_UNSUPPORTED : GEMM_ERR_INVALID_ARG;
+    if (dtype_out != GEMM_F16 && dtype_out != GEMM_BF16 && dtype_out != GEMM_F32)
+        return GEMM_ERR_INVALID_ARG;
+    if (layoutA != GEMM_K_MAJOR && layoutA != GEMM_MN_MAJOR)
+        return GEMM_ERR_INVALID_ARG;
+    if (layoutA == GEMM_MN_MAJOR)
+        return GEMM_ERR_UNSUPPORTED;
+    if (layoutB != GEMM_K_MAJOR && layoutB != GEMM_MN_MAJOR)
+        return GEMM_ERR_INVALID_ARG;
+    if (o) {
+        if (o->cta_group < 0 || o->cta_group > 2 || o->max_clusters < 0 || o->group_m < 0 ||
+            o->timeout_ms < 0 || o->block_n < 0)
+            return GEMM_ERR_INVALID_ARG;
+        if (o->block_n != 0 && o->block_n != 224 && o->block_n != 256)
+            return GEMM_ERR_UNSUPPORTED;
+    }
+    return GEMM_OK;
+}
+
+struct Plan {
+    int variant;
+    int num_m, num_n, num_tiles, num_kb;
+    int grid_ctas;
+    int group_m;
+    bool realign_a, realign_b, direct_store;
+};
+
+bool misaligned(const void *p, int64_t row_elems, int elem_bytes)
+{
+    return (reinterpret_cast<uintptr_t>(p) % 16) != 0 || (row_elems * elem_bytes) % 16 != 0;
+}
+
+// Choose the tile shape with the fewest output columns per SM over the whole
+// problem: waves = ceil(tiles / co-resident units), cost = waves x block_n.
+// Single-CTA tiles pay ~15% for their higher shared-memory read rate per flop.
+gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, int dtype_out,
+                        int layoutB, const void *A, const void *B, const void *C,
+                        const gemm_options_t *o, Plan *pl)
+{
+    const bool b_mn = layoutB == GEMM_MN_MAJOR;
+    int best = -1;
+    double best_cost = 0;
+    for (int v = 0; v < NUM_VARIANTS; ++v) {
+        const Variant &var = kVariants[v];
+        if (o && o->cta_group && o->cta_group != var.cg)
+            continue;
+        if (o && o->block_n && o->block_n != var.bn)
+            continue;
+        if (b_mn && !var.b_mn_ok)
+            continue;
+        int units = d.max_units[v];
+        if (o && o->max_clusters)
+            units = std::min(units, static_cast<int>(o->max_clusters));
+        if (units < 1)
+            continue;
+        const int64_t tiles = ((M + 128 * var.cg - 1) / (128 * var.cg)) * ((N + var.bn - 1) / var.bn);
+        const int64_t waves = (tiles + units - 1) / units;
+        const double cost = static_cast<double>(waves) * var.bn * (var.cg == 1 ? 1.15 : 1.0);
+        if (best < 0 || cost < best_cost) {
+            best = v;
+            best_cost = cost;
+        }
+    }
+    if (best < 0)
+        return GEMM_ERR_UNSUPPORTED;
+    const Variant &var = kVariants[best];
+    int units = d.max_units[best];
+    if (o && o->max_clusters)
+        units = std::min(units, static_cast<int>(o->max_clusters));
+    pl->variant = best;
+    pl->num_m = static_cast<int>((M + 128 * var.cg - 1) / (128 * var.cg));
+    pl->num_n = static_cast<int>((N + var.bn - 1) / var.bn);
+    const int64_t tiles = static_cast<int64_t>(pl->num_m) * pl->num_n;
+    if (tiles > INT_MAX)
+        return GEMM_ERR_UNSUPPORTED;
+    pl->num_tiles = static_cast<int>(tiles);
+    pl->num_kb = static_cast<int>((K + BLOCK_K - 1) / BLOCK_K);
+    pl->grid_ctas = static_cast<int>(std::min<int64_t>(tiles, units)) * var.cg;
+    pl->group_m = (o && o->group_m) ? o->group_m : 8;
+    pl->realign_a = misaligned(A, K, 2);
+    pl->realign_b = misaligned(B, b_mn ? N : K, 2);
+    pl->direct_store = misaligned(C, N, esize(dtype_out));
+    return GEMM_OK;
+}
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swizzle)
+{
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estride[2] = {1, 1};
+    return g_encode(map, dt, 2, const_cast<void *>(base), dims, strides, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+CUtensorMapDataType tma_dtype(int dtype)
+{
+    switch (dtype) {
+    case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    case GEMM_F32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    }
+}
+
+// Copy a rows x cols 16-bit matrix into stream-ordered scratch with a row
+// pitch padded to 8 elements (16 bytes). The pad is never read: the tensor
+// map keeps the logical width `cols`, and TMA zero-fills past it.
+gemm_status_t realign(const void *src, int64_t rows, int64_t cols, int sms, cudaStream_t st,
+                      void **out, int64_t *ld_out)
+{
+    const int64_t ld = (cols + 7) / 8 * 8;
+    if (cudaMallocAsync(out, static_cast<size_t>(rows * ld * 2), st) != cudaSuccess) {
+        cudaGetLastError();
+        *out = nullptr;
+        return GEMM_ERR_OUT_OF_MEMORY;
+    }
+    const int64_t total = rows * cols;
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(sms) * 8);
+    realign_rows_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(
+        static_cast<const uint16_t *>(src), static_cast<uint16_t *>(*out), rows, cols, ld);
+    if (cudaGetLastError() != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    *ld_out = ld;
+    return GEMM_OK;
+}
+
+template <int CG, int BN>
+cudaError_t launch_variant(int grid_ctas, const CUtensorMap &ta, const CUtensorMap &tb,
+                           const CUtensorMap &tc, const KernelParams &kp, cudaStream_t st)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas));
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = TileConfig<CG, BN>::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (CG == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<CG, BN>, ta, tb, tc, kp);
+}
+
+gemm_status_t run(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                  int dtype_in, int dtype_out, int layoutA, int layoutB, const gemm_options_t *opts,
+                  cudaStream_t st)
+{
+    gemm_status_t rc = validate(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, opts);
+    if (rc != GEMM_OK)
+        return rc;
+    DeviceState *d = nullptr;
+    if ((rc = device_state(&d)) != GEMM_OK)
+        return rc;
+    Plan pl;
+    if ((rc = make_plan(*d, M, N, K, dtype_out, layoutB, A, B, C, opts, &pl)) != GEMM_OK)
+        return rc;
+    const Variant &var = kVariants[pl.variant];
+    const bool b_mn = layoutB == GEMM_MN_MAJOR;
+
+    const void *a_ptr = A, *b_ptr = B;
+    int64_t lda = K, ldb = b_mn ? N : K;
+    void *a_tmp = nullptr, *b_tmp = nullptr;
+    auto release = [&]() {
+        if (a_tmp)
+            cudaFreeAsync(a_tmp, st);
+        if (b_tmp)
+            cudaFreeAsync(b_tmp, st);
+    };
+    if (pl.realign_a && (rc = realign(A, M, K, d->sms, st, &a_tmp, &lda)) != GEMM_OK) {
+        release();
+        return rc;
+    }
+    if (a_tmp)
+        a_ptr = a_tmp;
+    if (pl.realign_b && (rc = realign(B, b_mn ? K : N, b_mn ? N : K, d->sms, st, &b_tmp, &ldb)) != GEMM_OK) {
+        release();
+        return rc;
+    }
+    if (b_tmp)
+        b_ptr = b_tmp;
+
+    alignas(64) CUtensorMap ta, tb, tc;
+    std::memset(&tc, 0, sizeof(tc));
+    const CUtensorMapDataType in_dt = tma_dtype(dtype_in);
+    bool ok = encode_2d(&ta, in_dt, a_ptr, K, M, lda * 2, BLOCK_K, BLOCK_M_CTA, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!b_mn)
+        ok = ok && encode_2d(&tb, in_dt, b_ptr, K, N, ldb * 2, BLOCK_K, var.bn / var.cg,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        ok = ok && encode_2d(&tb, in_dt, b_ptr, N, K, ldb * 2, 64, BLOCK_K, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!pl.direct_store)
+        ok = ok && encode_2d(&tc, tma_dtype(dtype_out), C, N, M, N * esize(dtype_out), EPI_COLS, 32,
+                             dtype_out == GEMM_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!ok) {
+        release();
+        return GEMM_ERR_CUDA;
+    }
+
+    KernelParams kp = {};
+    kp.M = static_cast<int32_t>(M);
+    kp.N = static_cast<int32_t>(N);
+    kp.K = static_cast<int32_t>(K);
+    kp.num_m_tiles = pl.num_m;
+    kp.num_n_tiles = pl.num_n;
+    kp.num_tiles = pl.num_tiles;
+    kp.num_k_blocks = pl.num_kb;
+    kp.group_m = pl.group_m;
+    kp.idesc = make_idesc_f16(128u * var.cg, static_cast<uint32_t>(var.bn), dtype_in == GEMM_BF16 ? 1u : 0u,
+                              b_mn ? 1u : 0u);
+    kp.out_dtype = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_BF16 ? OUT_BF16 : OUT_F16);
+    kp.b_mn_major = b_mn ? 1u : 0u;
+    kp.direct_store = pl.direct_store ? 1u : 0u;
+    kp.C = C;
+    kp.timeout_ns = (opts && opts->timeout_ms ? static_cast<uint64_t>(opts->timeout_ms) : DEFAULT_TIMEOUT_MS) *
+                    1000000ull;
+    kp.launch_id = g_next_id.fetch_add(1, std::memory_order_relaxed);
+    kp.status = d->status;
+
+    cudaError_t err;
+    if (var.cg == 2 && var.bn == 256)
+        err = launch_variant<2, 256>(pl.grid_ctas, ta, tb, tc, kp, st);
+    else if (var.cg == 2 && var.bn == 224)
+        err = launch_variant<2, 224>(pl.grid_ctas, ta, tb, tc, kp, st);
+    else
+        err = launch_variant<1, 256>(pl.grid_ctas, ta, tb, tc, kp, st);
+    release();
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return GEMM_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+gemm_status_t gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int dtype_in,
+                   int dtype_out, int layoutA, int layoutB, void *stream)
+{
+    return run(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, nullptr,
+               static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_ex(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                      int dtype_in, int dtype_out, int layoutA, int layoutB, const gemm_options_t *opts,
+                      void *stream)
+{
+    return run(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, opts,
+               static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA,
+                        int layoutB, const void *A, const void *B, const void *C,
+                        const gemm_options_t *opts, gemm_plan_t *plan)
+{
+    if (!plan)
+        return GEMM_ERR_INVALID_ARG;
+    gemm_status_t rc = validate(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, opts);
+    if (rc != GEMM_OK)
+        return rc;
+    DeviceState *d = nullptr;
+    if ((rc = device_state(&d)) != GEMM_OK)
+        return rc;
+    Plan pl;
+    if ((rc = make_plan(*d, M, N, K, dtype_out, layoutB, A, B, C, opts, &pl)) != GEMM_OK)
+        return rc;
+    const Variant &var = kVariants[pl.variant];
+    std::memset(plan, 0, sizeof(*plan));
+    plan->cta_group = var.cg;
+    plan->block_m = 128 * var.cg;
+    plan->block_n = var.bn;
+    plan->block_k = BLOCK_K;
+    plan->stages = var.stages;
+    plan->num_tiles = pl.num_tiles;
+    plan->grid_ctas = pl.grid_ctas;
+    plan->group_m = pl.group_m;
+    plan->realign_a = pl.realign_a;
+    plan->realign_b = pl.realign_b;
+    plan->direct_store = pl.direct_store;
+    plan->smem_bytes = var.smem;
+    plan->num_sms = d->sms;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_host, int64_t M, int64_t N,
+                             int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB, void *stream)
+{
+    gemm_status_t rc = validate(A_host, B_host, C_host, M, N, K, dtype_in, dtype_out, layoutA, layoutB,
+                                nullptr);
+    if (rc != GEMM_OK)
+        return rc;
+    DeviceState *d = nullptr;
+    if ((rc = device_state(&d)) != GEMM_OK)
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto up256 = [](size_t x) { return (x + 255) / 256 * 256; };
+    const size_t a_bytes = static_cast<size_t>(M * K * 2), b_bytes = static_cast<size_t>(N * K * 2);
+    const size_t c_bytes = static_cast<size_t>(M * N * esize(dtype_out));
+    const size_t need = up256(a_bytes) + up256(b_bytes) + up256(c_bytes);
+    std::lock_guard<std::mutex> lock(d->ws_mu);
+    if (d->ws_bytes < need) {
+        if (d->ws) {
+            cudaFree(d->ws);   // synchronises the device
+            d->ws = nullptr;
+            d->ws_bytes = 0;
+        }
+        if (cudaMalloc(&d->ws, need) != cudaSuccess) {
+            cudaGetLastError();
+            d->ws = nullptr;
+            return GEMM_ERR_OUT_OF_MEMORY;
+        }
+        d->ws_bytes = need;
+    }
+    char *dA = static_cast<char *>(d->ws);
+    char *dB = dA + up256(a_bytes);
+    char *dC = dB + up256(b_bytes);
+    if (cudaMemcpyAsync(dA, A_host, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(dB, B_host, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    rc = run(dA, dB, dC, M, N, K, dtype_in, dtype_out, layoutA, layoutB, nullptr, st);
+    if (rc != GEMM_OK)
+        return rc;
+    if (cudaMemcpyAsync(C_host, dC, c_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_release_workspace(void)
+{
+    DeviceState *d = nullptr;
+    gemm_status_t rc = device_state(&d);
+    if (rc != GEMM_OK)
+        return rc;
+    std::lock_guard<std::mutex> lock(d->ws_mu);
+    if (d->ws) {
+        if (cudaFree(d->ws) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        d->ws = nullptr;
+        d->ws_bytes = 0;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_last_device_status(void *stream, uint32_t *detail)
+{
+    if (detail)
+        *detail = 0;
+    DeviceState *d = nullptr;
+    gemm_status_t rc = device_state(&d);
+    if (rc != GEMM_OK)
+        return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    unsigned long long h[4] = {0, 0, 0, 0};
+    if (cudaMemcpyFromSymbol(h, g_status, sizeof(h)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (h[0] == 0)
+        return GEMM_OK;
+    const unsigned long long zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpyToSymbol(g_status, zero, sizeof(zero)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (detail)
+        *detail = static_cast<uint32_t>(h[1]);
+    return GEMM_ERR_TIMEOUT;
+}
+
+gemm_status_t gemm_selftest_wait_timeout(int32_t timeout_ms, void *stream)
+{
+    if (timeout_ms < 1 || timeout_ms > 10000)
+        return GEMM_ERR_INVALID_ARG;
+    DeviceState *d = nullptr;
+    gemm_status_t rc = device_state(&d);
+    if (rc != GEMM_OK)
+        return rc;
+    wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint64_t>(timeout_ms) * 1000000ull, g_next_id.fetch_add(1), d->status);
+    if (cudaGetLastError() != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+const char *gemm_status_string(int status)
+{
+    switch (status) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE";
+    case GEMM_ERR_OUT_OF_MEMORY: return "GEMM_ERR_OUT_OF_MEMORY";
+    default: return "GEMM_ERR_UNKNOWN";
+    }
+}
+
+uint64_t gemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+} // extern "C"

@@ -1,0 +1,536 @@
+// gemm_kernel.cuh: the persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// C = A·B with FP16/BF16 operands, an FP32 accumulator in tensor memory (TMEM)
+// and a cast on store. "Two Waves, One Stage Apart" (sections "Why the Matrix
+// Pipeline Drains" and "Two Waves, One Stage Apart") keeps the matrix unit
+// busy by holding data preparation one stage ahead of matrix work. Here that
+// offset comes from fixed warp roles linked by shared-memory barriers, not
+// from two wave groups taking turns:
+//
+//   warp 0     producer: one thread issues TMA loads of A and B k-blocks into
+//              a ring of STAGES shared-memory slots;
+//   warp 1     MMA issuer: one thread issues tcgen05.mma on each filled slot
+//              and frees it with tcgen05.commit; the warp owns the TMEM
+//              allocation;
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator, FP32 -> output cast,
+//              swizzled staging in shared memory, TMA store.
+//
+// The dependency rule of that page's section "Dependencies Cross Groups and
+// Iterations" (writes complete before the reader starts, reads finish before
+// a slot is refilled) maps onto a full/empty barrier pair per ring slot, and
+// a full/empty pair per TMEM accumulator. The page's section "Avoiding
+// Unnecessary Waits" asks for one barrier per independent buffer, so that no
+// false wait delays matrix work; each slot has its own pair here.
+//
+// Two accumulators of up to 256 FP32 columns each (TMEM columns 0 and 256)
+// let the epilogue of one tile run under the main loop of the next. With
+// CG = 2 a cluster of two CTAs shares each 256-row tile (tcgen05 cta_group::2):
+// each CTA loads its own 128 rows of A and its half of B, and the even CTA
+// issues the MMAs for both.
+//
+// Tails: TMA loads fill out-of-range rows/columns (ragged M, N and the last
+// k-block of K) with zeros, and TMA stores clip at the matrix edge. The
+// "Porting High-Performance HIP Kernels to FlyDSL" page (section "Buffer
+// Resource Descriptors") relies on hardware range checks in the same way.
+//
+// Every wait is bounded (WaitCtx). Past the limit, a thread records the site
+// in the library's device status word and skips the remaining work. It
+// keeps the kernel's control flow, so every CTA barrier is still reached and
+// the kernel returns instead of hanging.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace dtg {
+
+constexpr int BLOCK_K = 64;          // 64 x 16-bit = one 128-byte swizzle row
+constexpr int BLOCK_M_CTA = 128;     // accumulator rows per CTA = TMEM lanes
+constexpr int UMMA_K = 16;           // K of one kind::f16 tcgen05.mma
+constexpr int NUM_THREADS = 192;     // producer warp, MMA warp, 4 epilogue warps
+constexpr int EPI_WARP0 = 2;
+constexpr int TMEM_COLS = 512;       // two accumulators at columns 0 and 256
+constexpr int ACC_STRIDE = 256;
+constexpr int EPI_COLS = 32;         // accumulator columns per epilogue chunk
+constexpr int STAGING_BYTES = 32 * 128;  // one chunk: 32 rows x up to 128 bytes
+
+enum : uint32_t { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 2 };
+
+// Wait sites reported in the status detail: role << 8 | barrier kind.
+enum : uint32_t {
+    SITE_PRODUCER_EMPTY = 0x001,
+    SITE_PRODUCER_DRAIN = 0x002,
+    SITE_MMA_TMEM_EMPTY = 0x103,
+    SITE_MMA_FULL = 0x104,
+    SITE_MMA_DONE = 0x105,
+    SITE_EPI_TMEM_FULL = 0x206,
+    SITE_SELFTEST = 0x307,
+};
+
+struct KernelParams {
+    int32_t M, N, K;
+    int32_t num_m_tiles, num_n_tiles, num_tiles, num_k_blocks, group_m;
+    uint32_t idesc;
+    uint32_t out_dtype;
+    uint32_t b_mn_major;
+    uint32_t direct_store;     // 1: write C with ordinary stores (unaligned C)
+    void *C;                   // used by the direct-store path
+    uint64_t timeout_ns;       // per-wait limit
+    unsigned long long launch_id;
+    unsigned long long *status;  // [0] first timed-out launch, [1] site, [2] last timed-out launch
+};
+
+template <int CG, int BN>
+struct TileConfig {
+    static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
+    static constexpr int BN_CTA = BN / CG;   // B rows (K-major) or columns (MN-major) per CTA
+    static_assert(BN % (16 * CG) == 0 && BN <= 256 && BN_CTA % 8 == 0, "invalid tile width");
+    static constexpr int A_BYTES = BLOCK_M_CTA * BLOCK_K * 2;
+    static constexpr int B_BYTES = BN_CTA * BLOCK_K * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // a multiple of 1024
+    static constexpr int STAGES = (CG == 1) ? 4 : 6;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int STAGING_OFF = RING_BYTES;
+    static constexpr int STAGING_TOTAL = 4 * 2 * STAGING_BYTES;   // 4 warps x 2 buffers
+    static constexpr int BAR_OFF = STAGING_OFF + STAGING_TOTAL;
+    // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], mma_done
+    static constexpr int NUM_BARS = 2 * STAGES + 5;
+    static constexpr int TMEM_PTR_OFF = BAR_OFF + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = TMEM_PTR_OFF + 16 + 1024;   // + room to align the base
+    static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+    static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
+    static constexpr uint32_t IDESC_M = BLOCK_M_CTA * CG;
+};
+
+// ------------------------------------------------------------------ bounded waits
+struct WaitCtx {
+    uint64_t limit_ns;
+    unsigned long long id;
+    unsigned long long *status;
+    bool aborted;
+};
+
+__device__ __forceinline__ void record_timeout(unsigned long long *status, unsigned long long id,
+                                               uint32_t site)
+{
+    atomicCAS(&status[0], 0ull, id);
+    atomicExch(&status[1], static_cast<unsigned long long>(site));
+    atomicExch(&status[2], id);
+    __threadfence();
+}
+
+template <bool CLUSTER>
+__device__ __forceinline__ bool probe(uint32_t bar, uint32_t parity)
+{
+    return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+}
+
+// Slow path of a wait: spin on `bar` until phase `parity` completes (returns
+// true), until another thread of this launch has timed out (returns false),
+// or until `limit_ns` passes (records the site and returns false).
+template <bool CLUSTER>
+__device__ __noinline__ bool wait_bounded_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                               unsigned long long id, unsigned long long *status,
+                                               uint32_t site)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (probe<CLUSTER>(bar, parity))
+            return true;
+        if ((n & 63u) == 0) {
+            const volatile unsigned long long *st = status;
+            if (st[2] == id)
+                return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                record_timeout(status, id, site);
+                return false;
+            }
+        }
+    }
+}
+
+// Wait for phase `parity` of `bar`. Returns false, without waiting, once this
+// thread has seen the launch time out; the fast path is one probe.
+template <bool CLUSTER>
+__device__ __forceinline__ bool wait_bounded(WaitCtx &w, uint32_t bar, uint32_t parity,
+                                             uint32_t site)
+{
+    if (w.aborted)
+        return false;
+    if (probe<CLUSTER>(bar, parity))
+        return true;
+    if (!wait_bounded_slow<CLUSTER>(bar, parity, w.limit_ns, w.id, w.status, site))
+        w.aborted = true;
+    return !w.aborted;
+}
+
+// Teardown wait: runs even after an abort (it only bounds how long copies or
+// MMAs already in flight may take to land), and never waits past the limit.
+template <bool CLUSTER>
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                        unsigned long long id, unsigned long long *status,
+                                        uint32_t site)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (probe<CLUSTER>(bar, parity))
+            return;
+        if ((n & 63u) == 0 && global_timer_ns() - t0 > limit_ns) {
+            record_timeout(status, id, site);
+            return;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ tile order
+// Persistent tile t -> (m_blk, n_blk). Tiles run in groups of group_m tile
+// rows. Inside a group, the tile row changes fastest, so tiles running at the
+// same time share A row panels and B column panels in L2.
+__device__ __forceinline__ void tile_coords(const KernelParams &p, int t, int &m_blk, int &n_blk)
+{
+    const int per_group = p.group_m * p.num_n_tiles;
+    const int g = t / per_group;
+    const int first_m = g * p.group_m;
+    const int gm = min(p.num_m_tiles - first_m, p.group_m);
+    const int r = t - g * per_group;
+    m_blk = first_m + r % gm;
+    n_blk = r / gm;
+}
+
+// ------------------------------------------------------------------ epilogue helpers
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi, uint32_t out_dtype)
+{
+    const float a = __uint_as_float(lo), b = __uint_as_float(hi);
+    if (out_dtype == OUT_BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);   // .x (low half) = a
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Write one accumulator row chunk (32 FP32 values of row `lane`) into a staging
+// buffer in the layout the C tensor map's swizzle expects:
+//   FP32 out: 128-byte rows, 16-byte unit j stored at j ^ (row % 8)        (128B swizzle)
+//   16-bit out: 64-byte rows, 16-byte unit j stored at j ^ ((row / 2) % 4) (64B swizzle)
+__device__ __forceinline__ void stage_row(uint32_t buf, uint32_t lane, const uint32_t (&v)[32],
+                                          uint32_t out_dtype)
+{
+    if (out_dtype == OUT_F32) {
+        const uint32_t row = buf + lane * 128u;
+#pragma unroll
+        for (uint32_t j = 0; j < 8; ++j)
+            st_shared_v4(row + ((j ^ (lane & 7u)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                         v[4 * j + 3]);
+    } else {
+        const uint32_t row = buf + lane * 64u;
+#pragma unroll
+        for (uint32_t j = 0; j < 4; ++j)
+            st_shared_v4(row + ((j ^ ((lane >> 1) & 3u)) << 4), pack2(v[8 * j], v[8 * j + 1], out_dtype),
+                         pack2(v[8 * j + 2], v[8 * j + 3], out_dtype),
+                         pack2(v[8 * j + 4], v[8 * j + 5], out_dtype),
+                         pack2(v[8 * j + 6], v[8 * j + 7], out_dtype));
+    }
+}
+
+// Ordinary predicated stores of one row chunk, for a C whose base or row pitch
+// cannot be described to the TMA engine.
+__device__ __forceinline__ void store_row_direct(const KernelParams &p, int row, int col0,
+                                                 const uint32_t (&v)[32])
+{
+    if (row >= p.M)
+        return;
+    const int64_t base = static_cast<int64_t>(row) * p.N;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int col = col0 + i;
+        if (col >= p.N)
+            break;
+        const float f = __uint_as_float(v[i]);
+        if (p.out_dtype == OUT_F32)
+            static_cast<float *>(p.C)[base + col] = f;
+        else if (p.out_dtype == OUT_F16)
+            static_cast<__half *>(p.C)[base + col] = __float2half_rn(f);
+        else
+            static_cast<__nv_bfloat16 *>(p.C)[base + col] = __float2bfloat16_rn(f);
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int CG, int BN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
+                    const __grid_constant__ CUtensorMap tmap_b,
+                    const __grid_constant__ CUtensorMap tmap_c, const KernelParams p)
+{
+    using Cfg = TileConfig<CG, BN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;     // 128B-swizzled tiles need 1024 B alignment
+    uint8_t *smem = smem_raw + (base - raw);
+
+    const uint32_t warp = threadIdx.x / 32u;
+    const uint32_t lane = threadIdx.x % 32u;
+    const uint32_t rank = (CG == 2) ? cluster_cta_rank() : 0u;
+    const int cluster_id = static_cast<int>(blockIdx.x) / CG;
+    const int num_clusters = static_cast<int>(gridDim.x) / CG;
+
+    const uint32_t bar0 = base + Cfg::BAR_OFF;
+    auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (Cfg::STAGES + s); };
+    auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cfg::STAGES + b); };
+    auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cfg::STAGES + 2 + b); };
+    const uint32_t done_bar = bar0 + 8u * (2 * Cfg::STAGES + 4);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::TMEM_PTR_OFF);
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < Cfg::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);    // producer's arrive.expect_tx (+ bytes of both CTAs)
+            mbar_init(empty_bar(s), 1);   // one tcgen05.commit
+        }
+        for (uint32_t b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);             // one tcgen05.commit
+            mbar_init(tempty_bar(b), 4u * CG);      // every epilogue warp of the tile
+        }
+        mbar_init(done_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc<CG>(smem_u32(tmem_holder), TMEM_COLS);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before_sync();
+    if constexpr (CG == 2)
+        cluster_sync();
+    else
+        __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
+
+    WaitCtx w{p.timeout_ns, p.launch_id, p.status, false};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tensor_map(&tmap_a);
+            prefetch_tensor_map(&tmap_b);
+            uint32_t s = 0, ph = 0, pend_mask = 0, pend_par = 0;
+            for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+                int m_blk, n_blk;
+                tile_coords(p, t, m_blk, n_blk);
+                const int a_row = m_blk * (BLOCK_M_CTA * CG) + static_cast<int>(rank) * BLOCK_M_CTA;
+                const int b_off = n_blk * BN + static_cast<int>(rank) * Cfg::BN_CTA;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    wait_bounded<CG == 2>(w, empty_bar(s), ph ^ 1u, SITE_PRODUCER_EMPTY);
+                    if (!w.aborted) {
+                        const uint32_t a_dst = base + s * Cfg::STAGE_BYTES;
+                        const uint32_t b_dst = a_dst + Cfg::A_BYTES;
+                        const int k0 = kb * BLOCK_K;
+                        if constexpr (CG == 1) {
+                            const uint32_t bar = full_bar(s);
+                            mbar_arrive_expect_tx(bar, Cfg::STAGE_BYTES);
+                            tma_load_2d(a_dst, &tmap_a, bar, k0, a_row);
+                            if (!p.b_mn_major)
+                                tma_load_2d(b_dst, &tmap_b, bar, k0, b_off);
+                            else
+                                for (int j = 0; j < Cfg::BN_CTA / 64; ++j)
+                                    tma_load_2d(b_dst + j * 8192u, &tmap_b, bar, b_off + 64 * j, k0);
+                        } else {
+                            // both CTAs' boxes complete on the even CTA's full barrier
+                            const uint32_t bar = map_to_cta(full_bar(s), 0);
+                            if (rank == 0)
+                                mbar_arrive_expect_tx(full_bar(s), 2u * Cfg::STAGE_BYTES);
+                            tma_load_2d_pair(a_dst, &tmap_a, bar, k0, a_row);
+                            if (!p.b_mn_major)
+                                tma_load_2d_pair(b_dst, &tmap_b, bar, k0, b_off);
+                            else
+                                for (int j = 0; j < Cfg::BN_CTA / 64; ++j)
+                                    tma_load_2d_pair(b_dst + j * 8192u, &tmap_b, bar, b_off + 64 * j, k0);
+                        }
+                        pend_mask |= 1u << s;
+                        pend_par = (pend_par & ~(1u << s)) | (ph << s);
+                    }
+                    if (++s == Cfg::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            // Leave no bulk copy into shared memory in flight: wait for the last
+            // fill of every slot (the peer CTA's copies land on these barriers too).
+            if (CG == 1 || rank == 0)
+                for (uint32_t s2 = 0; s2 < Cfg::STAGES; ++s2)
+                    if ((pend_mask >> s2) & 1u)
+                        wait_drain<CG == 2>(full_bar(s2), (pend_par >> s2) & 1u, w.limit_ns, w.id, w.status,
+                                           SITE_PRODUCER_DRAIN);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && (CG == 1 || rank == 0)) {
+            const bool b_mn = p.b_mn_major != 0;
+            // K-major: rows of 128 B in 8-row groups 1024 B apart; one K=16 step = 32 B.
+            // MN-major: 64-wide N atoms 8192 B apart (LBO), 8-row K groups 1024 B
+            // apart (SBO); one K=16 step = 16 rows = 2048 B.
+            const uint32_t b_lbo = b_mn ? 8192u : 16u;
+            const uint32_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
+            uint32_t s = 0, ph = 0, acc = 0, acc_ph = 0;
+            for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+                wait_bounded<CG == 2>(w, tempty_bar(acc), acc_ph ^ 1u, SITE_MMA_TMEM_EMPTY);
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    wait_bounded<CG == 2>(w, full_bar(s), ph, SITE_MMA_FULL);
+                    tc_fence_after_sync();
+                    if (!w.aborted) {
+                        const uint32_t a_addr = base + s * Cfg::STAGE_BYTES;
+                        const uint64_t a_desc = smem_desc_sw128(a_addr, 16u, 1024u);
+                        const uint64_t b_desc = smem_desc_sw128(a_addr + Cfg::A_BYTES, b_lbo, 1024u);
+#pragma unroll
+                        for (uint32_t k = 0; k < BLOCK_K / UMMA_K; ++k)
+                            mma_f16<CG>(d_tmem, a_desc + 2u * k, b_desc + b_step * k, p.idesc,
+                                        (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    if constexpr (CG == 1)
+                        mma_commit(empty_bar(s));
+                    else
+                        mma_commit_pair(empty_bar(s), 0x3);
+                    if (++s == Cfg::STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if constexpr (CG == 1)
+                    mma_commit(tfull_bar(acc));
+                else
+                    mma_commit_pair(tfull_bar(acc), 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_ph ^= 1u;
+                }
+            }
+            // No MMA may still be writing TMEM when it is freed.
+            if constexpr (CG == 1)
+                mma_commit(done_bar);
+            else
+                mma_commit_pair(done_bar, 0x1);
+            wait_drain<false>(done_bar, 0, w.limit_ns, w.id, w.status, SITE_MMA_DONE);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const uint32_t quarter = warp & 3u;      // the TMEM lane quarter this warp may access
+        const uint32_t staging = base + Cfg::STAGING_OFF + (warp - EPI_WARP0) * 2u * STAGING_BYTES;
+        uint32_t acc = 0, acc_ph = 0, sb = 0;
+        for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+            int m_blk, n_blk;
+            tile_coords(p, t, m_blk, n_blk);
+            wait_bounded<CG == 2>(w, tfull_bar(acc), acc_ph, SITE_EPI_TMEM_FULL);
+            const bool skip = __any_sync(0xffffffffu, w.aborted);   // warp-uniform
+            w.aborted = skip;
+            tc_fence_after_sync();
+            const int row0 = m_blk * (BLOCK_M_CTA * CG) + static_cast<int>(rank) * BLOCK_M_CTA +
+                             static_cast<int>(quarter) * 32;
+            const int col0 = n_blk * BN;
+            const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + acc * ACC_STRIDE;
+#pragma unroll 1
+            for (int c = 0; c < BN / EPI_COLS; ++c) {
+                uint32_t v[32];
+                if (!skip) {
+                    tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * EPI_COLS), v);
+                    tmem_ld_wait();
+                }
+                if (c == BN / EPI_COLS - 1) {
+                    // accumulator fully read: hand it back to the MMA issuer
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CG == 1)
+                            mbar_arrive_local(tempty_bar(acc));
+                        else
+                            mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
+                    }
+                }
+                const int gcol = col0 + c * EPI_COLS;
+                if (skip || gcol >= p.N)
+                    continue;
+                if (p.direct_store) {
+                    store_row_direct(p, row0 + static_cast<int>(lane), gcol, v);
+                    continue;
+                }
+                const uint32_t buf = staging + sb * STAGING_BYTES;
+                if (lane == 0)
+                    bulk_wait_group_read<1>();   // the store that last used `buf` has read it
+                __syncwarp();
+                stage_row(buf, lane, v, p.out_dtype);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && row0 < p.M) {
+                    tma_store_2d(&tmap_c, buf, gcol, row0);
+                    bulk_commit_group();
+                }
+                sb ^= 1u;
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_ph ^= 1u;
+            }
+        }
+        if (lane == 0)
+            bulk_wait_group_all();
+    }
+
+    // ---------------------------------------------------------------- teardown
+    __syncwarp();
+    tc_fence_before_sync();
+    if constexpr (CG == 2)
+        cluster_sync();   // the peer no longer touches this CTA's barriers or TMEM
+    else
+        __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc<CG>(tmem_base, TMEM_COLS);
+    }
+}
+
+// One CTA waits, through the same bounded wait, on a barrier that nothing
+// arrives at; it must record SITE_SELFTEST and return.
+__global__ void wait_selftest_kernel(uint64_t timeout_ns, unsigned long long launch_id,
+                                     unsigned long long *status)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        WaitCtx w{timeout_ns, launch_id, status, false};
+        wait_bounded<false>(w, smem_u32(&bar), 0, SITE_SELFTEST);
+    }
+}
+
+// Copy a rows x cols matrix of 16-bit elements (row pitch `cols`, any 2-byte
+// alignment) to a buffer whose row pitch `ld_dst` is a multiple of 8 elements
+// and whose base is 256-byte aligned, so the TMA engine can describe it.
+__global__ void realign_rows_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst,
+                                    int64_t rows, int64_t cols, int64_t ld_dst)
+{
+    const int64_t total = rows * cols;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / cols;
+        const int64_t c = i - r * cols;
+        dst[r * ld_dst + c] = src[i];
+    }
+}
+
+} // namespace dtg

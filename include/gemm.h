@@ -1,0 +1,195 @@
+/*
+ * gemm.h: C ABI of the GB300 (sm_103a) dense tiled GEMM library.
+ *
+ * The library computes C = A·B for FP16 or BF16 operands. It accumulates in
+ * FP32 in tensor memory and casts on store to FP16, BF16 or FP32. The
+ * operation is the tiled GEMM of "Two Waves, One Stage Apart:
+ * Warp-Pipelining Triton GEMMs on AMD Instinct" (opening paragraph: compute
+ * on one pair of operand tiles while the next pair is prepared). Throughput
+ * is counted as 2·M·N·K / elapsed time, as in that page's Table 1 caption.
+ *
+ * Conventions shared by every entry point:
+ *   - A is M x K, row-major (K contiguous, leading dimension K).
+ *   - B is stored in one of two ways:
+ *       GEMM_K_MAJOR : N x K, K contiguous (the transposed "B_T" operand of
+ *                      "Porting High-Performance HIP Kernels to FlyDSL",
+ *                      section "A More Complex Kernel");
+ *       GEMM_MN_MAJOR: K x N, N contiguous (plain row-major B).
+ *   - C is M x N, row-major, densely packed (leading dimension N).
+ *   - Every matrix is dense; there are no leading-dimension arguments.
+ *   - The caller owns all operand memory. The library never frees it.
+ *   - C must not overlap A or B. This is not checked.
+ *   - Calls are asynchronous on the given stream, except where stated.
+ *     `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *     default stream.
+ *   - Host-side argument errors are reported by the return value before
+ *     anything is enqueued. They never abort the process.
+ */
+#ifndef DENSE_TILED_GEMM_GEMM_H
+#define DENSE_TILED_GEMM_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_F16 = 0,
+    GEMM_BF16 = 1,
+    GEMM_F32 = 2
+} gemm_dtype_t;
+
+typedef enum {
+    GEMM_K_MAJOR = 0,
+    GEMM_MN_MAJOR = 1
+} gemm_layout_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,    /* null pointer, non-positive size, unknown enum */
+    GEMM_ERR_UNSUPPORTED = 2,    /* valid request the library does not implement */
+    GEMM_ERR_CUDA = 3,           /* a CUDA runtime or driver call failed */
+    GEMM_ERR_TIMEOUT = 4,        /* a kernel wait ran past its limit (device status) */
+    GEMM_ERR_NO_DEVICE = 5,      /* no usable sm_100-family GPU is current */
+    GEMM_ERR_OUT_OF_MEMORY = 6   /* a workspace allocation failed */
+} gemm_status_t;
+
+/*
+ * gemm: C = A·B on the current CUDA device.
+ *
+ *   A, B, C   device pointers (layouts above). A and B are FP16 or BF16, and
+ *             they must share a type. C has type dtype_out.
+ *   M, N, K   sizes, each >= 1. K = 0 is rejected (GEMM_ERR_INVALID_ARG).
+ *   dtype_in  GEMM_F16 or GEMM_BF16: the type of both A and B.
+ *   dtype_out GEMM_F16, GEMM_BF16 or GEMM_F32. The FP32 accumulator is
+ *             rounded to nearest-even when it is cast.
+ *   layoutA   must be GEMM_K_MAJOR (GEMM_MN_MAJOR gives GEMM_ERR_UNSUPPORTED).
+ *   layoutB   GEMM_K_MAJOR or GEMM_MN_MAJOR.
+ *   stream    cudaStream_t as void*.
+ *
+ * Alignment: the tensor-memory-access engine needs 16-byte-aligned bases and
+ * row pitches. When A or B misses this (for example K*2 bytes not a multiple
+ * of 16), the call first copies that operand into a padded, stream-ordered
+ * scratch buffer. It takes this buffer with cudaMallocAsync and frees it with
+ * cudaFreeAsync on the same stream. When C misses it, the epilogue writes C
+ * with ordinary stores instead of bulk tensor stores. Results do not depend
+ * on either path.
+ *
+ * Errors: returns GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED,
+ * GEMM_ERR_NO_DEVICE, GEMM_ERR_OUT_OF_MEMORY or GEMM_ERR_CUDA before or at
+ * launch. A kernel that stalls past the wait limit (2 s per wait) sets the
+ * library's device status word and exits; gemm_last_device_status reports it.
+ */
+gemm_status_t gemm(const void *A, const void *B, void *C,
+                   int64_t M, int64_t N, int64_t K,
+                   int dtype_in, int dtype_out, int layoutA, int layoutB,
+                   void *stream);
+
+/*
+ * gemm_options_t: overrides for gemm_ex. A zero field means the library
+ * chooses that value.
+ *   cta_group     1: each output tile is 128 x block_n and one CTA owns it.
+ *                 2: tiles are 256 x block_n, and a cluster of two CTAs
+ *                 shares each one (paired tensor-core issue).
+ *   block_n       the tile width: 256 or 224 for cta_group 2, 256 for
+ *                 cta_group 1. 224 is valid only for a K-major B.
+ *   max_clusters  upper bound on the persistent grid, counted in CTAs
+ *                 (cta_group 1) or in pairs (cta_group 2). A small value
+ *                 makes each CTA loop over many tiles.
+ *   group_m       raster group height in tiles, for the swizzled tile order.
+ *   timeout_ms    per-wait limit inside the kernel (default 2000).
+ */
+typedef struct {
+    int32_t cta_group;
+    int32_t block_n;
+    int32_t max_clusters;
+    int32_t group_m;
+    int32_t timeout_ms;
+    int32_t reserved[3];
+} gemm_options_t;
+
+/* gemm with overrides. opts may be NULL. An unsupported override combination
+ * gives GEMM_ERR_UNSUPPORTED. */
+gemm_status_t gemm_ex(const void *A, const void *B, void *C,
+                      int64_t M, int64_t N, int64_t K,
+                      int dtype_in, int dtype_out, int layoutA, int layoutB,
+                      const gemm_options_t *opts, void *stream);
+
+/*
+ * gemm_plan_t: the launch gemm_ex would make for a problem. Filled by
+ * gemm_plan, which launches nothing.
+ */
+typedef struct {
+    int32_t cta_group;     /* CTAs per output tile */
+    int32_t block_m;       /* rows per output tile (128 * cta_group) */
+    int32_t block_n;       /* columns per output tile */
+    int32_t block_k;       /* K per pipeline stage (64) */
+    int32_t stages;        /* shared-memory ring depth */
+    int32_t num_tiles;     /* output tiles */
+    int32_t grid_ctas;     /* persistent CTAs launched */
+    int32_t group_m;       /* raster group height */
+    int32_t realign_a;     /* 1 if A goes through the padded copy */
+    int32_t realign_b;     /* 1 if B goes through the padded copy */
+    int32_t direct_store;  /* 1 if C is written with ordinary stores */
+    int32_t smem_bytes;    /* dynamic shared memory per CTA */
+    int32_t num_sms;       /* multiprocessors on the current device */
+    int32_t reserved[3];
+} gemm_plan_t;
+
+/* Fill *plan for a problem on the current device. Same validation and
+ * errors as gemm_ex. Needs a GPU, for the SM count and cluster occupancy. */
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K,
+                        int dtype_in, int dtype_out, int layoutA, int layoutB,
+                        const void *A, const void *B, const void *C,
+                        const gemm_options_t *opts, gemm_plan_t *plan);
+
+/*
+ * gemm_from_host: C = A·B with A, B and C in HOST memory (pinned or
+ * pageable). It copies A and B to a device workspace, runs gemm on `stream`,
+ * copies C back, and synchronises the stream before returning: C_host is
+ * complete when the call returns GEMM_OK. The workspace belongs to the
+ * library. It is cached per device and grows to the largest problem seen;
+ * gemm_release_workspace frees it. The errors are gemm's, plus
+ * GEMM_ERR_OUT_OF_MEMORY when the workspace cannot grow.
+ */
+gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_host,
+                             int64_t M, int64_t N, int64_t K,
+                             int dtype_in, int dtype_out, int layoutA, int layoutB,
+                             void *stream);
+
+/* Free the gemm_from_host workspace of the current device. Synchronises the
+ * device first. */
+gemm_status_t gemm_release_workspace(void);
+
+/*
+ * gemm_last_device_status: synchronise `stream`, then read and clear the
+ * device status word of the current device. Returns GEMM_OK, or
+ * GEMM_ERR_TIMEOUT if any kernel of this library timed out a wait since the
+ * last call. If detail is not NULL, *detail gets the wait site that timed
+ * out (role << 8 | barrier kind), or 0.
+ */
+gemm_status_t gemm_last_device_status(void *stream, uint32_t *detail);
+
+/*
+ * gemm_selftest_wait_timeout: launch one CTA that waits, through the
+ * kernel's own bounded wait, on a shared-memory barrier that nothing ever
+ * arrives at, with a limit of timeout_ms. The kernel records a timeout in
+ * the device status word and returns. It does not hang, trap or fault.
+ * Check the result with gemm_last_device_status. Exists so that tests can
+ * prove that a stalled wait ends.
+ */
+gemm_status_t gemm_selftest_wait_timeout(int32_t timeout_ms, void *stream);
+
+/* Human-readable name of a status code. Never NULL. */
+const char *gemm_status_string(int status);
+
+/* Number of GEMM kernel launches (main kernel and operand copies) this
+ * process made on any device. Used to count launches in a timed region. */
+uint64_t gemm_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_TILED_GEMM_GEMM_H */

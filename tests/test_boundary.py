@@ -1,0 +1,113 @@
+"""C-ABI boundary checks that need no GPU: the library loads, it exports
+every function include/gemm.h declares, the ctypes structs match the header,
+and invalid arguments are rejected on the host before any CUDA call."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from dense_tiled_gemm_gb300 import binding
+import dense_tiled_gemm_gb300 as dtg
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gemm.h")
+FAKE = 0x10000   # never dereferenced: every call below fails validation first
+
+
+def header_text() -> str:
+    with open(HEADER) as fh:
+        return fh.read()
+
+
+def declared_functions() -> list[str]:
+    text = re.sub(r"/\*.*?\*/", "", header_text(), flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gemm\w*)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("gemm", "gemm_ex", "gemm_plan", "gemm_from_host", "gemm_last_device_status",
+                     "gemm_status_string", "gemm_selftest_wait_timeout", "gemm_launch_count",
+                     "gemm_release_workspace"):
+        assert required in names
+
+
+def test_library_exports_every_declared_function():
+    for name in declared_functions():
+        assert hasattr(binding.lib, name), f"{name} declared in gemm.h but not exported"
+
+
+def test_enums_match_header():
+    text = header_text()
+    for name, val in (("GEMM_F16", 0), ("GEMM_BF16", 1), ("GEMM_F32", 2), ("GEMM_K_MAJOR", 0),
+                      ("GEMM_MN_MAJOR", 1), ("GEMM_OK", 0), ("GEMM_ERR_INVALID_ARG", 1),
+                      ("GEMM_ERR_UNSUPPORTED", 2), ("GEMM_ERR_CUDA", 3), ("GEMM_ERR_TIMEOUT", 4),
+                      ("GEMM_ERR_NO_DEVICE", 5), ("GEMM_ERR_OUT_OF_MEMORY", 6)):
+        assert re.search(rf"\b{name}\s*=\s*{val}\b", text), name
+        assert getattr(binding, name) == val
+
+
+def test_struct_sizes():
+    # gemm_options_t: 8 int32 fields; gemm_plan_t: 16 int32 fields
+    assert ctypes.sizeof(binding.GemmOptions) == 32
+    assert ctypes.sizeof(binding.GemmPlan) == 64
+
+
+def test_status_strings():
+    for code, name in binding.STATUS_NAMES.items():
+        assert dtg.gemm_status_string(code) == name
+    assert dtg.gemm_status_string(99) == "GEMM_ERR_UNKNOWN"
+
+
+def call(M=64, N=64, K=64, din=0, dout=0, la=0, lb=0, a=FAKE, b=FAKE, c=FAKE):
+    return binding.lib.gemm(a, b, c, M, N, K, din, dout, la, lb, None)
+
+
+@pytest.mark.parametrize("kwargs,expect", [
+    (dict(a=None), 1), (dict(b=None), 1), (dict(c=None), 1),
+    (dict(M=0), 1), (dict(N=0), 1), (dict(K=0), 1), (dict(M=-5), 1), (dict(K=2 ** 31), 1),
+    (dict(din=7), 1), (dict(din=2), 2), (dict(dout=5), 1), (dict(dout=-1), 1),
+    (dict(la=1), 2), (dict(la=3), 1), (dict(lb=2), 1),
+])
+def test_invalid_arguments_rejected_on_host(kwargs, expect):
+    assert call(**kwargs) == expect
+
+
+def test_invalid_options_rejected_on_host():
+    for field, val, expect in (("cta_group", 3, 1), ("cta_group", -1, 1), ("block_n", 128, 2),
+                               ("max_clusters", -2, 1), ("group_m", -1, 1), ("timeout_ms", -1, 1)):
+        o = binding.GemmOptions()
+        setattr(o, field, val)
+        rc = binding.lib.gemm_ex(FAKE, FAKE, FAKE, 64, 64, 64, 0, 0, 0, 0, ctypes.byref(o), None)
+        assert rc == expect, field
+
+
+def test_plan_requires_output_struct():
+    assert binding.lib.gemm_plan(64, 64, 64, 0, 0, 0, 0, FAKE, FAKE, FAKE, None, None) == 1
+
+
+def test_selftest_rejects_bad_limit():
+    assert binding.lib.gemm_selftest_wait_timeout(0, None) == 1
+    assert binding.lib.gemm_selftest_wait_timeout(20000, None) == 1
+
+
+def test_python_wrapper_validates_shapes():
+    import torch
+    A = torch.zeros(4, 8, dtype=torch.float16)
+    B = torch.zeros(5, 9, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        dtg.gemm(A, B)               # K mismatch
+    with pytest.raises(TypeError):
+        dtg.gemm(A.float(), B)       # unsupported input dtype
+    with pytest.raises(ValueError):
+        dtg.gemm(A, torch.zeros(5, 8, dtype=torch.float16))   # CPU tensors on the device path
+
+
+def test_no_gpu_gives_no_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call() == binding.GEMM_ERR_NO_DEVICE
+    assert binding.lib.gemm_last_device_status(None, None) == binding.GEMM_ERR_NO_DEVICE
