@@ -8,3 +8,6 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the CUDA path)")
+    # Build the library and the oracle if this checkout has not been built yet.
+    import __graft_entry__
+    __graft_entry__.build()
