@@ -79,6 +79,20 @@ def source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(x: float, pg, device) -> float:
+    """Maximum of a per-rank scalar over all ranks (identity without a process group)."""
+    if pg is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_step: float, steps: int, seconds: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time."""
+    return world * flops_per_step * steps / seconds / 1e12
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -294,12 +308,9 @@ def run_ours(args):
 
     region_ms = starts[0].elapsed_time(ends[-1])
     kernel_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    if pg:
-        t = torch.tensor([region_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        region_ms = float(t.item())
+    region_ms = max_over_ranks(region_ms, pg, dev)
     flops_step = float(w.flops)
-    value = world * flops_step * args.steps / (region_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops_step, args.steps, region_ms * 1e-3)
 
     peaks, peak_src = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))  # FP16 and BF16 share the dense rate
@@ -320,13 +331,9 @@ def run_ours(args):
         t0 = time.perf_counter()
         for _ in range(n):
             dtg.gemm_from_host(Ah, Bh, Ch, layout_b=w.layout_b, stream=stream)
-        dt = time.perf_counter() - t0
-        if pg:
-            t = torch.tensor([dt], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            dt = float(t.item())
+        dt = max_over_ranks(time.perf_counter() - t0, pg, dev)
         dtg.gemm_release_workspace()
-        e2e = {"value": world * flops_step * n / dt / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": whole_job_tflops(world, flops_step, n, dt), "unit": "TFLOP/s",
                "h2d_bytes_per_step": (Ah.numel() + Bh.numel()) * 2,
                "d2h_bytes_per_step": Ch.numel() * Ch.element_size(),
                "steps": n, "api": "gemm_from_host (pinned host buffers, synchronous)"}
