@@ -162,3 +162,22 @@ def gemm_status_string(status: int) -> str:
 
 def gemm_launch_count() -> int:
     return int(binding.lib.gemm_launch_count())
+
+
+def gemm_no_alloc(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *, layout_b: str = "k",
+                  stream=None) -> torch.Tensor:
+    """gemm for callers that must not allocate device memory, for example a serving
+    runtime whose memory pool already owns the GPU, or a latency-critical loop where an
+    allocation could stall or fail. The caller passes C. An operand that needs
+    re-pitching goes into the library's fixed 32 MiB device array instead of newly
+    allocated memory. Calls whose padded operands exceed that array raise GemmError
+    (GEMM_ERR_UNSUPPORTED). Calls that overlap on the GPU share the array and race."""
+    if C is None:
+        raise ValueError("gemm_no_alloc needs the caller's C")
+    M, N, K, C = _prepare(A, B, C, layout_b, None, "cuda")
+    with torch.cuda.device(A.device):
+        _check(binding.lib.gemm_no_alloc(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                                         _DT_IN[A.dtype], _DT_OUT[C.dtype], GEMM_K_MAJOR,
+                                         _LAYOUT[layout_b], _stream_ptr(stream)),
+               "gemm_no_alloc")
+    return C

@@ -84,3 +84,9 @@ def load(path: str = LIB_PATH):
 
 
 lib = load()
+
+# gemm_no_alloc: the same arguments as gemm; declared here for the binding below.
+lib.gemm_no_alloc.restype = ctypes.c_int
+lib.gemm_no_alloc.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                              ctypes.c_int, ctypes.c_int, ctypes.c_void_p]

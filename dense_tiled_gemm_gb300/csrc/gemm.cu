@@ -565,3 +565,163 @@ const char *gemm_status_string(int status)
 uint64_t gemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 } // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point (gemm_no_alloc).
+//
+// For callers that cannot allocate device memory, for example a serving
+// runtime that has given all of the GPU's memory to its own pool, or a
+// latency-critical loop where cudaMalloc/cudaFree could synchronise the device
+// or fail. The only allocation gemm makes is the re-pitch scratch of a
+// misaligned A or B. Here that scratch is this fixed array, held on every GPU
+// that loads the library until the process exits. Host code must not use
+// the name g_no_alloc_scratch as a device address: it stands for a host-side
+// shadow. The device address comes from cudaGetSymbolAddress, looked up once
+// per device with that device current.
+static __device__ __align__(256) unsigned char g_no_alloc_scratch[GEMM_NO_ALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_no_alloc_mu;
+void *g_no_alloc_ptr[MAX_DEVICES] = {};
+
+// Device address of g_no_alloc_scratch on the current device (first call per
+// device: cudaGetSymbolAddress, return code checked).
+gemm_status_t no_alloc_scratch(void **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_no_alloc_mu);
+    if (!g_no_alloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        g_no_alloc_ptr[dev] = p;
+    }
+    *out = g_no_alloc_ptr[dev];
+    return GEMM_OK;
+}
+
+// Re-pitch a rows x cols 16-bit matrix into caller-provided memory `dst`
+// (row pitch ld = cols rounded up to 8 elements). The pad is never read.
+gemm_status_t realign_into(const void *src, int64_t rows, int64_t cols, int64_t ld, int sms,
+                           cudaStream_t st, void *dst)
+{
+    const int64_t total = rows * cols;
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(sms) * 8);
+    realign_rows_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(
+        static_cast<const uint16_t *>(src), static_cast<uint16_t *>(dst), rows, cols, ld);
+    if (cudaGetLastError() != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return GEMM_OK;
+}
+
+gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                           int dtype_in, int dtype_out, int layoutA, int layoutB, cudaStream_t st)
+{
+    gemm_status_t rc = validate(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, nullptr);
+    if (rc != GEMM_OK)
+        return rc;
+    DeviceState *d = nullptr;
+    if ((rc = device_state(&d)) != GEMM_OK)
+        return rc;
+    Plan pl;
+    if ((rc = make_plan(*d, M, N, K, dtype_out, layoutB, A, B, C, nullptr, &pl)) != GEMM_OK)
+        return rc;
+    const Variant &var = kVariants[pl.variant];
+    const bool b_mn = layoutB == GEMM_MN_MAJOR;
+
+    // Scratch layout: padded A at offset 0, padded B at the next 256-byte boundary.
+    const int64_t b_rows = b_mn ? K : N, b_cols = b_mn ? N : K;
+    const int64_t lda_pad = (K + 7) / 8 * 8, ldb_pad = (b_cols + 7) / 8 * 8;
+    const uint64_t a_bytes = pl.realign_a ? static_cast<uint64_t>(M) * lda_pad * 2 : 0;
+    const uint64_t b_off = (a_bytes + 255) / 256 * 256;
+    const uint64_t b_bytes = pl.realign_b ? static_cast<uint64_t>(b_rows) * ldb_pad * 2 : 0;
+    if (b_off + b_bytes > GEMM_NO_ALLOC_SCRATCH_BYTES)
+        return GEMM_ERR_UNSUPPORTED;   // padded operands exceed the fixed scratch array
+
+    const void *a_ptr = A, *b_ptr = B;
+    int64_t lda = K, ldb = b_cols;
+    if (pl.realign_a || pl.realign_b) {
+        void *scratch = nullptr;
+        if ((rc = no_alloc_scratch(&scratch)) != GEMM_OK)
+            return rc;
+        char *base = static_cast<char *>(scratch);
+        if (pl.realign_a) {
+            if ((rc = realign_into(A, M, K, lda_pad, d->sms, st, base)) != GEMM_OK)
+                return rc;
+            a_ptr = base;
+            lda = lda_pad;
+        }
+        if (pl.realign_b) {
+            if ((rc = realign_into(B, b_rows, b_cols, ldb_pad, d->sms, st, base + b_off)) != GEMM_OK)
+                return rc;
+            b_ptr = base + b_off;
+            ldb = ldb_pad;
+        }
+    }
+
+    alignas(64) CUtensorMap ta, tb, tc;
+    std::memset(&tc, 0, sizeof(tc));
+    const CUtensorMapDataType in_dt = tma_dtype(dtype_in);
+    bool ok = encode_2d(&ta, in_dt, a_ptr, K, M, lda * 2, BLOCK_K, BLOCK_M_CTA, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!b_mn)
+        ok = ok && encode_2d(&tb, in_dt, b_ptr, K, N, ldb * 2, BLOCK_K, var.bn / var.cg,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        ok = ok && encode_2d(&tb, in_dt, b_ptr, N, K, ldb * 2, 64, BLOCK_K, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!pl.direct_store)
+        ok = ok && encode_2d(&tc, tma_dtype(dtype_out), C, N, M, N * esize(dtype_out), EPI_COLS, 32,
+                             dtype_out == GEMM_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!ok)
+        return GEMM_ERR_CUDA;
+
+    KernelParams kp = {};
+    kp.M = static_cast<int32_t>(M);
+    kp.N = static_cast<int32_t>(N);
+    kp.K = static_cast<int32_t>(K);
+    kp.num_m_tiles = pl.num_m;
+    kp.num_n_tiles = pl.num_n;
+    kp.num_tiles = pl.num_tiles;
+    kp.num_k_blocks = pl.num_kb;
+    kp.group_m = pl.group_m;
+    kp.idesc = make_idesc_f16(128u * var.cg, static_cast<uint32_t>(var.bn), dtype_in == GEMM_BF16 ? 1u : 0u,
+                              b_mn ? 1u : 0u);
+    kp.out_dtype = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_BF16 ? OUT_BF16 : OUT_F16);
+    kp.b_mn_major = b_mn ? 1u : 0u;
+    kp.direct_store = pl.direct_store ? 1u : 0u;
+    kp.C = C;
+    kp.timeout_ns = DEFAULT_TIMEOUT_MS * 1000000ull;
+    kp.launch_id = g_next_id.fetch_add(1, std::memory_order_relaxed);
+    kp.status = d->status;
+
+    cudaError_t err;
+    if (var.cg == 2 && var.bn == 256)
+        err = launch_variant<2, 256>(pl.grid_ctas, ta, tb, tc, kp, st);
+    else if (var.cg == 2 && var.bn == 224)
+        err = launch_variant<2, 224>(pl.grid_ctas, ta, tb, tc, kp, st);
+    else
+        err = launch_variant<1, 256>(pl.grid_ctas, ta, tb, tc, kp, st);
+    if (err != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return GEMM_OK;
+}
+
+} // namespace
+
+extern "C" gemm_status_t gemm_no_alloc(const void *A, const void *B, void *C, int64_t M, int64_t N,
+                                       int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB,
+                                       void *stream)
+{
+    return run_no_alloc(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB,
+                        static_cast<cudaStream_t>(stream));
+}

@@ -181,6 +181,44 @@ gemm_status_t gemm_last_device_status(void *stream, uint32_t *detail);
  */
 gemm_status_t gemm_selftest_wait_timeout(int32_t timeout_ms, void *stream);
 
+/*
+ * gemm_no_alloc: gemm for callers that must not allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * such as a serving runtime that has already handed all of the GPU's memory
+ * to its own pool, or a latency-critical loop in which a cudaMalloc or
+ * cudaFree could synchronise the device or fail. gemm itself calls
+ * cudaMallocAsync/cudaFreeAsync whenever A or B must be re-pitched (a base
+ * or row pitch that is not a multiple of 16 bytes, for example K*2 bytes
+ * not a multiple of 16). gemm_no_alloc takes the same arguments and computes
+ * the same result, but it never allocates or frees: the re-pitched copies go
+ * into one fixed device array that the library holds on every GPU that
+ * loads it, GEMM_NO_ALLOC_SCRATCH_BYTES (32 MiB) in size, until the process
+ * exits.
+ *
+ *   - Limit: the padded copies (rows x pitch rounded up to 8 elements x 2
+ *     bytes, A then B, each started on a 256-byte boundary) must fit in
+ *     GEMM_NO_ALLOC_SCRATCH_BYTES. Otherwise the call returns
+ *     GEMM_ERR_UNSUPPORTED and launches nothing. When no operand needs
+ *     re-pitching the array is not used, and there is no size limit beyond
+ *     gemm's.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current. Make this first call
+ *     before any stream capture.
+ *   - Sharing: every call on a device uses the same array, and the array
+ *     keeps the previous call's contents. Nothing in it has to start at zero:
+ *     each call writes every element it later reads. Calls whose work
+ *     overlaps on the GPU (for example on two streams at once) race on the
+ *     array, so serialise them.
+ * Other errors are as for gemm.
+ */
+#define GEMM_NO_ALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+gemm_status_t gemm_no_alloc(const void *A, const void *B, void *C,
+                            int64_t M, int64_t N, int64_t K,
+                            int dtype_in, int dtype_out, int layoutA, int layoutB,
+                            void *stream);
+
 /* Human-readable name of a status code. Never NULL. */
 const char *gemm_status_string(int status);
 

@@ -1,0 +1,73 @@
+"""gemm_no_alloc: the allocation-free entry point, checked through the C ABI.
+
+Some callers cannot allocate device memory: a serving runtime whose own pool
+already owns the GPU's memory, or a latency-critical loop in which cudaMalloc
+or cudaFree could stall the device or fail. gemm_no_alloc serves them by
+putting re-pitched operands into a fixed device array instead of newly
+allocated scratch. These tests give it inputs that need that scratch and
+require the same result as gemm, within the parity tolerance, on two
+different calls in a row. The second call runs while the array still holds
+the first call's data. The file is named so that pytest collects it last.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import tolerance
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+OUT = {"f16": (torch.float16, 0), "bf16": (torch.bfloat16, 1), "f32": (torch.float32, 2)}
+IN = {"f16": 0, "bf16": 1}
+LAYOUT = {"k": 0, "mn": 1}
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    from dense_tiled_gemm_gb300 import binding
+    return binding.lib
+
+
+def _call(fn, A, B, C, M, N, K, din, dout, layout_b):
+    stream = torch.cuda.current_stream().cuda_stream
+    return fn(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, IN[din], OUT[dout][1], 0,
+              LAYOUT[layout_b], stream)
+
+
+def test_no_alloc_matches_gemm_on_two_calls_in_a_row(lib):
+    # Both shapes need re-pitched operands (K*2 or N*2 bytes not a multiple of 16).
+    cases = [(300, 333, 2050, "bf16", "f32", "k", 21),
+             (257, 129, 1001, "f16", "f16", "mn", 22)]
+    for M, N, K, din, dout, layout_b, seed in cases:
+        A, B = workloads.make_operands(M, N, K, din, layout_b, ("uniform", -2.0, 2.0), seed)
+        Ad, Bd = A.cuda(), B.cuda()
+        C_gemm = torch.empty((M, N), dtype=OUT[dout][0], device="cuda")
+        C_new = torch.full((M, N), float("nan"), dtype=OUT[dout][0], device="cuda")
+        assert _call(lib.gemm, Ad, Bd, C_gemm, M, N, K, din, dout, layout_b) == 0
+        assert _call(lib.gemm_no_alloc, Ad, Bd, C_new, M, N, K, din, dout, layout_b) == 0
+        torch.cuda.synchronize()
+        import ctypes
+        detail = ctypes.c_uint32(0)
+        assert lib.gemm_last_device_status(None, ctypes.byref(detail)) == 0
+        Bkn = B.double() if layout_b == "mn" else B.double().T
+        C_abs = (A.double().abs() @ Bkn.abs()).numpy()
+        ref = C_gemm.double().cpu().numpy()
+        ok, ratio, n_bad, first = tolerance.check(C_new.double().cpu().numpy(), ref, C_abs, dout)
+        assert ok, f"{n_bad} elements differ beyond the bound, first {first}"
+
+
+def test_no_alloc_rejects_operands_beyond_its_array(lib):
+    # Padded A alone needs 8200 x 2056 x 2 bytes > 32 MiB: refused before any launch.
+    M, N, K = 8200, 64, 2050
+    A = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((M, N), dtype=torch.float32, device="cuda")
+    assert _call(lib.gemm_no_alloc, A, B, C, M, N, K, "bf16", "f32", "k") == 2   # UNSUPPORTED
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(C).item() == 0
