@@ -34,21 +34,39 @@ constexpr uint64_t DEFAULT_TIMEOUT_MS = 2000;
 struct Variant {
     int cg;
     int bn;
-    int stages;
-    int smem;
+    int stage_bytes;   // one ring slot: A and B tiles of one k-block (per CTA)
     const void *fn;
-    bool b_mn_ok;   // MN-major B needs 64-column TMA boxes per CTA
+    bool b_mn_ok;      // MN-major B needs 64-column TMA boxes per CTA
 };
 
 const Variant kVariants[] = {
-    {2, 256, TileConfig<2, 256>::STAGES, TileConfig<2, 256>::SMEM_BYTES,
-     reinterpret_cast<const void *>(&gemm_tcgen05_kernel<2, 256>), true},
-    {2, 224, TileConfig<2, 224>::STAGES, TileConfig<2, 224>::SMEM_BYTES,
-     reinterpret_cast<const void *>(&gemm_tcgen05_kernel<2, 224>), false},
-    {1, 256, TileConfig<1, 256>::STAGES, TileConfig<1, 256>::SMEM_BYTES,
-     reinterpret_cast<const void *>(&gemm_tcgen05_kernel<1, 256>), true},
+    {2, 256, TileConfig<2, 256>::STAGE_BYTES, reinterpret_cast<const void *>(&gemm_tcgen05_kernel<2, 256>),
+     true},
+    {2, 224, TileConfig<2, 224>::STAGE_BYTES, reinterpret_cast<const void *>(&gemm_tcgen05_kernel<2, 224>),
+     false},
+    {1, 256, TileConfig<1, 256>::STAGE_BYTES, reinterpret_cast<const void *>(&gemm_tcgen05_kernel<1, 256>),
+     true},
 };
 constexpr int NUM_VARIANTS = sizeof(kVariants) / sizeof(kVariants[0]);
+
+// Shared-memory budget of one launch: the deepest ring that fits next to the
+// epilogue staging buffers (2 KB each for a 16-bit C, 4 KB for an FP32 C).
+struct Layout {
+    uint32_t stages;
+    uint32_t staging_bytes;
+    uint32_t smem;
+};
+
+Layout layout_for(const Variant &v, int dtype_out)
+{
+    Layout l;
+    l.staging_bytes = dtype_out == GEMM_F32 ? 4096u : 2048u;
+    l.stages = MAX_STAGES;
+    while (l.stages > 2 && smem_bytes_for(v.stage_bytes, l.stages, l.staging_bytes) > SMEM_LIMIT)
+        --l.stages;
+    l.smem = smem_bytes_for(v.stage_bytes, l.stages, l.staging_bytes);
+    return l;
+}
 
 struct DeviceState {
     bool ready = false;
@@ -94,20 +112,20 @@ gemm_status_t device_state(DeviceState **out)
         d.status = static_cast<unsigned long long *>(status);
         for (int v = 0; v < NUM_VARIANTS; ++v) {
             const Variant &var = kVariants[v];
-            if (cudaFuncSetAttribute(var.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, var.smem) !=
+            if (cudaFuncSetAttribute(var.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT) !=
                 cudaSuccess)
                 return GEMM_ERR_CUDA;
             if (var.cg == 1) {
                 int per_sm = 0;
                 if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, var.fn, NUM_THREADS,
-                                                                  var.smem) != cudaSuccess)
+                                                                  SMEM_LIMIT) != cudaSuccess)
                     return GEMM_ERR_CUDA;
                 d.max_units[v] = per_sm * d.sms;
             } else {
                 cudaLaunchConfig_t cfg = {};
                 cfg.gridDim = dim3(2 * d.sms);
                 cfg.blockDim = dim3(NUM_THREADS);
-                cfg.dynamicSmemBytes = var.smem;
+                cfg.dynamicSmemBytes = SMEM_LIMIT;
                 cudaLaunchAttribute attr[1];
                 attr[0].id = cudaLaunchAttributeClusterDimension;
                 attr[0].val.clusterDim.x = 2;
@@ -275,13 +293,13 @@ gemm_status_t realign(const void *src, int64_t rows, int64_t cols, int sms, cuda
 }
 
 template <int CG, int BN>
-cudaError_t launch_variant(int grid_ctas, const CUtensorMap &ta, const CUtensorMap &tb,
+cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap &ta, const CUtensorMap &tb,
                            const CUtensorMap &tc, const KernelParams &kp, cudaStream_t st)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas));
     cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = TileConfig<CG, BN>::SMEM_BYTES;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     if (CG == 2) {
@@ -364,6 +382,9 @@ gemm_status_t run(const void *A, const void *B, void *C, int64_t M, int64_t N, i
     kp.out_dtype = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_BF16 ? OUT_BF16 : OUT_F16);
     kp.b_mn_major = b_mn ? 1u : 0u;
     kp.direct_store = pl.direct_store ? 1u : 0u;
+    const Layout lay = layout_for(var, dtype_out);
+    kp.stages = lay.stages;
+    kp.staging_bytes = lay.staging_bytes;
     kp.C = C;
     kp.timeout_ns = (opts && opts->timeout_ms ? static_cast<uint64_t>(opts->timeout_ms) : DEFAULT_TIMEOUT_MS) *
                     1000000ull;
@@ -372,11 +393,11 @@ gemm_status_t run(const void *A, const void *B, void *C, int64_t M, int64_t N, i
 
     cudaError_t err;
     if (var.cg == 2 && var.bn == 256)
-        err = launch_variant<2, 256>(pl.grid_ctas, ta, tb, tc, kp, st);
+        err = launch_variant<2, 256>(pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
     else if (var.cg == 2 && var.bn == 224)
-        err = launch_variant<2, 224>(pl.grid_ctas, ta, tb, tc, kp, st);
+        err = launch_variant<2, 224>(pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
     else
-        err = launch_variant<1, 256>(pl.grid_ctas, ta, tb, tc, kp, st);
+        err = launch_variant<1, 256>(pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
     release();
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -426,14 +447,15 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype
     plan->block_m = 128 * var.cg;
     plan->block_n = var.bn;
     plan->block_k = BLOCK_K;
-    plan->stages = var.stages;
+    const Layout lay = layout_for(var, dtype_out);
+    plan->stages = static_cast<int32_t>(lay.stages);
     plan->num_tiles = pl.num_tiles;
     plan->grid_ctas = pl.grid_ctas;
     plan->group_m = pl.group_m;
     plan->realign_a = pl.realign_a;
     plan->realign_b = pl.realign_b;
     plan->direct_store = pl.direct_store;
-    plan->smem_bytes = var.smem;
+    plan->smem_bytes = static_cast<int32_t>(lay.smem);
     plan->num_sms = d->sms;
     return GEMM_OK;
 }
@@ -696,6 +718,9 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
     kp.out_dtype = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_BF16 ? OUT_BF16 : OUT_F16);
     kp.b_mn_major = b_mn ? 1u : 0u;
     kp.direct_store = pl.direct_store ? 1u : 0u;
+    const Layout lay = layout_for(var, dtype_out);
+    kp.stages = lay.stages;
+    kp.staging_bytes = lay.staging_bytes;
     kp.C = C;
     kp.timeout_ns = DEFAULT_TIMEOUT_MS * 1000000ull;
     kp.launch_id = g_next_id.fetch_add(1, std::memory_order_relaxed);
@@ -703,11 +728,11 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
 
     cudaError_t err;
     if (var.cg == 2 && var.bn == 256)
-        err = launch_variant<2, 256>(pl.grid_ctas, ta, tb, tc, kp, st);
+        err = launch_variant<2, 256>(pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
     else if (var.cg == 2 && var.bn == 224)
-        err = launch_variant<2, 224>(pl.grid_ctas, ta, tb, tc, kp, st);
+        err = launch_variant<2, 224>(pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
     else
-        err = launch_variant<1, 256>(pl.grid_ctas, ta, tb, tc, kp, st);
+        err = launch_variant<1, 256>(pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;

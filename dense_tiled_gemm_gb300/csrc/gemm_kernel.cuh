@@ -34,9 +34,13 @@
 // Resource Descriptors") relies on hardware range checks in the same way.
 //
 // Every wait is bounded (WaitCtx). Past the limit, a thread records the site
-// in the library's device status word and skips the remaining work. It
-// keeps the kernel's control flow, so every CTA barrier is still reached and
-// the kernel returns instead of hanging.
+// in the library's device status word and stops: from then on it issues no
+// work and no signal (no TMA, no MMA, no commit, no arrive), so it can never
+// push a barrier out of step. The roles that depend on it then block in their
+// own bounded waits, see the launch's timeout in the status word, and stop
+// too. Only operations already in flight are drained, with bounded waits. The
+// control flow is unchanged, so every CTA or cluster barrier is still reached
+// and the kernel returns instead of hanging.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -54,7 +58,8 @@ constexpr int EPI_WARP0 = 2;
 constexpr int TMEM_COLS = 512;       // two accumulators at columns 0 and 256
 constexpr int ACC_STRIDE = 256;
 constexpr int EPI_COLS = 32;         // accumulator columns per epilogue chunk
-constexpr int STAGING_BYTES = 32 * 128;  // one chunk: 32 rows x up to 128 bytes
+constexpr int MAX_STAGES = 8;
+constexpr int SMEM_LIMIT = 232448;   // 227 KB of dynamic shared memory per CTA
 
 enum : uint32_t { OUT_F16 = 0, OUT_BF16 = 1, OUT_F32 = 2 };
 
@@ -67,6 +72,7 @@ enum : uint32_t {
     SITE_MMA_DONE = 0x105,
     SITE_EPI_TMEM_FULL = 0x206,
     SITE_SELFTEST = 0x307,
+    SITE_SMEM_ALIGN = 0x008,   // dynamic shared memory not 1024-byte aligned: nothing ran
 };
 
 struct KernelParams {
@@ -76,6 +82,8 @@ struct KernelParams {
     uint32_t out_dtype;
     uint32_t b_mn_major;
     uint32_t direct_store;     // 1: write C with ordinary stores (unaligned C)
+    uint32_t stages;           // ring depth (2 .. MAX_STAGES)
+    uint32_t staging_bytes;    // one epilogue staging buffer: 32 rows x 32 columns of C
     void *C;                   // used by the direct-store path
     uint64_t timeout_ns;       // per-wait limit
     unsigned long long launch_id;
@@ -90,19 +98,19 @@ struct TileConfig {
     static constexpr int A_BYTES = BLOCK_M_CTA * BLOCK_K * 2;
     static constexpr int B_BYTES = BN_CTA * BLOCK_K * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // a multiple of 1024
-    static constexpr int STAGES = (CG == 1) ? 4 : 6;
-    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
-    static constexpr int STAGING_OFF = RING_BYTES;
-    static constexpr int STAGING_TOTAL = 4 * 2 * STAGING_BYTES;   // 4 warps x 2 buffers
-    static constexpr int BAR_OFF = STAGING_OFF + STAGING_TOTAL;
-    // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], mma_done
-    static constexpr int NUM_BARS = 2 * STAGES + 5;
-    static constexpr int TMEM_PTR_OFF = BAR_OFF + NUM_BARS * 8;
-    static constexpr int SMEM_BYTES = TMEM_PTR_OFF + 16 + 1024;   // + room to align the base
     static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
-    static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB per-CTA shared memory limit");
-    static constexpr uint32_t IDESC_M = BLOCK_M_CTA * CG;
 };
+
+// Dynamic shared memory, from a 1024-byte aligned base:
+//   ring      stages x {A 128x64, B BN_CTA x 64} tiles (128-byte swizzle)
+//   staging   4 epilogue warps x 2 buffers x staging_bytes (2 KB for 16-bit C, 4 KB for FP32 C)
+//   barriers  full[stages], empty[stages], tmem_full[2], tmem_empty[2], mma_done
+//   TMEM base address written by tcgen05.alloc
+__host__ __device__ constexpr uint32_t smem_bytes_for(uint32_t stage_bytes, uint32_t stages,
+                                                      uint32_t staging_bytes)
+{
+    return stages * stage_bytes + 8u * staging_bytes + (2u * stages + 5u) * 8u + 16u;
+}
 
 // ------------------------------------------------------------------ bounded waits
 struct WaitCtx {
@@ -275,9 +283,15 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
 {
     using Cfg = TileConfig<CG, BN>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;     // 128B-swizzled tiles need 1024 B alignment
-    uint8_t *smem = smem_raw + (base - raw);
+    const uint32_t base = smem_u32(smem_raw);
+    if (base & 1023u) {
+        // 128-byte-swizzled tiles need a 1024-byte aligned base; report and run nothing
+        if (threadIdx.x == 0)
+            record_timeout(p.status, p.launch_id, SITE_SMEM_ALIGN);
+        return;
+    }
+    uint8_t *smem = smem_raw;
+    const uint32_t stages = p.stages;
 
     const uint32_t warp = threadIdx.x / 32u;
     const uint32_t lane = threadIdx.x % 32u;
@@ -285,16 +299,18 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int cluster_id = static_cast<int>(blockIdx.x) / CG;
     const int num_clusters = static_cast<int>(gridDim.x) / CG;
 
-    const uint32_t bar0 = base + Cfg::BAR_OFF;
+    const uint32_t staging_off = stages * Cfg::STAGE_BYTES;
+    const uint32_t bar_off = staging_off + 8u * p.staging_bytes;
+    const uint32_t bar0 = base + bar_off;
     auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (Cfg::STAGES + s); };
-    auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cfg::STAGES + b); };
-    auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2 * Cfg::STAGES + 2 + b); };
-    const uint32_t done_bar = bar0 + 8u * (2 * Cfg::STAGES + 4);
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + Cfg::TMEM_PTR_OFF);
+    auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (stages + s); };
+    auto tfull_bar = [&](uint32_t b) { return bar0 + 8u * (2u * stages + b); };
+    auto tempty_bar = [&](uint32_t b) { return bar0 + 8u * (2u * stages + 2u + b); };
+    const uint32_t done_bar = bar0 + 8u * (2u * stages + 4u);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + bar_off + 8u * (2u * stages + 5u));
 
     if (threadIdx.x == 0) {
-        for (uint32_t s = 0; s < Cfg::STAGES; ++s) {
+        for (uint32_t s = 0; s < stages; ++s) {
             mbar_init(full_bar(s), 1);    // producer's arrive.expect_tx (+ bytes of both CTAs)
             mbar_init(empty_bar(s), 1);   // one tcgen05.commit
         }
@@ -360,7 +376,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         pend_mask |= 1u << s;
                         pend_par = (pend_par & ~(1u << s)) | (ph << s);
                     }
-                    if (++s == Cfg::STAGES) {
+                    if (++s == stages) {
                         s = 0;
                         ph ^= 1u;
                     }
@@ -369,7 +385,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
             // Leave no bulk copy into shared memory in flight: wait for the last
             // fill of every slot (the peer CTA's copies land on these barriers too).
             if (CG == 1 || rank == 0)
-                for (uint32_t s2 = 0; s2 < Cfg::STAGES; ++s2)
+                for (uint32_t s2 = 0; s2 < stages; ++s2)
                     if ((pend_mask >> s2) & 1u)
                         wait_drain<CG == 2>(full_bar(s2), (pend_par >> s2) & 1u, w.limit_ns, w.id, w.status,
                                            SITE_PRODUCER_DRAIN);
@@ -399,20 +415,22 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         for (uint32_t k = 0; k < BLOCK_K / UMMA_K; ++k)
                             mma_f16<CG>(d_tmem, a_desc + 2u * k, b_desc + b_step * k, p.idesc,
                                         (kb > 0 || k > 0) ? 1u : 0u);
+                        if constexpr (CG == 1)
+                            mma_commit(empty_bar(s));
+                        else
+                            mma_commit_pair(empty_bar(s), 0x3);
                     }
-                    if constexpr (CG == 1)
-                        mma_commit(empty_bar(s));
-                    else
-                        mma_commit_pair(empty_bar(s), 0x3);
-                    if (++s == Cfg::STAGES) {
+                    if (++s == stages) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
-                if constexpr (CG == 1)
-                    mma_commit(tfull_bar(acc));
-                else
-                    mma_commit_pair(tfull_bar(acc), 0x3);
+                if (!w.aborted) {
+                    if constexpr (CG == 1)
+                        mma_commit(tfull_bar(acc));
+                    else
+                        mma_commit_pair(tfull_bar(acc), 0x3);
+                }
                 if (++acc == 2) {
                     acc = 0;
                     acc_ph ^= 1u;
@@ -428,7 +446,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
     } else {
         // ------------------------------------------------------------ epilogue
         const uint32_t quarter = warp & 3u;      // the TMEM lane quarter this warp may access
-        const uint32_t staging = base + Cfg::STAGING_OFF + (warp - EPI_WARP0) * 2u * STAGING_BYTES;
+        const uint32_t staging = base + staging_off + (warp - EPI_WARP0) * 2u * p.staging_bytes;
+        const uint64_t c_policy = l2_evict_first_policy();   // C is written once: keep A and B in L2
         uint32_t acc = 0, acc_ph = 0, sb = 0;
         for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
             int m_blk, n_blk;
@@ -452,7 +471,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     // accumulator fully read: hand it back to the MMA issuer
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) {
+                    if (lane == 0 && !skip) {
                         if constexpr (CG == 1)
                             mbar_arrive_local(tempty_bar(acc));
                         else
@@ -466,7 +485,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     store_row_direct(p, row0 + static_cast<int>(lane), gcol, v);
                     continue;
                 }
-                const uint32_t buf = staging + sb * STAGING_BYTES;
+                const uint32_t buf = staging + sb * p.staging_bytes;
                 if (lane == 0)
                     bulk_wait_group_read<1>();   // the store that last used `buf` has read it
                 __syncwarp();
@@ -474,7 +493,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && row0 < p.M) {
-                    tma_store_2d(&tmap_c, buf, gcol, row0);
+                    tma_store_2d_hint(&tmap_c, buf, gcol, row0, c_policy);
                     bulk_commit_group();
                 }
                 sb ^= 1u;

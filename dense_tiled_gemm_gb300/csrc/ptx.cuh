@@ -149,6 +149,24 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sr
                  : "memory");
 }
 
+// Same store with an L2 cache-policy hint (a policy from createpolicy).
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, uint32_t src, int32_t c0,
+                                                  int32_t c1, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint"
+                 " [%0, {%2, %3}], [%1], %4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "l"(policy)
+                 : "memory");
+}
+
+// L2 policy under which the accessed lines are the first to be evicted.
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    return policy;
+}
+
 __device__ __forceinline__ void bulk_commit_group()
 {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
