@@ -29,7 +29,8 @@ GEMM_ERR_TIMEOUT, GEMM_ERR_NO_DEVICE, GEMM_ERR_OUT_OF_MEMORY = 4, 5, 6
 class GemmOptions(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int32), ("block_n", ctypes.c_int32),
                 ("max_clusters", ctypes.c_int32), ("group_m", ctypes.c_int32),
-                ("timeout_ms", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("timeout_ms", ctypes.c_int32), ("k_stage", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 class GemmPlan(ctypes.Structure):

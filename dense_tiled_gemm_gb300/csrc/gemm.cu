@@ -30,22 +30,31 @@ namespace {
 
 constexpr int MAX_DEVICES = 64;
 constexpr uint64_t DEFAULT_TIMEOUT_MS = 2000;
+// K per ring stage, unless gemm_options_t.k_stage says otherwise: 128 for CTA
+// pairs (8 MMAs per barrier wait; the MMA issuer's wait costs ~60-100 cycles
+// of tensor idle, so fewer waits per MMA pay), 64 for single CTAs (a 128-deep
+// stage leaves room for only two of them).
+int default_k_slabs(int cg) { return cg == 2 ? 2 : 1; }
 
 struct Variant {
     int cg;
     int bn;
-    int stage_bytes;   // one ring slot: A and B tiles of one k-block (per CTA)
+    int ks;            // K slabs (of 64) per ring stage
+    int stage_bytes;   // one ring slot: A and B tiles of one stage (per CTA)
     const void *fn;
     bool b_mn_ok;      // MN-major B needs 64-column TMA boxes per CTA
 };
 
+template <int CG, int BN, int KS>
+constexpr Variant variant(bool b_mn_ok)
+{
+    return {CG, BN, KS, TileConfig<CG, BN, KS>::STAGE_BYTES,
+            reinterpret_cast<const void *>(&gemm_tcgen05_kernel<CG, BN, KS>), b_mn_ok};
+}
+
 const Variant kVariants[] = {
-    {2, 256, TileConfig<2, 256>::STAGE_BYTES, reinterpret_cast<const void *>(&gemm_tcgen05_kernel<2, 256>),
-     true},
-    {2, 224, TileConfig<2, 224>::STAGE_BYTES, reinterpret_cast<const void *>(&gemm_tcgen05_kernel<2, 224>),
-     false},
-    {1, 256, TileConfig<1, 256>::STAGE_BYTES, reinterpret_cast<const void *>(&gemm_tcgen05_kernel<1, 256>),
-     true},
+    variant<2, 256, 1>(true),  variant<2, 224, 1>(false), variant<1, 256, 1>(true),
+    variant<2, 256, 2>(true),  variant<2, 224, 2>(false), variant<1, 256, 2>(true),
 };
 constexpr int NUM_VARIANTS = sizeof(kVariants) / sizeof(kVariants[0]);
 
@@ -177,6 +186,8 @@ gemm_status_t validate(const void *A, const void *B, const void *C, int64_t M, i
             return GEMM_ERR_INVALID_ARG;
         if (o->block_n != 0 && o->block_n != 224 && o->block_n != 256)
             return GEMM_ERR_UNSUPPORTED;
+        if (o->k_stage != 0 && o->k_stage != 64 && o->k_stage != 128)
+            return o->k_stage < 0 ? GEMM_ERR_INVALID_ARG : GEMM_ERR_UNSUPPORTED;
     }
     return GEMM_OK;
 }
@@ -210,6 +221,8 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
             continue;
         if (o && o->block_n && o->block_n != var.bn)
             continue;
+        if (var.ks != ((o && o->k_stage) ? o->k_stage / BLOCK_K : default_k_slabs(var.cg)))
+            continue;
         if (b_mn && !var.b_mn_ok)
             continue;
         int units = d.max_units[v];
@@ -238,7 +251,7 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
     if (tiles > INT_MAX)
         return GEMM_ERR_UNSUPPORTED;
     pl->num_tiles = static_cast<int>(tiles);
-    pl->num_kb = static_cast<int>((K + BLOCK_K - 1) / BLOCK_K);
+    pl->num_kb = static_cast<int>((K + BLOCK_K * var.ks - 1) / (BLOCK_K * var.ks));
     pl->grid_ctas = static_cast<int>(std::min<int64_t>(tiles, units)) * var.cg;
     pl->group_m = (o && o->group_m) ? o->group_m : 8;
     pl->realign_a = misaligned(A, K, 2);
@@ -292,7 +305,7 @@ gemm_status_t realign(const void *src, int64_t rows, int64_t cols, int sms, cuda
     return GEMM_OK;
 }
 
-template <int CG, int BN>
+template <int CG, int BN, int KS>
 cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap &ta, const CUtensorMap &tb,
                            const CUtensorMap &tc, const KernelParams &kp, cudaStream_t st)
 {
@@ -310,7 +323,23 @@ cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap &ta, 
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<CG, BN>, ta, tb, tc, kp);
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<CG, BN, KS>, ta, tb, tc, kp);
+}
+
+cudaError_t launch_any(const Variant &v, int grid_ctas, uint32_t smem, const CUtensorMap &ta,
+                       const CUtensorMap &tb, const CUtensorMap &tc, const KernelParams &kp, cudaStream_t st)
+{
+#define DTG_LAUNCH(CG, BN, KS)                                                                     \
+    if (v.cg == CG && v.bn == BN && v.ks == KS)                                                    \
+        return launch_variant<CG, BN, KS>(grid_ctas, smem, ta, tb, tc, kp, st);
+    DTG_LAUNCH(2, 256, 1)
+    DTG_LAUNCH(2, 224, 1)
+    DTG_LAUNCH(1, 256, 1)
+    DTG_LAUNCH(2, 256, 2)
+    DTG_LAUNCH(2, 224, 2)
+    DTG_LAUNCH(1, 256, 2)
+#undef DTG_LAUNCH
+    return cudaErrorInvalidValue;
 }
 
 gemm_status_t run(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
@@ -391,13 +420,7 @@ gemm_status_t run(const void *A, const void *B, void *C, int64_t M, int64_t N, i
     kp.launch_id = g_next_id.fetch_add(1, std::memory_order_relaxed);
     kp.status = d->status;
 
-    cudaError_t err;
-    if (var.cg == 2 && var.bn == 256)
-        err = launch_variant<2, 256>(pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
-    else if (var.cg == 2 && var.bn == 224)
-        err = launch_variant<2, 224>(pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
-    else
-        err = launch_variant<1, 256>(pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
+    const cudaError_t err = launch_any(var, pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
     release();
     if (err != cudaSuccess) {
         cudaGetLastError();
@@ -446,7 +469,7 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype
     plan->cta_group = var.cg;
     plan->block_m = 128 * var.cg;
     plan->block_n = var.bn;
-    plan->block_k = BLOCK_K;
+    plan->block_k = BLOCK_K * var.ks;
     const Layout lay = layout_for(var, dtype_out);
     plan->stages = static_cast<int32_t>(lay.stages);
     plan->num_tiles = pl.num_tiles;
@@ -726,13 +749,7 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
     kp.launch_id = g_next_id.fetch_add(1, std::memory_order_relaxed);
     kp.status = d->status;
 
-    cudaError_t err;
-    if (var.cg == 2 && var.bn == 256)
-        err = launch_variant<2, 256>(pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
-    else if (var.cg == 2 && var.bn == 224)
-        err = launch_variant<2, 224>(pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
-    else
-        err = launch_variant<1, 256>(pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
+    const cudaError_t err = launch_any(var, pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
     if (err != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;

@@ -50,7 +50,7 @@
 
 namespace dtg {
 
-constexpr int BLOCK_K = 64;          // 64 x 16-bit = one 128-byte swizzle row
+constexpr int BLOCK_K = 64;          // one K slab: 64 x 16-bit = one 128-byte swizzle row
 constexpr int BLOCK_M_CTA = 128;     // accumulator rows per CTA = TMEM lanes
 constexpr int UMMA_K = 16;           // K of one kind::f16 tcgen05.mma
 constexpr int NUM_THREADS = 192;     // producer warp, MMA warp, 4 epilogue warps
@@ -90,19 +90,25 @@ struct KernelParams {
     unsigned long long *status;  // [0] first timed-out launch, [1] site, [2] last timed-out launch
 };
 
-template <int CG, int BN>
+// KS = K slabs per ring stage. One slab is a 64-wide K strip of A and B in the
+// 128-byte swizzle layout (4 MMAs of K = 16). A stage holds KS slabs of A then
+// KS slabs of B, so one barrier wait on the MMA thread covers 4 x KS MMAs.
+template <int CG, int BN, int KS>
 struct TileConfig {
     static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
+    static_assert(KS == 1 || KS == 2, "one or two K slabs per stage");
     static constexpr int BN_CTA = BN / CG;   // B rows (K-major) or columns (MN-major) per CTA
     static_assert(BN % (16 * CG) == 0 && BN <= 256 && BN_CTA % 8 == 0, "invalid tile width");
-    static constexpr int A_BYTES = BLOCK_M_CTA * BLOCK_K * 2;
-    static constexpr int B_BYTES = BN_CTA * BLOCK_K * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // a multiple of 1024
-    static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned");
+    static constexpr int A_SLAB = BLOCK_M_CTA * BLOCK_K * 2;
+    static constexpr int B_SLAB = BN_CTA * BLOCK_K * 2;
+    static constexpr int A_BYTES = KS * A_SLAB;
+    static constexpr int STAGE_BYTES = KS * (A_SLAB + B_SLAB);
+    static constexpr int STAGE_K = KS * BLOCK_K;
+    static_assert(A_SLAB % 1024 == 0 && B_SLAB % 1024 == 0, "slabs must stay 1024-byte aligned");
 };
 
 // Dynamic shared memory, from a 1024-byte aligned base:
-//   ring      stages x {A 128x64, B BN_CTA x 64} tiles (128-byte swizzle)
+//   ring      stages x {KS slabs of A 128x64, KS slabs of B BN_CTA x 64} (128-byte swizzle)
 //   staging   4 epilogue warps x 2 buffers x staging_bytes (2 KB for 16-bit C, 4 KB for FP32 C)
 //   barriers  full[stages], empty[stages], tmem_full[2], tmem_empty[2], mma_done
 //   TMEM base address written by tcgen05.alloc
@@ -275,13 +281,13 @@ __device__ __forceinline__ void store_row_direct(const KernelParams &p, int row,
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int CG, int BN>
+template <int CG, int BN, int KS>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_c, const KernelParams p)
 {
-    using Cfg = TileConfig<CG, BN>;
+    using Cfg = TileConfig<CG, BN, KS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     if (base & 1023u) {
@@ -351,27 +357,37 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     if (!w.aborted) {
                         const uint32_t a_dst = base + s * Cfg::STAGE_BYTES;
                         const uint32_t b_dst = a_dst + Cfg::A_BYTES;
-                        const int k0 = kb * BLOCK_K;
+                        const int k0 = kb * Cfg::STAGE_K;
                         if constexpr (CG == 1) {
                             const uint32_t bar = full_bar(s);
                             mbar_arrive_expect_tx(bar, Cfg::STAGE_BYTES);
-                            tma_load_2d(a_dst, &tmap_a, bar, k0, a_row);
-                            if (!p.b_mn_major)
-                                tma_load_2d(b_dst, &tmap_b, bar, k0, b_off);
-                            else
-                                for (int j = 0; j < Cfg::BN_CTA / 64; ++j)
-                                    tma_load_2d(b_dst + j * 8192u, &tmap_b, bar, b_off + 64 * j, k0);
+#pragma unroll
+                            for (int j = 0; j < KS; ++j) {
+                                const int kj = k0 + j * BLOCK_K;
+                                tma_load_2d(a_dst + j * Cfg::A_SLAB, &tmap_a, bar, kj, a_row);
+                                const uint32_t bj = b_dst + j * Cfg::B_SLAB;
+                                if (!p.b_mn_major)
+                                    tma_load_2d(bj, &tmap_b, bar, kj, b_off);
+                                else
+                                    for (int i = 0; i < Cfg::BN_CTA / 64; ++i)
+                                        tma_load_2d(bj + i * 8192u, &tmap_b, bar, b_off + 64 * i, kj);
+                            }
                         } else {
                             // both CTAs' boxes complete on the even CTA's full barrier
                             const uint32_t bar = map_to_cta(full_bar(s), 0);
                             if (rank == 0)
                                 mbar_arrive_expect_tx(full_bar(s), 2u * Cfg::STAGE_BYTES);
-                            tma_load_2d_pair(a_dst, &tmap_a, bar, k0, a_row);
-                            if (!p.b_mn_major)
-                                tma_load_2d_pair(b_dst, &tmap_b, bar, k0, b_off);
-                            else
-                                for (int j = 0; j < Cfg::BN_CTA / 64; ++j)
-                                    tma_load_2d_pair(b_dst + j * 8192u, &tmap_b, bar, b_off + 64 * j, k0);
+#pragma unroll
+                            for (int j = 0; j < KS; ++j) {
+                                const int kj = k0 + j * BLOCK_K;
+                                tma_load_2d_pair(a_dst + j * Cfg::A_SLAB, &tmap_a, bar, kj, a_row);
+                                const uint32_t bj = b_dst + j * Cfg::B_SLAB;
+                                if (!p.b_mn_major)
+                                    tma_load_2d_pair(bj, &tmap_b, bar, kj, b_off);
+                                else
+                                    for (int i = 0; i < Cfg::BN_CTA / 64; ++i)
+                                        tma_load_2d_pair(bj + i * 8192u, &tmap_b, bar, b_off + 64 * i, kj);
+                            }
                         }
                         pend_mask |= 1u << s;
                         pend_par = (pend_par & ~(1u << s)) | (ph << s);
@@ -409,12 +425,19 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     tc_fence_after_sync();
                     if (!w.aborted) {
                         const uint32_t a_addr = base + s * Cfg::STAGE_BYTES;
-                        const uint64_t a_desc = smem_desc_sw128(a_addr, 16u, 1024u);
-                        const uint64_t b_desc = smem_desc_sw128(a_addr + Cfg::A_BYTES, b_lbo, 1024u);
 #pragma unroll
-                        for (uint32_t k = 0; k < BLOCK_K / UMMA_K; ++k)
-                            mma_f16<CG>(d_tmem, a_desc + 2u * k, b_desc + b_step * k, p.idesc,
-                                        (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int j = 0; j < KS; ++j) {
+                            // a slab wholly past K holds only TMA zero fill: skip its MMAs
+                            if (j > 0 && kb * Cfg::STAGE_K + j * BLOCK_K >= p.K)
+                                break;
+                            const uint64_t a_desc = smem_desc_sw128(a_addr + j * Cfg::A_SLAB, 16u, 1024u);
+                            const uint64_t b_desc = smem_desc_sw128(a_addr + Cfg::A_BYTES + j * Cfg::B_SLAB,
+                                                                    b_lbo, 1024u);
+#pragma unroll
+                            for (uint32_t k = 0; k < BLOCK_K / UMMA_K; ++k)
+                                mma_f16<CG>(d_tmem, a_desc + 2u * k, b_desc + b_step * k, p.idesc,
+                                            (kb > 0 || j > 0 || k > 0) ? 1u : 0u);
+                        }
                         if constexpr (CG == 1)
                             mma_commit(empty_bar(s));
                         else

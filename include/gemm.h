@@ -99,6 +99,7 @@ gemm_status_t gemm(const void *A, const void *B, void *C,
  *                 makes each CTA loop over many tiles.
  *   group_m       raster group height in tiles, for the swizzled tile order.
  *   timeout_ms    per-wait limit inside the kernel (default 2000).
+ *   k_stage       K depth of one shared-memory ring stage: 64 or 128.
  */
 typedef struct {
     int32_t cta_group;
@@ -106,7 +107,8 @@ typedef struct {
     int32_t max_clusters;
     int32_t group_m;
     int32_t timeout_ms;
-    int32_t reserved[3];
+    int32_t k_stage;
+    int32_t reserved[2];
 } gemm_options_t;
 
 /* gemm with overrides. opts may be NULL. An unsupported override combination
@@ -124,7 +126,7 @@ typedef struct {
     int32_t cta_group;     /* CTAs per output tile */
     int32_t block_m;       /* rows per output tile (128 * cta_group) */
     int32_t block_n;       /* columns per output tile */
-    int32_t block_k;       /* K per pipeline stage (64) */
+    int32_t block_k;       /* K per pipeline stage (64 or 128) */
     int32_t stages;        /* shared-memory ring depth */
     int32_t num_tiles;     /* output tiles */
     int32_t grid_ctas;     /* persistent CTAs launched */

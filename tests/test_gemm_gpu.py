@@ -126,6 +126,30 @@ def test_many_tiles_per_cta(dtg, opts):
     exact_case(dtg, 1024, 1024, 448, "f16", "k", options=opts, seed=4)
 
 
+# ---------------------------------------------------------------- 128-deep ring stages
+K128 = [{"cta_group": 2, "k_stage": 128}, {"cta_group": 2, "block_n": 224, "k_stage": 128},
+        {"cta_group": 1, "k_stage": 128}, {"cta_group": 2, "k_stage": 128, "max_clusters": 2}]
+
+
+@pytest.mark.parametrize("opts", K128, ids=["cta2", "cta2_n224", "cta1", "cta2_two_pairs"])
+@pytest.mark.parametrize("layout_b", ["k", "mn"])
+@pytest.mark.parametrize("K", [960, 1000, 64])
+def test_k_stage_128_integer_exact(dtg, opts, layout_b, K):
+    """Two 64-wide K slabs per stage. K = 960 leaves the last stage's second slab
+    wholly past K (its MMAs are skipped); K = 1000 leaves it partly filled."""
+    if layout_b == "mn" and opts.get("block_n") == 224:
+        pytest.skip("224-wide tiles need a K-major B")
+    exact_case(dtg, 640, 512, K, "f16", layout_b, options=opts, seed=K)
+
+
+def test_k_stage_128_workload(dtg):
+    w = workloads.WORKLOADS["gemm_4096x4096x8192_f16"]
+    A, B = workloads.workload_operands(w)
+    C = run_gpu(dtg, A, B, w.layout_b, w.dtype_out, options={"k_stage": 128})
+    compare(C, A, B, w.M, w.N, w.K, w.dtype_in, w.dtype_out, w.layout_b,
+            rows=workloads.sample_rows(w.M, 32, w.seed))
+
+
 # ---------------------------------------------------------------- ragged shapes
 RAGGED = [
     (1, 1, 1), (7, 9, 3), (127, 129, 65), (129, 127, 63), (255, 257, 200), (300, 500, 130),
@@ -235,7 +259,7 @@ def test_from_host_matches_device(dtg):
 
 def test_plan_reports_launch(dtg):
     p = dtg.gemm_plan(4096, 4096, 8192)
-    assert p["cta_group"] == 2 and p["block_k"] == 64 and p["num_sms"] > 0
+    assert p["cta_group"] == 2 and p["block_k"] == 128 and p["num_sms"] > 0
     assert p["grid_ctas"] % 2 == 0 and p["realign_a"] == 0 and p["direct_store"] == 0
     q = dtg.gemm_plan(3000, 5000, 2050, dtype_in=torch.bfloat16, dtype_out=torch.float32,
                       layout_b="mn")
