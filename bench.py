@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--compare-cublas", action="store_true",
+                    help="also time torch.matmul (cuBLAS) the same way, as a labelled comparison")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
@@ -244,6 +246,34 @@ def run_reference(args):
     return 0
 
 
+def time_cublas(As, Bs, Cs, w, n_sets, args, stream, smi_id, pg, dev) -> dict:
+    """torch.matmul (cuBLAS) on the same rotating operands, timed the same way.
+    A comparison only: nothing on the product path calls it."""
+    def step(i):
+        j = i % n_sets
+        Bj = Bs[j].t() if w.layout_b == "k" else Bs[j]
+        torch.matmul(As[j], Bj, out=Cs[j])
+    for i in range(args.warmup):
+        step(i)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(smi_id)
+    sampler.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(args.warmup + i)
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    region_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), pg, dev)
+    kernel_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    return {"impl": "torch.matmul (cuBLAS)", "value": w.flops * args.steps / (region_ms * 1e-3) / 1e12,
+            "unit": "TFLOP/s", "kernel_ms": kernel_ms, "clocks": clocks}
+
+
 # ---------------------------------------------------------------------------- our arm
 def run_ours(args):
     world, rank, local = dist_env()
@@ -319,6 +349,10 @@ def run_ours(args):
                          layout_b=w.layout_b, a_ptr=As[0].data_ptr(), b_ptr=Bs[0].data_ptr(),
                          c_ptr=Cs[0].data_ptr())
 
+    cublas = None
+    if args.compare_cublas:
+        cublas = time_cublas(As, Bs, Cs, w, n_sets, args, stream, smi_id, pg, dev)
+
     e2e = None
     if not args.no_e2e:
         Ah = A0.pin_memory()
@@ -364,6 +398,7 @@ def run_ours(args):
             "gpu_launches": launches,
             "e2e": e2e,
             "cpu_baseline": cpu,
+            "cublas_comparison": cublas,
         }
         line["roofline"]["frac_of_nominal"] = achieved / NOMINAL_DENSE_TFLOPS
         if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
