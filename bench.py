@@ -10,7 +10,8 @@ FP16-in / FP16-out workload (FP32 accumulation), the compute-bound shape of
 
 Timing: W untimed warm-up steps, then exactly K steps between a barrier and
 torch.cuda.synchronize() on both sides. CUDA events are recorded on the
-launching stream around every launch. Operands rotate over enough
+launching stream at both ends of the timed region; the mean launch duration
+is the region time over K. Operands rotate over enough
 (A, B, C) sets to exceed twice the L2 size, so every step reads from HBM.
 SM clocks are sampled with nvidia-smi during the timed region.
 Under torchrun (N > 1) every rank runs its own replica; the time is the
@@ -249,28 +250,42 @@ def run_reference(args):
 def time_cublas(As, Bs, Cs, w, n_sets, args, stream, smi_id, pg, dev) -> dict:
     """torch.matmul (cuBLAS) on the same rotating operands, timed the same way.
     A comparison only: nothing on the product path calls it."""
+    same_dtype = Cs[0].dtype == As[0].dtype
+    how = "torch.matmul (cuBLAS)"
+    if not same_dtype:
+        try:   # cuBLAS writing the wider output type directly, where this torch has it
+            torch.mm(As[0], Bs[0].t() if w.layout_b == "k" else Bs[0], out_dtype=Cs[0].dtype)
+            how = f"torch.mm out_dtype={Cs[0].dtype} (cuBLAS)"
+        except (TypeError, RuntimeError):
+            how = f"torch.matmul (cuBLAS), output in {As[0].dtype}: no FP32-output path in this torch"
+
     def step(i):
         j = i % n_sets
         Bj = Bs[j].t() if w.layout_b == "k" else Bs[j]
-        torch.matmul(As[j], Bj, out=Cs[j])
+        if same_dtype:
+            torch.matmul(As[j], Bj, out=Cs[j])
+        elif how.startswith("torch.mm"):
+            torch.mm(As[j], Bj, out_dtype=Cs[j].dtype)
+        else:
+            torch.matmul(As[j], Bj)
     for i in range(args.warmup):
         step(i)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(smi_id)
     sampler.start()
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
+    ev_start.record(stream)
     for i in range(args.steps):
-        starts[i].record(stream)
         step(args.warmup + i)
-        ends[i].record(stream)
+    ev_end.record(stream)
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
-    region_ms = max_over_ranks(starts[0].elapsed_time(ends[-1]), pg, dev)
-    kernel_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
-    return {"impl": "torch.matmul (cuBLAS)", "value": w.flops * args.steps / (region_ms * 1e-3) / 1e12,
+    region_ms = max_over_ranks(ev_start.elapsed_time(ev_end), pg, dev)
+    kernel_ms = region_ms / args.steps
+    return {"impl": how, "value": w.flops * args.steps / (region_ms * 1e-3) / 1e12,
             "unit": "TFLOP/s", "kernel_ms": kernel_ms, "clocks": clocks}
 
 
@@ -311,8 +326,12 @@ def run_ours(args):
     if status != dtg.GEMM_OK:
         raise RuntimeError(f"device status {dtg.gemm_status_string(status)} site {detail:#x}")
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # Events only at the two ends of the timed region: an event recorded between
+    # two launches would stop the next launch from overlapping the previous one.
+    # Only this kernel runs on the stream here, so the mean launch duration is
+    # the region time over the step count.
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
     try:
         smi_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:  # noqa: BLE001  (older torch: fall back to the CUDA index)
@@ -323,10 +342,10 @@ def run_ours(args):
         pg.barrier()
     torch.cuda.synchronize(dev)
     launches0 = dtg.gemm_launch_count()
+    ev_start.record(stream)
     for i in range(args.steps):
-        starts[i].record(stream)
         step(args.warmup + i)
-        ends[i].record(stream)
+    ev_end.record(stream)
     torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
@@ -336,8 +355,8 @@ def run_ours(args):
     if status != dtg.GEMM_OK:
         raise RuntimeError(f"device status {dtg.gemm_status_string(status)} site {detail:#x}")
 
-    region_ms = starts[0].elapsed_time(ends[-1])
-    kernel_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    region_ms = ev_start.elapsed_time(ev_end)
+    kernel_ms = region_ms / args.steps
     region_ms = max_over_ranks(region_ms, pg, dev)
     flops_step = float(w.flops)
     value = whole_job_tflops(world, flops_step, args.steps, region_ms * 1e-3)

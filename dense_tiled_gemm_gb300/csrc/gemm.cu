@@ -314,14 +314,20 @@ cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap &ta, 
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    // Programmatic stream serialisation lets this grid's CTAs start their setup
+    // while the previous grid on the stream drains; the kernel waits
+    // (griddepcontrol.wait) before touching global memory.
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (CG == 2) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<CG, BN, KS>, ta, tb, tc, kp);
 }

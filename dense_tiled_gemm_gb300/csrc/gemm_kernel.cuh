@@ -338,6 +338,11 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
         __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
+    // Launched with programmatic stream serialisation: the setup above may run
+    // while the previous grid on the stream drains. Nothing in global memory is
+    // read or written before that grid has completed.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     WaitCtx w{p.timeout_ns, p.launch_id, p.status, false};
 

@@ -53,6 +53,20 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t cta)
     return r;
 }
 
+// ------------------------------------------------------------------ grid dependencies
+// Programmatic dependent launch: block until the grids this one depends on
+// (earlier work on the stream) have completed and their memory is visible.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next grid on the stream be scheduled before this one finishes.
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
