@@ -8,7 +8,10 @@ nothing from there. The two meet only in the seeded input generator
 
 ``gemm_ref`` is a ctypes wrapper around ``gemm_oracle.c``. It implements the
 plain definition C[i][j] = sum_k a[i][k]*b[k][j] in FP64 over the exact
-FP16/BF16 operand values (k ascending), plus C_abs[i][j] = sum_k |a·b|.
+FP16/BF16 or FP8 (E4M3/E5M2) operand values (k ascending), plus
+C_abs[i][j] = sum_k |a·b|. FP8 operands carry the identity block scale
+(1.0) of "Porting High-Performance HIP Kernels to FlyDSL", section "A More
+Complex Kernel", so their products are the plain products.
 It follows "Two Waves, One Stage Apart" (opening paragraph: a tiled GEMM
 sums operand-tile products) and counts 2·M·N·K flops as in that page's
 Table 1 caption.
@@ -28,9 +31,11 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F16, BF16 = 0, 1
+F16, BF16, E4M3, E5M2 = 0, 1, 3, 4
 K_MAJOR, MN_MAJOR = 0, 1
-_DTYPE = {"f16": F16, "bf16": BF16}
+_DTYPE = {"f16": F16, "bf16": BF16, "e4m3": E4M3, "e5m2": E5M2}
+# numpy type of the raw operand patterns for each input type
+_STORAGE = {"f16": np.uint16, "bf16": np.uint16, "e4m3": np.uint8, "e5m2": np.uint8}
 _LAYOUT = {"k": K_MAJOR, "mn": MN_MAJOR}
 
 
@@ -59,6 +64,9 @@ def load_library(path: str):
     lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
     lib.oracle_decode_bf16.restype = ctypes.c_double
     lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
+    for name in ("oracle_decode_e4m3", "oracle_decode_e5m2"):
+        getattr(lib, name).restype = ctypes.c_double
+        getattr(lib, name).argtypes = [ctypes.c_uint8]
     return lib
 
 
@@ -78,10 +86,11 @@ def host_threads() -> int:
 
 
 def decode(bits, dtype: str, lib=None) -> np.ndarray:
-    """Decode 16-bit FP16/BF16 patterns to FP64 with the oracle's own decoder."""
+    """Decode FP16/BF16 (16-bit) or E4M3/E5M2 (8-bit) patterns to FP64 with
+    the oracle's own decoders."""
     lib = lib or _load()
-    fn = lib.oracle_decode_bf16 if dtype == "bf16" else lib.oracle_decode_f16
-    flat = np.asarray(bits, dtype=np.uint16).ravel()
+    fn = getattr(lib, f"oracle_decode_{dtype}")
+    flat = np.asarray(bits, dtype=_STORAGE[dtype]).ravel()
     return np.array([fn(int(b)) for b in flat], dtype=np.float64).reshape(np.shape(bits))
 
 
@@ -90,14 +99,15 @@ def gemm_ref(A_bits: np.ndarray, B_bits: np.ndarray, M: int, N: int, K: int,
              lib=None):
     """FP64 reference rows of C = A·B and of C_abs = sum_k |a·b|.
 
-    A_bits: uint16 M×K (row-major). B_bits: uint16 N×K for layout_b="k",
-    K×N for layout_b="mn". ``rows``: output rows to compute (None = all).
+    A_bits: M×K patterns (row-major), uint16 for "f16"/"bf16" and uint8 for
+    "e4m3"/"e5m2". B_bits: N×K for layout_b="k", K×N for layout_b="mn".
+    ``rows``: output rows to compute (None = all).
     Returns (C, C_abs), each len(rows)×N (or M×N) float64. ``lib`` selects
     another compiled copy of the oracle (the tests' planted-mistake checks).
     """
     lib = lib or _load()
-    A = np.ascontiguousarray(A_bits, dtype=np.uint16)
-    B = np.ascontiguousarray(B_bits, dtype=np.uint16)
+    A = np.ascontiguousarray(A_bits, dtype=_STORAGE[dtype_in])
+    B = np.ascontiguousarray(B_bits, dtype=_STORAGE[dtype_in])
     if A.size != M * K or B.size != N * K:
         raise ValueError("operand sizes do not match M, N, K")
     if rows is None:

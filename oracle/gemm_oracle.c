@@ -13,17 +13,26 @@
  *     C[i][j] = sum_{k=0}^{K-1} a[i][k] * b[k][j]
  *
  * and the oracle evaluates it in FP64, with k ascending, over the exact
- * values of the FP16/BF16 operands. It also returns
+ * values of the FP16/BF16 or FP8 (E4M3, E5M2) operands. It also returns
  *
  *     C_abs[i][j] = sum_k |a[i][k] * b[k][j]|
  *
  * which the acceptance bound uses. Every product of two FP16 values (11-bit
- * significands) or two BF16 values (8-bit significands) is exact in FP64, so
- * the only rounding is in the FP64 running sum. No blocking or reordering:
- * one plain i-k-j loop per output row, with rows shared among threads.
+ * significands), two BF16 values (8-bit) or two FP8 values (4-bit E4M3,
+ * 3-bit E5M2) is exact in FP64, so the only rounding is in the FP64 running
+ * sum. No blocking or reordering: one plain i-k-j loop per output row, with
+ * rows shared among threads.
+ *
+ * FP8 inputs follow "Porting High-Performance HIP Kernels to FlyDSL"
+ * (section "A More Complex Kernel"): E4M3 operands, FP32 accumulation and a
+ * block scale of 1.0 on every operand (the identity scale), so the scaled
+ * product is the plain product and the definition above is unchanged. The
+ * same page's BF8 sibling (E5M2, named among the FP8/BF8 formats of the RDNA
+ * instruction-set pages) is decoded too.
  *
  * Operand storage (the reading taken for the "K-major" wording of the pages'
- * kernels, whose B operand is passed transposed, "B_T"):
+ * kernels, whose B operand is passed transposed, "B_T"); elements are 16-bit
+ * words for FP16/BF16 and bytes for FP8:
  *   A       : M x K row-major, a[i][k] at A[i*K + k]
  *   B k-major : N x K, K contiguous, b[k][j] at B[j*K + k]
  *   B mn-major: K x N, N contiguous, b[k][j] at B[k*N + j]
@@ -38,7 +47,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORACLE_F16 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 3, ORACLE_E5M2 = 4 };
 enum { ORACLE_K_MAJOR = 0, ORACLE_MN_MAJOR = 1 };
 
 /* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
@@ -78,16 +87,66 @@ double oracle_decode_bf16(uint16_t h)
     return sign ? -v : v;
 }
 
-static double decode(uint16_t h, int dtype)
+/* FP8 E4M3 in its "FN" form (finite, NaN only): 1 sign bit, 4 exponent bits
+ * (bias 7), 3 fraction bits, no infinities; S.1111.111 is NaN, so the largest
+ * finite magnitude is 1.75 * 2^8 = 448.
+ * Normal:    (8 + f) * 2^(e - 7 - 3)
+ * Subnormal: f * 2^(1 - 7 - 3) = f * 2^-9                                   */
+double oracle_decode_e4m3(uint8_t h)
 {
-    return dtype == ORACLE_BF16 ? oracle_decode_bf16(h) : oracle_decode_f16(h);
+    int sign = (h >> 7) & 1;
+    int e = (h >> 3) & 0xf;
+    int f = h & 0x7;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -9);
+    else if (e == 0xf && f == 0x7)
+        v = NAN;
+    else
+        v = ldexp((double)(8 + f), e - 10);
+    return sign ? -v : v;
+}
+
+/* FP8 E5M2: 1 sign bit, 5 exponent bits (bias 15), 2 fraction bits, with
+ * IEEE infinities and NaNs at exponent 31; largest finite 1.75 * 2^15.
+ * Normal:    (4 + f) * 2^(e - 15 - 2)
+ * Subnormal: f * 2^(1 - 15 - 2) = f * 2^-16                                 */
+double oracle_decode_e5m2(uint8_t h)
+{
+    int sign = (h >> 7) & 1;
+    int e = (h >> 2) & 0x1f;
+    int f = h & 0x3;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -16);
+    else if (e == 0x1f)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(4 + f), e - 17);
+    return sign ? -v : v;
+}
+
+static int is_fp8(int dtype)
+{
+    return dtype == ORACLE_E4M3 || dtype == ORACLE_E5M2;
+}
+
+/* element idx of an operand array holding dtype's patterns */
+static double decode(const void *base, int64_t idx, int dtype)
+{
+    switch (dtype) {
+    case ORACLE_BF16: return oracle_decode_bf16(((const uint16_t *)base)[idx]);
+    case ORACLE_E4M3: return oracle_decode_e4m3(((const uint8_t *)base)[idx]);
+    case ORACLE_E5M2: return oracle_decode_e5m2(((const uint8_t *)base)[idx]);
+    default:          return oracle_decode_f16(((const uint16_t *)base)[idx]);
+    }
 }
 
 typedef struct {
     /* shared */
-    const uint16_t *A;
+    const void *A;
     const double *Bd;      /* decoded b[k][j], K x N row-major */
-    const uint16_t *B;     /* raw B, for the decode phase */
+    const void *B;         /* raw B, for the decode phase */
     int64_t M, N, K;
     int dtype, layout_b;
     const int64_t *rows;
@@ -103,9 +162,8 @@ static void decode_b_rows(const job_t *j)
     double *Bd = (double *)j->Bd;
     for (int64_t k = j->lo; k < j->hi; ++k)
         for (int64_t c = 0; c < j->N; ++c) {
-            uint16_t bits = j->layout_b == ORACLE_K_MAJOR ? j->B[c * j->K + k]
-                                                          : j->B[k * j->N + c];
-            Bd[k * j->N + c] = decode(bits, j->dtype);
+            int64_t idx = j->layout_b == ORACLE_K_MAJOR ? c * j->K + k : k * j->N + c;
+            Bd[k * j->N + c] = decode(j->B, idx, j->dtype);
         }
 }
 
@@ -121,7 +179,7 @@ static void gemm_rows(const job_t *j)
             cabs[col] = 0.0;
         }
         for (int64_t k = 0; k < K; ++k) {
-            const double a = decode(j->A[i * K + k], j->dtype);
+            const double a = decode(j->A, i * K + k, j->dtype);
             const double *b = j->Bd + k * N;
             for (int64_t col = 0; col < N; ++col) {
                 const double p = a * b[col];
@@ -179,8 +237,10 @@ static int run_threads(job_t *base, int64_t count, int n_threads)
 
 /*
  * Compute selected rows of C = A·B in FP64.
- *   A, B      : raw 16-bit operand patterns, layouts as described above
- *   dtype     : ORACLE_F16 or ORACLE_BF16 (both operands)
+ *   A, B      : raw operand patterns (16-bit words for ORACLE_F16 and
+ *               ORACLE_BF16, bytes for ORACLE_E4M3 and ORACLE_E5M2),
+ *               layouts as described above
+ *   dtype     : the element type of both operands
  *   layout_b  : ORACLE_K_MAJOR or ORACLE_MN_MAJOR
  *   rows      : indices of the output rows to compute, or NULL for all M
  *   n_rows    : number of entries in rows (ignored when rows is NULL)
@@ -188,13 +248,13 @@ static int run_threads(job_t *base, int64_t count, int n_threads)
  *   n_threads : worker threads (<= 0: all online CPUs)
  * Returns 0 on success, -1 for invalid arguments, -2 when memory runs out.
  */
-int oracle_gemm(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K,
+int oracle_gemm(const void *A, const void *B, int64_t M, int64_t N, int64_t K,
                 int dtype, int layout_b, const int64_t *rows, int64_t n_rows,
                 double *C, double *C_abs, int n_threads)
 {
     if (!A || !B || !C || !C_abs || M <= 0 || N <= 0 || K <= 0)
         return -1;
-    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16)
+    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16 && !is_fp8(dtype))
         return -1;
     if (layout_b != ORACLE_K_MAJOR && layout_b != ORACLE_MN_MAJOR)
         return -1;

@@ -1,8 +1,9 @@
 """Pins for the CPU FP64 oracle (no GPU).
 
-The oracle is checked against things other than itself: the IEEE/bfloat16
-format definitions (hand-written fixtures), numpy's and torch's own FP16/BF16
-conversions, exact rational arithmetic (``fractions``) on tiny shapes, closed
+The oracle is checked against things other than itself: the IEEE/bfloat16/
+OCP FP8 format definitions (hand-written fixtures), numpy's and torch's own
+FP16/BF16/FP8 conversions, the bit-level identity E5M2 = upper byte of FP16,
+exact rational arithmetic (``fractions``) on tiny shapes, closed
 forms (identity, all-ones, rank-1), exact integer arithmetic, and
 ``torch.matmul`` in float64. ``test_planted_mistakes`` compiles copies of the
 oracle with one deliberate bug each and requires every copy to fail at least
@@ -25,6 +26,8 @@ from oracle import tolerance
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 U = 2.0 ** -53
+DTYPES = ("f16", "bf16", "e4m3", "e5m2")
+FP8_TORCH = {"e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 
 
 # ---------------------------------------------------------------- helpers
@@ -37,7 +40,14 @@ def bf16_bits(vals) -> np.ndarray:
     return t.view(torch.int16).numpy().view(np.uint16)
 
 
+def fp8_bits(vals, dtype) -> np.ndarray:
+    t = torch.tensor(np.asarray(vals, dtype=np.float64), dtype=torch.float64)
+    return t.to(torch.float32).to(FP8_TORCH[dtype]).view(torch.uint8).numpy()
+
+
 def bits_of(vals, dtype):
+    if dtype in FP8_TORCH:
+        return fp8_bits(vals, dtype)
     return f16_bits(vals) if dtype == "f16" else bf16_bits(vals)
 
 
@@ -45,11 +55,21 @@ def exact_value(bits: int, dtype: str) -> float:
     """FP64 value of a pattern via numpy/torch conversions (not the oracle's decoder)."""
     if dtype == "f16":
         return float(np.array([bits], dtype=np.uint16).view(np.float16)[0])
+    if dtype in FP8_TORCH:
+        return float(torch.tensor([bits], dtype=torch.uint8).view(FP8_TORCH[dtype]).double()[0])
     return float(np.array([bits << 16], dtype=np.uint32).view(np.float32)[0])
 
 
 def random_finite_bits(rng: np.random.Generator, n: int, dtype: str) -> np.ndarray:
     """Finite patterns with every exponent represented, subnormals included."""
+    if dtype == "e4m3":
+        # every byte but the two NaNs (S.1111.111)
+        low = rng.integers(0, 127, n)
+        return (low | (rng.integers(0, 2, n) << 7)).astype(np.uint8)
+    if dtype == "e5m2":
+        e = rng.integers(0, 31, n)
+        f = rng.integers(0, 4, n)
+        return ((e << 2) | f | (rng.integers(0, 2, n) << 7)).astype(np.uint8)
     if dtype == "f16":
         e = rng.integers(0, 31, n)
         f = rng.integers(0, 1024, n)
@@ -86,6 +106,18 @@ def _pin_decoders(lib):
         same = (mine == ref) | (np.isnan(mine) & np.isnan(ref))
         if not same.all():
             out.append(f"decoder_{dtype}")
+    bytes_ = np.arange(256, dtype=np.uint32).astype(np.uint8)
+    for dtype, tdt in FP8_TORCH.items():
+        mine = oracle.decode(bytes_, dtype, lib=lib)
+        ref = torch.from_numpy(bytes_.copy()).view(tdt).double().numpy()
+        same = (mine == ref) | (np.isnan(mine) & np.isnan(ref))
+        if not same.all():
+            out.append(f"decoder_{dtype}")
+    # E5M2 is the upper byte of an FP16 pattern (same sign and exponent fields)
+    e5 = oracle.decode(bytes_, "e5m2", lib=lib)
+    f16 = oracle.decode(bytes_.astype(np.uint16) << 8, "f16", lib=lib)
+    if not ((e5 == f16) | (np.isnan(e5) & np.isnan(f16))).all():
+        out.append("decoder_e5m2_vs_f16")
     return out
 
 
@@ -97,7 +129,7 @@ def _parse_format_fixture(name):
             if not line:
                 continue
             bits, mant, expo = line.split()[:3]
-            if mant in ("inf", "-inf"):
+            if mant in ("inf", "-inf", "nan"):
                 val = float(mant)
             else:
                 val = math.ldexp(float(int(mant)), int(expo))
@@ -107,10 +139,11 @@ def _parse_format_fixture(name):
 
 def _pin_format_fixtures(lib):
     out = []
-    for name, dtype in (("binary16_values.txt", "f16"), ("bfloat16_values.txt", "bf16")):
+    for name, dtype in (("binary16_values.txt", "f16"), ("bfloat16_values.txt", "bf16"),
+                        ("e4m3_values.txt", "e4m3"), ("e5m2_values.txt", "e5m2")):
         for bits, val in _parse_format_fixture(name):
-            got = float(oracle.decode(np.array([bits], dtype=np.uint16), dtype, lib=lib)[0])
-            if got != val:
+            got = float(oracle.decode(np.array([bits]), dtype, lib=lib)[0])
+            if not (got == val or (math.isnan(got) and math.isnan(val))):
                 out.append(f"fixture_{dtype}_{bits:#06x}")
     return out
 
@@ -124,14 +157,15 @@ def _parse_gemm_fixture():
                 continue
             tok = line.split()
             if tok[0] == "case":
-                cur = {"name": tok[1]}
+                cur = {"name": tok[1], "dtypes": tuple(tok[2:]) or DTYPES}
                 cases.append(cur)
             elif tok[0] in ("A", "B", "C", "C_abs"):
                 key = tok[0]
                 cur[key] = []
             else:
                 cur[key].append([float(t) for t in tok])
-    return [{k: (np.array(v) if k != "name" else v) for k, v in c.items()} for c in cases]
+    return [{k: (np.array(v) if k not in ("name", "dtypes") else v) for k, v in c.items()}
+            for c in cases]
 
 
 def _pin_hand_gemm(lib):
@@ -140,7 +174,7 @@ def _pin_hand_gemm(lib):
         A, Bkn, C, Cabs = case["A"], case["B"], case["C"], case["C_abs"]
         M, K = A.shape
         N = Bkn.shape[1]
-        for dtype in ("f16", "bf16"):
+        for dtype in case["dtypes"]:
             for lay in ("k", "mn"):
                 got, gabs = oracle.gemm_ref(bits_of(A, dtype), b_storage(bits_of(Bkn, dtype), lay),
                                             M, N, K, dtype, lay, lib=lib)
@@ -153,7 +187,7 @@ def _pin_brute_force(lib):
     out = []
     rng = np.random.default_rng(1234)
     for (M, N, K) in ((1, 1, 1), (2, 3, 4), (5, 7, 3), (17, 9, 33)):
-        for dtype in ("f16", "bf16"):
+        for dtype in DTYPES:
             for lay in ("k", "mn"):
                 Ab = random_finite_bits(rng, M * K, dtype).reshape(M, K)
                 Bkn = random_finite_bits(rng, K * N, dtype).reshape(K, N)
@@ -181,7 +215,7 @@ def _pin_brute_force(lib):
 def _pin_closed_forms(lib):
     out = []
     rng = np.random.default_rng(7)
-    for dtype in ("f16", "bf16"):
+    for dtype in DTYPES:
         for lay in ("k", "mn"):
             # identity B (N = K): C = A exactly
             M, K = 13, 24
@@ -222,7 +256,7 @@ def _pin_integers(lib):
     """Small integers: every partial sum is exact, so C equals int64 matmul."""
     out = []
     rng = np.random.default_rng(11)
-    for dtype in ("f16", "bf16"):
+    for dtype in DTYPES:
         for lay in ("k", "mn"):
             M, N, K = 19, 23, 300
             Ai = rng.integers(-3, 4, (M, K))
@@ -238,15 +272,18 @@ def _pin_integers(lib):
 def _pin_torch_matmul(lib):
     out = []
     g = torch.Generator().manual_seed(5)
-    for dtype, tdt in (("f16", torch.float16), ("bf16", torch.bfloat16)):
+    for dtype, tdt in (("f16", torch.float16), ("bf16", torch.bfloat16)) + tuple(FP8_TORCH.items()):
         for lay in ("k", "mn"):
             M, N, K = 40, 33, 200
             A = torch.randn(M, K, generator=g).to(tdt)
             Bkn = torch.randn(K, N, generator=g).to(tdt)
             ref = (A.double() @ Bkn.double()).numpy()
             refabs = (A.double().abs() @ Bkn.double().abs()).numpy()
-            Ab = A.view(torch.int16).numpy().view(np.uint16)
-            Bb = Bkn.contiguous().view(torch.int16).numpy().view(np.uint16)
+            view = torch.uint8 if dtype in FP8_TORCH else torch.int16
+            Ab = A.view(view).numpy()
+            Bb = Bkn.contiguous().view(view).numpy()
+            if view is torch.int16:
+                Ab, Bb = Ab.view(np.uint16), Bb.view(np.uint16)
             got, gabs = oracle.gemm_ref(Ab, b_storage(Bb, lay), M, N, K, dtype, lay, lib=lib)
             lim = 2 * gamma(K) * refabs
             if np.any(np.abs(got - ref) > lim) or np.any(np.abs(gabs - refabs) > lim):
@@ -258,7 +295,7 @@ def _pin_row_subset(lib):
     out = []
     rng = np.random.default_rng(3)
     M, N, K = 21, 10, 17
-    for dtype in ("f16", "bf16"):
+    for dtype in DTYPES:
         Ab = random_finite_bits(rng, M * K, dtype).reshape(M, K)
         Bb = random_finite_bits(rng, K * N, dtype).reshape(N, K)
         full, fabs_ = oracle.gemm_ref(Ab, Bb, M, N, K, dtype, "k", lib=lib)
@@ -323,7 +360,8 @@ def test_threads_do_not_change_bits(lib):
 # Each entry plants one plausible mistake in a copy of the oracle's source.
 MUTANTS = {
     "dropped_term": ("for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = 1; k < K; ++k) {"),
-    "transposed_b": ("j->B[c * j->K + k]", "j->B[k * j->N + c]"),
+    "transposed_b": ("j->layout_b == ORACLE_K_MAJOR ? c * j->K + k : k * j->N + c",
+                     "j->layout_b == ORACLE_K_MAJOR ? k * j->N + c : k * j->N + c"),
     "wrong_sign": ("c[col] += p;", "c[col] -= p;"),
     "f16_bias": ("e - 25", "e - 24"),
     "f16_subnormal": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
@@ -331,7 +369,16 @@ MUTANTS = {
     "bf16_hidden_bit": ("(double)(128 + f)", "(double)(f)"),
     "abs_dropped": ("cabs[col] += fabs(p);", "cabs[col] += p;"),
     "row_map_ignored": ("j->rows ? j->rows[r] : r", "r"),
-    "a_index_reversed": ("j->A[i * K + k]", "j->A[i * K + (K - 1 - k)]"),
+    "a_index_reversed": ("decode(j->A, i * K + k, j->dtype)",
+                         "decode(j->A, i * K + (K - 1 - k), j->dtype)"),
+    "e4m3_bias": ("e - 10", "e - 11"),
+    "e4m3_subnormal": ("ldexp((double)f, -9)", "ldexp((double)f, -10)"),
+    "e4m3_top_binade_as_nan": ("e == 0xf && f == 0x7", "e == 0xf"),
+    "e4m3_fraction_width": ("int f = h & 0x7;", "int f = h & 0x3;"),
+    "e5m2_bias": ("e - 17", "e - 16"),
+    "e5m2_hidden_bit": ("(double)(4 + f)", "(double)(8 + f)"),
+    "fp8_read_as_16bit": ("case ORACLE_E4M3: return oracle_decode_e4m3(((const uint8_t *)base)[idx]);",
+                          "case ORACLE_E4M3: return oracle_decode_e4m3((uint8_t)((const uint16_t *)base)[idx]);"),
 }
 
 

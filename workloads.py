@@ -10,13 +10,16 @@ Recipe (the pages fix no generator; this is the plain reading):
     (A: M×K row-major; B K-major: N×K, K contiguous; B MN-major: K×N,
     N contiguous);
   * uniform[a, b] = a + (b − a)·rand, normal(0, σ) = σ·randn;
-  * rounded to FP16/BF16 with round-to-nearest-even (``Tensor.to``).
+  * rounded to FP16/BF16 or FP8 (E4M3 "FN", E5M2) with round-to-nearest-even
+    (``Tensor.to``); the draws stay well inside each type's finite range.
 
 The workloads are the five GEMM shapes the tiled-GEMM pages measure or that
 exercise the method's edge paths (a small 256³ check, the compute-bound
 4096×4096×8192 FP16 shape of "Two Waves, One Stage Apart", §"MI350 Series",
 a BF16 8192³ shape, a ragged 3000×5000×2050 shape with N-contiguous B, and
-a square FP16 sweep).
+a square FP16 sweep), plus the FP8 E4M3 squares of "Porting
+High-Performance HIP Kernels to FlyDSL", section "Results" (8192 and 12288,
+normally distributed data; the page does not give C's type, BF16 is taken).
 """
 from __future__ import annotations
 
@@ -25,7 +28,9 @@ from dataclasses import dataclass, field
 
 import torch
 
-DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+          "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+FP8 = ("e4m3", "e5m2")
 
 
 @dataclass(frozen=True)
@@ -34,7 +39,7 @@ class Workload:
     M: int
     N: int
     K: int
-    dtype_in: str          # "f16" | "bf16"
+    dtype_in: str          # "f16" | "bf16" | "e4m3" | "e5m2"
     dtype_out: str         # "f16" | "bf16" | "f32"
     layout_b: str          # "k": B stored N×K (K contiguous); "mn": B stored K×N
     dist: tuple            # ("uniform", lo, hi) | ("normal", sigma) | ("int", lo, hi)
@@ -63,7 +68,12 @@ WORKLOADS = {w.name: w for w in [
              ("normal", 1.0 / math.sqrt(8192)), 2, "BF16 square"),
     Workload("gemm_3000x5000x2050_bf16_f32_bmn", 3000, 5000, 2050, "bf16", "f32", "mn",
              ("uniform", -2.0, 2.0), 3, "ragged tails, N-contiguous B"),
-] + _sweep()}
+] + _sweep() + [
+    Workload("gemm_8192_e4m3", 8192, 8192, 8192, "e4m3", "bf16", "k",
+             ("normal", 1.0), 9, "FP8 E4M3 square"),
+    Workload("gemm_12288_e4m3", 12288, 12288, 12288, "e4m3", "bf16", "k",
+             ("normal", 1.0), 10, "FP8 E4M3 square"),
+]}
 
 HEADLINE = "gemm_4096x4096x8192_f16"
 
@@ -105,10 +115,13 @@ def workload_operands(w: Workload) -> tuple[torch.Tensor, torch.Tensor]:
 
 
 def as_bits(t: torch.Tensor):
-    """Raw 16-bit patterns of an FP16/BF16 CPU tensor as a numpy uint16 array."""
+    """Raw patterns of a CPU tensor: numpy uint16 for FP16/BF16, uint8 for FP8."""
     import numpy as np
-    assert t.dtype in (torch.float16, torch.bfloat16) and t.device.type == "cpu"
-    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    assert t.device.type == "cpu"
+    if t.dtype in (torch.float16, torch.bfloat16):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    assert t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2), t.dtype
+    return t.contiguous().view(torch.uint8).numpy()
 
 
 def sample_rows(M: int, count: int, seed: int, tile: int = 128) -> list[int]:
