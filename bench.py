@@ -47,6 +47,7 @@ METRIC = "GEMM TFLOP/s at 4096x4096x8192 FP16 and % of GB300 dense tensor peak"
 PAGES_REFERENCE_TFLOPS = 1437.0   # MI355X, 8-wave warp-pipelined Triton, same shape (context only)
 FALLBACK_BF16_TFLOPS = 1900.0
 NOMINAL_DENSE_TFLOPS = 2250.0     # GB300 dense FP16/BF16 tensor peak, nominal
+FP8_RATE = 2.0                    # nominal dense FP8 / FP16 rate on GB300 (4.5 vs 2.25 PFLOP/s)
 
 
 def parse_args():
@@ -251,8 +252,12 @@ def time_cublas(As, Bs, Cs, w, n_sets, args, stream, smi_id, pg, dev) -> dict:
     """torch.matmul (cuBLAS) on the same rotating operands, timed the same way.
     A comparison only: nothing on the product path calls it."""
     same_dtype = Cs[0].dtype == As[0].dtype
+    fp8 = w.dtype_in in workloads.FP8
     how = "torch.matmul (cuBLAS)"
-    if not same_dtype:
+    if fp8:
+        one = torch.ones((), dtype=torch.float32, device=dev)
+        how = f"torch._scaled_mm unit scales, out_dtype={Cs[0].dtype} (cuBLASLt FP8)"
+    elif not same_dtype:
         try:   # cuBLAS writing the wider output type directly, where this torch has it
             torch.mm(As[0], Bs[0].t() if w.layout_b == "k" else Bs[0], out_dtype=Cs[0].dtype)
             how = f"torch.mm out_dtype={Cs[0].dtype} (cuBLAS)"
@@ -262,7 +267,9 @@ def time_cublas(As, Bs, Cs, w, n_sets, args, stream, smi_id, pg, dev) -> dict:
     def step(i):
         j = i % n_sets
         Bj = Bs[j].t() if w.layout_b == "k" else Bs[j]
-        if same_dtype:
+        if fp8:
+            torch._scaled_mm(As[j], Bj, scale_a=one, scale_b=one, out_dtype=Cs[j].dtype)
+        elif same_dtype:
             torch.matmul(As[j], Bj, out=Cs[j])
         elif how.startswith("torch.mm"):
             torch.mm(As[j], Bj, out_dtype=Cs[j].dtype)
@@ -305,13 +312,20 @@ def run_ours(args):
     w = workloads.WORKLOADS[args.workload]
     out_dt = workloads.DTYPES[w.dtype_out]
     A0, B0 = workloads.workload_operands(w)
+    in_bytes = A0.element_size()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    set_bytes = (A0.numel() + B0.numel()) * 2 + w.M * w.N * torch.finfo(out_dt).bits // 8
+    set_bytes = (A0.numel() + B0.numel()) * in_bytes + w.M * w.N * torch.finfo(out_dt).bits // 8
     n_sets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+    bits_dt = torch.uint8 if in_bytes == 1 else torch.int16
+
+    def rolled(t, i):
+        # rotate rows through a same-width integer view (no roll kernel for FP8 types)
+        return t.to(dev) if i == 0 else t.to(dev).view(bits_dt).roll(i, 0).view(t.dtype)
+
     As, Bs, Cs = [], [], []
     for i in range(n_sets):
-        As.append(A0.to(dev) if i == 0 else A0.to(dev).roll(i, 0))
-        Bs.append(B0.to(dev) if i == 0 else B0.to(dev).roll(i, 0))
+        As.append(rolled(A0, i))
+        Bs.append(rolled(B0, i))
         Cs.append(torch.empty((w.M, w.N), dtype=out_dt, device=dev))
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
@@ -363,6 +377,14 @@ def run_ours(args):
 
     peaks, peak_src = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))  # FP16 and BF16 share the dense rate
+    fp8 = w.dtype_in in workloads.FP8
+    nominal = NOMINAL_DENSE_TFLOPS * (FP8_RATE if fp8 else 1.0)
+    if fp8:
+        peak *= FP8_RATE
+        peak_note = (f"{peak_src} bf16_tflops (burst) x {FP8_RATE:g}, the nominal dense "
+                     "FP8/BF16 ratio (4.5 / 2.25 PFLOP/s)")
+    else:
+        peak_note = f"{peak_src} bf16_tflops (burst); FP16 dense rate = BF16"
     achieved = flops_step / (kernel_ms * 1e-3) / 1e12
     plan = dtg.gemm_plan(w.M, w.N, w.K, dtype_in=workloads.DTYPES[w.dtype_in], dtype_out=out_dt,
                          layout_b=w.layout_b, a_ptr=As[0].data_ptr(), b_ptr=Bs[0].data_ptr(),
@@ -387,7 +409,7 @@ def run_ours(args):
         dt = max_over_ranks(time.perf_counter() - t0, pg, dev)
         dtg.gemm_release_workspace()
         e2e = {"value": whole_job_tflops(world, flops_step, n, dt), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": (Ah.numel() + Bh.numel()) * 2,
+               "h2d_bytes_per_step": (Ah.numel() + Bh.numel()) * in_bytes,
                "d2h_bytes_per_step": Ch.numel() * Ch.element_size(),
                "steps": n, "api": "gemm_from_host (pinned host buffers, synchronous)"}
 
@@ -402,7 +424,7 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak",
             "vs_baseline": value / world / PAGES_REFERENCE_TFLOPS if w.name == workloads.HEADLINE else None,
             "vs_baseline_ref": "1437 TFLOP/s: MI355X 8-wave warp-pipelined Triton, same shape (context)",
-            "dtype": "f16" if w.dtype_in == "f16" else "bf16", "accumulate": "f32",
+            "dtype": w.dtype_in, "accumulate": "f32",
             "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype_in": w.dtype_in,
                        "dtype_out": w.dtype_out, "layout_b": w.layout_b,
@@ -411,7 +433,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}", "plan": plan},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": profiled_traffic(w.name),
-                         "peak_source": f"{peak_src} bf16_tflops (burst); FP16 dense rate = BF16",
+                         "peak_source": peak_note,
                          "kernel_ms": kernel_ms},
             "clocks": clocks,
             "gpu_launches": launches,
@@ -419,10 +441,10 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "cublas_comparison": cublas,
         }
-        line["roofline"]["frac_of_nominal"] = achieved / NOMINAL_DENSE_TFLOPS
+        line["roofline"]["frac_of_nominal"] = achieved / nominal
         if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
             line["roofline"]["frac_of_nominal_at_measured_clock"] = achieved / (
-                NOMINAL_DENSE_TFLOPS * clocks["sm_mhz"] / clocks["sm_max_mhz"])
+                nominal * clocks["sm_mhz"] / clocks["sm_max_mhz"])
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()

@@ -1,5 +1,5 @@
-"""Dense tiled GEMM for GB300 (sm_103a): C = A·B with FP16/BF16 operands,
-FP32 accumulation and a cast-on-store epilogue.
+"""Dense tiled GEMM for GB300 (sm_103a): C = A·B with FP16/BF16 or FP8
+(E4M3/E5M2) operands, FP32 accumulation and a cast-on-store epilogue.
 
 Every function here has the name of a C-ABI entry point in include/gemm.h and
 only marshals arguments: torch tensors become device pointers and sizes, and
@@ -14,14 +14,17 @@ import ctypes
 import torch
 
 from . import binding
-from .binding import (GEMM_BF16, GEMM_F16, GEMM_F32, GEMM_K_MAJOR, GEMM_MN_MAJOR, GEMM_OK,
-                      GEMM_ERR_TIMEOUT, GemmError, GemmOptions, GemmPlan, STATUS_NAMES)
+from .binding import (GEMM_BF16, GEMM_E4M3, GEMM_E5M2, GEMM_F16, GEMM_F32, GEMM_K_MAJOR,
+                      GEMM_MN_MAJOR, GEMM_OK, GEMM_ERR_TIMEOUT, GemmError, GemmOptions, GemmPlan,
+                      STATUS_NAMES)
 
 __all__ = ["gemm", "gemm_ex", "gemm_plan", "gemm_from_host", "gemm_release_workspace",
            "gemm_last_device_status", "gemm_selftest_wait_timeout", "gemm_status_string",
            "gemm_launch_count", "GemmError", "GemmOptions", "GemmPlan"]
 
-_DT_IN = {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16}
+_DT_IN = {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16,
+          torch.float8_e4m3fn: GEMM_E4M3, torch.float8_e5m2: GEMM_E5M2}
+_FP8 = (torch.float8_e4m3fn, torch.float8_e5m2)
 _DT_OUT = {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16, torch.float32: GEMM_F32}
 _LAYOUT = {"k": GEMM_K_MAJOR, "mn": GEMM_MN_MAJOR}
 
@@ -66,7 +69,8 @@ def _check(status: int, what: str):
 def _prepare(A, B, C, layout_b, out_dtype, device_kind):
     for name, t in (("A", A), ("B", B)):
         if t.dtype not in _DT_IN:
-            raise TypeError(f"{name} must be float16 or bfloat16, got {t.dtype}")
+            raise TypeError(f"{name} must be float16, bfloat16, float8_e4m3fn or float8_e5m2, "
+                            f"got {t.dtype}")
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
         if t.device.type != device_kind:
@@ -75,7 +79,8 @@ def _prepare(A, B, C, layout_b, out_dtype, device_kind):
         raise TypeError("A and B must have the same dtype")
     M, N, K = _shapes(A, B, layout_b)
     if C is None:
-        C = torch.empty((M, N), dtype=out_dtype or A.dtype, device=A.device,
+        default_out = torch.bfloat16 if A.dtype in _FP8 else A.dtype
+        C = torch.empty((M, N), dtype=out_dtype or default_out, device=A.device,
                         pin_memory=(device_kind == "cpu" and torch.cuda.is_available()))
     if C.dtype not in _DT_OUT or tuple(C.shape) != (M, N) or not C.is_contiguous():
         raise ValueError("C must be a contiguous (M, N) float16/bfloat16/float32 tensor")
@@ -89,8 +94,9 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *,
          options=None) -> torch.Tensor:
     """C = A·B on A's CUDA device, asynchronously on ``stream`` (default: torch's current).
 
-    A: (M, K). B: (N, K) for layout_b="k", (K, N) for layout_b="mn".
-    C: (M, N) of ``out_dtype`` (default A.dtype), allocated when not given.
+    A: (M, K). B: (N, K) for layout_b="k", (K, N) for layout_b="mn" (16-bit types
+    only). C: (M, N) of ``out_dtype`` (default A.dtype, BF16 for FP8 inputs),
+    allocated when not given.
     ``options``: dict or GemmOptions of gemm_ex overrides.
     """
     M, N, K, C = _prepare(A, B, C, layout_b, out_dtype, "cuda")

@@ -11,7 +11,7 @@ import os
 
 from .build import LIB_PATH
 
-GEMM_F16, GEMM_BF16, GEMM_F32 = 0, 1, 2
+GEMM_F16, GEMM_BF16, GEMM_F32, GEMM_E4M3, GEMM_E5M2 = 0, 1, 2, 3, 4
 GEMM_K_MAJOR, GEMM_MN_MAJOR = 0, 1
 STATUS_NAMES = {
     0: "GEMM_OK",

@@ -39,22 +39,25 @@ int default_k_slabs(int cg) { return cg == 2 ? 2 : 1; }
 struct Variant {
     int cg;
     int bn;
-    int ks;            // K slabs (of 64) per ring stage
+    int ks;            // K slabs (128 bytes of K each) per ring stage
+    int eb;            // operand element bytes: 2 (FP16/BF16) or 1 (FP8)
     int stage_bytes;   // one ring slot: A and B tiles of one stage (per CTA)
     const void *fn;
-    bool b_mn_ok;      // MN-major B needs 64-column TMA boxes per CTA
+    bool b_mn_ok;      // MN-major B needs 64-column TMA boxes per CTA (16-bit only)
 };
 
-template <int CG, int BN, int KS>
+template <int CG, int BN, int KS, int EB>
 constexpr Variant variant(bool b_mn_ok)
 {
-    return {CG, BN, KS, TileConfig<CG, BN, KS>::STAGE_BYTES,
-            reinterpret_cast<const void *>(&gemm_tcgen05_kernel<CG, BN, KS>), b_mn_ok};
+    return {CG, BN, KS, EB, TileConfig<CG, BN, KS, EB>::STAGE_BYTES,
+            reinterpret_cast<const void *>(&gemm_tcgen05_kernel<CG, BN, KS, EB>), b_mn_ok};
 }
 
 const Variant kVariants[] = {
-    variant<2, 256, 1>(true),  variant<2, 224, 1>(false), variant<1, 256, 1>(true),
-    variant<2, 256, 2>(true),  variant<2, 224, 2>(false), variant<1, 256, 2>(true),
+    variant<2, 256, 1, 2>(true),  variant<2, 224, 1, 2>(false), variant<1, 256, 1, 2>(true),
+    variant<2, 256, 2, 2>(true),  variant<2, 224, 2, 2>(false), variant<1, 256, 2, 2>(true),
+    variant<2, 256, 1, 1>(false), variant<2, 224, 1, 1>(false), variant<1, 256, 1, 1>(false),
+    variant<2, 256, 2, 1>(false), variant<2, 224, 2, 1>(false), variant<1, 256, 2, 1>(false),
 };
 constexpr int NUM_VARIANTS = sizeof(kVariants) / sizeof(kVariants[0]);
 
@@ -93,7 +96,16 @@ std::atomic<uint64_t> g_launches{0};
 std::atomic<unsigned long long> g_next_id{1};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-int esize(int dtype) { return dtype == GEMM_F32 ? 4 : 2; }
+bool is_fp8(int dtype) { return dtype == GEMM_E4M3 || dtype == GEMM_E5M2; }
+int in_bytes(int dtype_in) { return is_fp8(dtype_in) ? 1 : 2; }
+int out_bytes(int dtype_out) { return dtype_out == GEMM_F32 ? 4 : 2; }
+
+// Row pitch, in elements, that makes a row of `cols` elements a multiple of 16 bytes.
+int64_t padded_pitch(int64_t cols, int eb)
+{
+    const int64_t q = 16 / eb;
+    return (cols + q - 1) / q * q;
+}
 
 gemm_status_t device_state(DeviceState **out)
 {
@@ -170,24 +182,29 @@ gemm_status_t validate(const void *A, const void *B, const void *C, int64_t M, i
         return GEMM_ERR_INVALID_ARG;
     if (M < 1 || N < 1 || K < 1 || M > INT_MAX || N > INT_MAX || K > INT_MAX)
         return GEMM_ERR_INVALID_ARG;
-    if (dtype_in != GEMM_F16 && dtype_in != GEMM_BF16)
+    if (dtype_in != GEMM_F16 && dtype_in != GEMM_BF16 && !is_fp8(dtype_in))
         return dtype_in == GEMM_F32 ? GEMM_ERR_UNSUPPORTED : GEMM_ERR_INVALID_ARG;
     if (dtype_out != GEMM_F16 && dtype_out != GEMM_BF16 && dtype_out != GEMM_F32)
-        return GEMM_ERR_INVALID_ARG;
+        return is_fp8(dtype_out) ? GEMM_ERR_UNSUPPORTED : GEMM_ERR_INVALID_ARG;
     if (layoutA != GEMM_K_MAJOR && layoutA != GEMM_MN_MAJOR)
         return GEMM_ERR_INVALID_ARG;
     if (layoutA == GEMM_MN_MAJOR)
         return GEMM_ERR_UNSUPPORTED;
     if (layoutB != GEMM_K_MAJOR && layoutB != GEMM_MN_MAJOR)
         return GEMM_ERR_INVALID_ARG;
+    if (is_fp8(dtype_in) && layoutB == GEMM_MN_MAJOR)
+        return GEMM_ERR_UNSUPPORTED;
     if (o) {
         if (o->cta_group < 0 || o->cta_group > 2 || o->max_clusters < 0 || o->group_m < 0 ||
             o->timeout_ms < 0 || o->block_n < 0)
             return GEMM_ERR_INVALID_ARG;
         if (o->block_n != 0 && o->block_n != 224 && o->block_n != 256)
             return GEMM_ERR_UNSUPPORTED;
-        if (o->k_stage != 0 && o->k_stage != 64 && o->k_stage != 128)
-            return o->k_stage < 0 ? GEMM_ERR_INVALID_ARG : GEMM_ERR_UNSUPPORTED;
+        if (o->k_stage < 0)
+            return GEMM_ERR_INVALID_ARG;
+        const int sk = slab_k(in_bytes(dtype_in));
+        if (o->k_stage != 0 && o->k_stage != sk && o->k_stage != 2 * sk)
+            return GEMM_ERR_UNSUPPORTED;
     }
     return GEMM_OK;
 }
@@ -208,20 +225,23 @@ bool misaligned(const void *p, int64_t row_elems, int elem_bytes)
 // Choose the tile shape with the fewest output columns per SM over the whole
 // problem: waves = ceil(tiles / co-resident units), cost = waves x block_n.
 // Single-CTA tiles pay ~15% for their higher shared-memory read rate per flop.
-gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, int dtype_out,
-                        int layoutB, const void *A, const void *B, const void *C,
+gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, int dtype_in,
+                        int dtype_out, int layoutB, const void *A, const void *B, const void *C,
                         const gemm_options_t *o, Plan *pl)
 {
     const bool b_mn = layoutB == GEMM_MN_MAJOR;
+    const int eb = in_bytes(dtype_in);
     int best = -1;
     double best_cost = 0;
     for (int v = 0; v < NUM_VARIANTS; ++v) {
         const Variant &var = kVariants[v];
+        if (var.eb != eb)
+            continue;
         if (o && o->cta_group && o->cta_group != var.cg)
             continue;
         if (o && o->block_n && o->block_n != var.bn)
             continue;
-        if (var.ks != ((o && o->k_stage) ? o->k_stage / BLOCK_K : default_k_slabs(var.cg)))
+        if (var.ks != ((o && o->k_stage) ? o->k_stage / slab_k(eb) : default_k_slabs(var.cg)))
             continue;
         if (b_mn && !var.b_mn_ok)
             continue;
@@ -251,12 +271,13 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
     if (tiles > INT_MAX)
         return GEMM_ERR_UNSUPPORTED;
     pl->num_tiles = static_cast<int>(tiles);
-    pl->num_kb = static_cast<int>((K + BLOCK_K * var.ks - 1) / (BLOCK_K * var.ks));
+    const int64_t stage_k = static_cast<int64_t>(slab_k(eb)) * var.ks;
+    pl->num_kb = static_cast<int>((K + stage_k - 1) / stage_k);
     pl->grid_ctas = static_cast<int>(std::min<int64_t>(tiles, units)) * var.cg;
     pl->group_m = (o && o->group_m) ? o->group_m : 8;
-    pl->realign_a = misaligned(A, K, 2);
-    pl->realign_b = misaligned(B, b_mn ? N : K, 2);
-    pl->direct_store = misaligned(C, N, esize(dtype_out));
+    pl->realign_a = misaligned(A, K, eb);
+    pl->realign_b = misaligned(B, b_mn ? N : K, eb);
+    pl->direct_store = misaligned(C, N, out_bytes(dtype_out));
     return GEMM_OK;
 }
 
@@ -278,34 +299,49 @@ CUtensorMapDataType tma_dtype(int dtype)
     switch (dtype) {
     case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     case GEMM_F32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    case GEMM_E4M3:
+    case GEMM_E5M2: return CU_TENSOR_MAP_DATA_TYPE_UINT8;   // bytes are moved, not converted
     default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     }
 }
 
-// Copy a rows x cols 16-bit matrix into stream-ordered scratch with a row
-// pitch padded to 8 elements (16 bytes). The pad is never read: the tensor
-// map keeps the logical width `cols`, and TMA zero-fills past it.
-gemm_status_t realign(const void *src, int64_t rows, int64_t cols, int sms, cudaStream_t st,
+// Copy a rows x cols matrix of eb-byte elements into `dst`, whose row pitch
+// ld (elements) makes every row a multiple of 16 bytes. The pad is never
+// read: the tensor map keeps the logical width `cols`, and TMA zero-fills
+// past it.
+gemm_status_t realign_into(const void *src, int64_t rows, int64_t cols, int64_t ld, int eb, int sms,
+                           cudaStream_t st, void *dst)
+{
+    const int64_t total = rows * cols;
+    const unsigned blocks = static_cast<unsigned>(
+        std::max<int64_t>(std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(sms) * 8), 1));
+    if (eb == 1)
+        realign_rows_kernel<uint8_t><<<blocks, 256, 0, st>>>(static_cast<const uint8_t *>(src),
+                                                             static_cast<uint8_t *>(dst), rows, cols, ld);
+    else
+        realign_rows_kernel<uint16_t><<<blocks, 256, 0, st>>>(static_cast<const uint16_t *>(src),
+                                                              static_cast<uint16_t *>(dst), rows, cols, ld);
+    if (cudaGetLastError() != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return GEMM_OK;
+}
+
+// realign_into stream-ordered scratch taken with cudaMallocAsync.
+gemm_status_t realign(const void *src, int64_t rows, int64_t cols, int eb, int sms, cudaStream_t st,
                       void **out, int64_t *ld_out)
 {
-    const int64_t ld = (cols + 7) / 8 * 8;
-    if (cudaMallocAsync(out, static_cast<size_t>(rows * ld * 2), st) != cudaSuccess) {
+    const int64_t ld = padded_pitch(cols, eb);
+    if (cudaMallocAsync(out, static_cast<size_t>(rows * ld * eb), st) != cudaSuccess) {
         cudaGetLastError();
         *out = nullptr;
         return GEMM_ERR_OUT_OF_MEMORY;
     }
-    const int64_t total = rows * cols;
-    const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(sms) * 8);
-    realign_rows_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(
-        static_cast<const uint16_t *>(src), static_cast<uint16_t *>(*out), rows, cols, ld);
-    if (cudaGetLastError() != cudaSuccess)
-        return GEMM_ERR_CUDA;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
     *ld_out = ld;
-    return GEMM_OK;
+    return realign_into(src, rows, cols, ld, eb, sms, st, *out);
 }
 
-template <int CG, int BN, int KS>
+template <int CG, int BN, int KS, int EB>
 cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap &ta, const CUtensorMap &tb,
                            const CUtensorMap &tc, const KernelParams &kp, cudaStream_t st)
 {
@@ -329,23 +365,83 @@ cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap &ta, 
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<CG, BN, KS>, ta, tb, tc, kp);
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<CG, BN, KS, EB>, ta, tb, tc, kp);
 }
 
 cudaError_t launch_any(const Variant &v, int grid_ctas, uint32_t smem, const CUtensorMap &ta,
                        const CUtensorMap &tb, const CUtensorMap &tc, const KernelParams &kp, cudaStream_t st)
 {
-#define DTG_LAUNCH(CG, BN, KS)                                                                     \
-    if (v.cg == CG && v.bn == BN && v.ks == KS)                                                    \
-        return launch_variant<CG, BN, KS>(grid_ctas, smem, ta, tb, tc, kp, st);
-    DTG_LAUNCH(2, 256, 1)
-    DTG_LAUNCH(2, 224, 1)
-    DTG_LAUNCH(1, 256, 1)
-    DTG_LAUNCH(2, 256, 2)
-    DTG_LAUNCH(2, 224, 2)
-    DTG_LAUNCH(1, 256, 2)
+#define DTG_LAUNCH(CG, BN, KS, EB)                                                                 \
+    if (v.cg == CG && v.bn == BN && v.ks == KS && v.eb == EB)                                      \
+        return launch_variant<CG, BN, KS, EB>(grid_ctas, smem, ta, tb, tc, kp, st);
+    DTG_LAUNCH(2, 256, 1, 2)
+    DTG_LAUNCH(2, 224, 1, 2)
+    DTG_LAUNCH(1, 256, 1, 2)
+    DTG_LAUNCH(2, 256, 2, 2)
+    DTG_LAUNCH(2, 224, 2, 2)
+    DTG_LAUNCH(1, 256, 2, 2)
+    DTG_LAUNCH(2, 256, 1, 1)
+    DTG_LAUNCH(2, 224, 1, 1)
+    DTG_LAUNCH(1, 256, 1, 1)
+    DTG_LAUNCH(2, 256, 2, 1)
+    DTG_LAUNCH(2, 224, 2, 1)
+    DTG_LAUNCH(1, 256, 2, 1)
 #undef DTG_LAUNCH
     return cudaErrorInvalidValue;
+}
+
+// Build the three tensor maps and the kernel parameters for operands already
+// at TMA-describable addresses (a_ptr/b_ptr with row pitches lda/ldb in
+// elements), and launch the plan's kernel on `st`.
+gemm_status_t encode_and_launch(const DeviceState &d, const Plan &pl, const void *a_ptr, int64_t lda,
+                                const void *b_ptr, int64_t ldb, void *C, int64_t M, int64_t N, int64_t K,
+                                int dtype_in, int dtype_out, bool b_mn, uint64_t timeout_ms, cudaStream_t st)
+{
+    const Variant &var = kVariants[pl.variant];
+    const int eb = var.eb;
+    const uint32_t sk = static_cast<uint32_t>(slab_k(eb));
+    alignas(64) CUtensorMap ta, tb, tc;
+    std::memset(&tc, 0, sizeof(tc));
+    const CUtensorMapDataType in_dt = tma_dtype(dtype_in);
+    bool ok = encode_2d(&ta, in_dt, a_ptr, K, M, lda * eb, sk, BLOCK_M_CTA, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!b_mn)
+        ok = ok && encode_2d(&tb, in_dt, b_ptr, K, N, ldb * eb, sk, var.bn / var.cg, CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+        ok = ok && encode_2d(&tb, in_dt, b_ptr, N, K, ldb * eb, 64, sk, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!pl.direct_store)
+        ok = ok && encode_2d(&tc, tma_dtype(dtype_out), C, N, M, N * out_bytes(dtype_out), EPI_COLS, 32,
+                             dtype_out == GEMM_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!ok)
+        return GEMM_ERR_CUDA;
+
+    KernelParams kp = {};
+    kp.M = static_cast<int32_t>(M);
+    kp.N = static_cast<int32_t>(N);
+    kp.K = static_cast<int32_t>(K);
+    kp.num_m_tiles = pl.num_m;
+    kp.num_n_tiles = pl.num_n;
+    kp.num_tiles = pl.num_tiles;
+    kp.num_k_blocks = pl.num_kb;
+    kp.group_m = pl.group_m;
+    const uint32_t fmt = (dtype_in == GEMM_BF16 || dtype_in == GEMM_E5M2) ? 1u : 0u;
+    kp.idesc = make_idesc(128u * var.cg, static_cast<uint32_t>(var.bn), fmt, b_mn ? 1u : 0u);
+    kp.out_dtype = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_BF16 ? OUT_BF16 : OUT_F16);
+    kp.b_mn_major = b_mn ? 1u : 0u;
+    kp.direct_store = pl.direct_store ? 1u : 0u;
+    const Layout lay = layout_for(var, dtype_out);
+    kp.stages = lay.stages;
+    kp.staging_bytes = lay.staging_bytes;
+    kp.C = C;
+    kp.timeout_ns = timeout_ms * 1000000ull;
+    kp.launch_id = g_next_id.fetch_add(1, std::memory_order_relaxed);
+    kp.status = d.status;
+
+    if (launch_any(var, pl.grid_ctas, lay.smem, ta, tb, tc, kp, st) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return GEMM_OK;
 }
 
 gemm_status_t run(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
@@ -359,10 +455,10 @@ gemm_status_t run(const void *A, const void *B, void *C, int64_t M, int64_t N, i
     if ((rc = device_state(&d)) != GEMM_OK)
         return rc;
     Plan pl;
-    if ((rc = make_plan(*d, M, N, K, dtype_out, layoutB, A, B, C, opts, &pl)) != GEMM_OK)
+    if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, opts, &pl)) != GEMM_OK)
         return rc;
-    const Variant &var = kVariants[pl.variant];
     const bool b_mn = layoutB == GEMM_MN_MAJOR;
+    const int eb = in_bytes(dtype_in);
 
     const void *a_ptr = A, *b_ptr = B;
     int64_t lda = K, ldb = b_mn ? N : K;
@@ -373,67 +469,25 @@ gemm_status_t run(const void *A, const void *B, void *C, int64_t M, int64_t N, i
         if (b_tmp)
             cudaFreeAsync(b_tmp, st);
     };
-    if (pl.realign_a && (rc = realign(A, M, K, d->sms, st, &a_tmp, &lda)) != GEMM_OK) {
+    if (pl.realign_a && (rc = realign(A, M, K, eb, d->sms, st, &a_tmp, &lda)) != GEMM_OK) {
         release();
         return rc;
     }
     if (a_tmp)
         a_ptr = a_tmp;
-    if (pl.realign_b && (rc = realign(B, b_mn ? K : N, b_mn ? N : K, d->sms, st, &b_tmp, &ldb)) != GEMM_OK) {
+    if (pl.realign_b &&
+        (rc = realign(B, b_mn ? K : N, b_mn ? N : K, eb, d->sms, st, &b_tmp, &ldb)) != GEMM_OK) {
         release();
         return rc;
     }
     if (b_tmp)
         b_ptr = b_tmp;
 
-    alignas(64) CUtensorMap ta, tb, tc;
-    std::memset(&tc, 0, sizeof(tc));
-    const CUtensorMapDataType in_dt = tma_dtype(dtype_in);
-    bool ok = encode_2d(&ta, in_dt, a_ptr, K, M, lda * 2, BLOCK_K, BLOCK_M_CTA, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!b_mn)
-        ok = ok && encode_2d(&tb, in_dt, b_ptr, K, N, ldb * 2, BLOCK_K, var.bn / var.cg,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-    else
-        ok = ok && encode_2d(&tb, in_dt, b_ptr, N, K, ldb * 2, 64, BLOCK_K, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!pl.direct_store)
-        ok = ok && encode_2d(&tc, tma_dtype(dtype_out), C, N, M, N * esize(dtype_out), EPI_COLS, 32,
-                             dtype_out == GEMM_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-    if (!ok) {
-        release();
-        return GEMM_ERR_CUDA;
-    }
-
-    KernelParams kp = {};
-    kp.M = static_cast<int32_t>(M);
-    kp.N = static_cast<int32_t>(N);
-    kp.K = static_cast<int32_t>(K);
-    kp.num_m_tiles = pl.num_m;
-    kp.num_n_tiles = pl.num_n;
-    kp.num_tiles = pl.num_tiles;
-    kp.num_k_blocks = pl.num_kb;
-    kp.group_m = pl.group_m;
-    kp.idesc = make_idesc_f16(128u * var.cg, static_cast<uint32_t>(var.bn), dtype_in == GEMM_BF16 ? 1u : 0u,
-                              b_mn ? 1u : 0u);
-    kp.out_dtype = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_BF16 ? OUT_BF16 : OUT_F16);
-    kp.b_mn_major = b_mn ? 1u : 0u;
-    kp.direct_store = pl.direct_store ? 1u : 0u;
-    const Layout lay = layout_for(var, dtype_out);
-    kp.stages = lay.stages;
-    kp.staging_bytes = lay.staging_bytes;
-    kp.C = C;
-    kp.timeout_ns = (opts && opts->timeout_ms ? static_cast<uint64_t>(opts->timeout_ms) : DEFAULT_TIMEOUT_MS) *
-                    1000000ull;
-    kp.launch_id = g_next_id.fetch_add(1, std::memory_order_relaxed);
-    kp.status = d->status;
-
-    const cudaError_t err = launch_any(var, pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
+    const uint64_t timeout_ms = opts && opts->timeout_ms ? static_cast<uint64_t>(opts->timeout_ms)
+                                                         : DEFAULT_TIMEOUT_MS;
+    rc = encode_and_launch(*d, pl, a_ptr, lda, b_ptr, ldb, C, M, N, K, dtype_in, dtype_out, b_mn, timeout_ms, st);
     release();
-    if (err != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
-    }
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return GEMM_OK;
+    return rc;
 }
 
 } // namespace
@@ -468,14 +522,14 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype
     if ((rc = device_state(&d)) != GEMM_OK)
         return rc;
     Plan pl;
-    if ((rc = make_plan(*d, M, N, K, dtype_out, layoutB, A, B, C, opts, &pl)) != GEMM_OK)
+    if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, opts, &pl)) != GEMM_OK)
         return rc;
     const Variant &var = kVariants[pl.variant];
     std::memset(plan, 0, sizeof(*plan));
     plan->cta_group = var.cg;
     plan->block_m = 128 * var.cg;
     plan->block_n = var.bn;
-    plan->block_k = BLOCK_K * var.ks;
+    plan->block_k = slab_k(var.eb) * var.ks;
     const Layout lay = layout_for(var, dtype_out);
     plan->stages = static_cast<int32_t>(lay.stages);
     plan->num_tiles = pl.num_tiles;
@@ -501,8 +555,9 @@ gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_hos
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto up256 = [](size_t x) { return (x + 255) / 256 * 256; };
-    const size_t a_bytes = static_cast<size_t>(M * K * 2), b_bytes = static_cast<size_t>(N * K * 2);
-    const size_t c_bytes = static_cast<size_t>(M * N * esize(dtype_out));
+    const int eb = in_bytes(dtype_in);
+    const size_t a_bytes = static_cast<size_t>(M * K * eb), b_bytes = static_cast<size_t>(N * K * eb);
+    const size_t c_bytes = static_cast<size_t>(M * N * out_bytes(dtype_out));
     const size_t need = up256(a_bytes) + up256(b_bytes) + up256(c_bytes);
     std::lock_guard<std::mutex> lock(d->ws_mu);
     if (d->ws_bytes < need) {
@@ -658,21 +713,6 @@ gemm_status_t no_alloc_scratch(void **out)
     return GEMM_OK;
 }
 
-// Re-pitch a rows x cols 16-bit matrix into caller-provided memory `dst`
-// (row pitch ld = cols rounded up to 8 elements). The pad is never read.
-gemm_status_t realign_into(const void *src, int64_t rows, int64_t cols, int64_t ld, int sms,
-                           cudaStream_t st, void *dst)
-{
-    const int64_t total = rows * cols;
-    const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(sms) * 8);
-    realign_rows_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(
-        static_cast<const uint16_t *>(src), static_cast<uint16_t *>(dst), rows, cols, ld);
-    if (cudaGetLastError() != cudaSuccess)
-        return GEMM_ERR_CUDA;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return GEMM_OK;
-}
-
 gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
                            int dtype_in, int dtype_out, int layoutA, int layoutB, cudaStream_t st)
 {
@@ -683,17 +723,17 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
     if ((rc = device_state(&d)) != GEMM_OK)
         return rc;
     Plan pl;
-    if ((rc = make_plan(*d, M, N, K, dtype_out, layoutB, A, B, C, nullptr, &pl)) != GEMM_OK)
+    if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, nullptr, &pl)) != GEMM_OK)
         return rc;
-    const Variant &var = kVariants[pl.variant];
     const bool b_mn = layoutB == GEMM_MN_MAJOR;
+    const int eb = in_bytes(dtype_in);
 
     // Scratch layout: padded A at offset 0, padded B at the next 256-byte boundary.
     const int64_t b_rows = b_mn ? K : N, b_cols = b_mn ? N : K;
-    const int64_t lda_pad = (K + 7) / 8 * 8, ldb_pad = (b_cols + 7) / 8 * 8;
-    const uint64_t a_bytes = pl.realign_a ? static_cast<uint64_t>(M) * lda_pad * 2 : 0;
+    const int64_t lda_pad = padded_pitch(K, eb), ldb_pad = padded_pitch(b_cols, eb);
+    const uint64_t a_bytes = pl.realign_a ? static_cast<uint64_t>(M) * lda_pad * eb : 0;
     const uint64_t b_off = (a_bytes + 255) / 256 * 256;
-    const uint64_t b_bytes = pl.realign_b ? static_cast<uint64_t>(b_rows) * ldb_pad * 2 : 0;
+    const uint64_t b_bytes = pl.realign_b ? static_cast<uint64_t>(b_rows) * ldb_pad * eb : 0;
     if (b_off + b_bytes > GEMM_NO_ALLOC_SCRATCH_BYTES)
         return GEMM_ERR_UNSUPPORTED;   // padded operands exceed the fixed scratch array
 
@@ -705,63 +745,20 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
             return rc;
         char *base = static_cast<char *>(scratch);
         if (pl.realign_a) {
-            if ((rc = realign_into(A, M, K, lda_pad, d->sms, st, base)) != GEMM_OK)
+            if ((rc = realign_into(A, M, K, lda_pad, eb, d->sms, st, base)) != GEMM_OK)
                 return rc;
             a_ptr = base;
             lda = lda_pad;
         }
         if (pl.realign_b) {
-            if ((rc = realign_into(B, b_rows, b_cols, ldb_pad, d->sms, st, base + b_off)) != GEMM_OK)
+            if ((rc = realign_into(B, b_rows, b_cols, ldb_pad, eb, d->sms, st, base + b_off)) != GEMM_OK)
                 return rc;
             b_ptr = base + b_off;
             ldb = ldb_pad;
         }
     }
-
-    alignas(64) CUtensorMap ta, tb, tc;
-    std::memset(&tc, 0, sizeof(tc));
-    const CUtensorMapDataType in_dt = tma_dtype(dtype_in);
-    bool ok = encode_2d(&ta, in_dt, a_ptr, K, M, lda * 2, BLOCK_K, BLOCK_M_CTA, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!b_mn)
-        ok = ok && encode_2d(&tb, in_dt, b_ptr, K, N, ldb * 2, BLOCK_K, var.bn / var.cg,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
-    else
-        ok = ok && encode_2d(&tb, in_dt, b_ptr, N, K, ldb * 2, 64, BLOCK_K, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!pl.direct_store)
-        ok = ok && encode_2d(&tc, tma_dtype(dtype_out), C, N, M, N * esize(dtype_out), EPI_COLS, 32,
-                             dtype_out == GEMM_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
-    if (!ok)
-        return GEMM_ERR_CUDA;
-
-    KernelParams kp = {};
-    kp.M = static_cast<int32_t>(M);
-    kp.N = static_cast<int32_t>(N);
-    kp.K = static_cast<int32_t>(K);
-    kp.num_m_tiles = pl.num_m;
-    kp.num_n_tiles = pl.num_n;
-    kp.num_tiles = pl.num_tiles;
-    kp.num_k_blocks = pl.num_kb;
-    kp.group_m = pl.group_m;
-    kp.idesc = make_idesc_f16(128u * var.cg, static_cast<uint32_t>(var.bn), dtype_in == GEMM_BF16 ? 1u : 0u,
-                              b_mn ? 1u : 0u);
-    kp.out_dtype = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_BF16 ? OUT_BF16 : OUT_F16);
-    kp.b_mn_major = b_mn ? 1u : 0u;
-    kp.direct_store = pl.direct_store ? 1u : 0u;
-    const Layout lay = layout_for(var, dtype_out);
-    kp.stages = lay.stages;
-    kp.staging_bytes = lay.staging_bytes;
-    kp.C = C;
-    kp.timeout_ns = DEFAULT_TIMEOUT_MS * 1000000ull;
-    kp.launch_id = g_next_id.fetch_add(1, std::memory_order_relaxed);
-    kp.status = d->status;
-
-    const cudaError_t err = launch_any(var, pl.grid_ctas, lay.smem, ta, tb, tc, kp, st);
-    if (err != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
-    }
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return GEMM_OK;
+    return encode_and_launch(*d, pl, a_ptr, lda, b_ptr, ldb, C, M, N, K, dtype_in, dtype_out, b_mn,
+                             DEFAULT_TIMEOUT_MS, st);
 }
 
 } // namespace

@@ -1,7 +1,7 @@
 // gemm_kernel.cuh: the persistent, warp-specialised tcgen05 GEMM for sm_103a.
 //
-// C = A·B with FP16/BF16 operands, an FP32 accumulator in tensor memory (TMEM)
-// and a cast on store. "Two Waves, One Stage Apart" (sections "Why the Matrix
+// C = A·B with FP16/BF16 or FP8 (E4M3/E5M2) operands, an FP32 accumulator in
+// tensor memory (TMEM) and a cast on store. "Two Waves, One Stage Apart" (sections "Why the Matrix
 // Pipeline Drains" and "Two Waves, One Stage Apart") keeps the matrix unit
 // busy by holding data preparation one stage ahead of matrix work. Here that
 // offset comes from fixed warp roles linked by shared-memory barriers, not
@@ -50,9 +50,13 @@
 
 namespace dtg {
 
-constexpr int BLOCK_K = 64;          // one K slab: 64 x 16-bit = one 128-byte swizzle row
+constexpr int SLAB_BYTES = 128;      // one K slab: one 128-byte swizzle row of every operand row
 constexpr int BLOCK_M_CTA = 128;     // accumulator rows per CTA = TMEM lanes
-constexpr int UMMA_K = 16;           // K of one kind::f16 tcgen05.mma
+constexpr int MMA_K_BYTES = 32;      // K bytes of one tcgen05.mma (K = 16 FP16/BF16, 32 FP8)
+constexpr int SLAB_MMAS = SLAB_BYTES / MMA_K_BYTES;
+
+// K elements in one slab: 64 for 16-bit operands, 128 for FP8.
+__host__ __device__ constexpr int slab_k(int elem_bytes) { return SLAB_BYTES / elem_bytes; }
 constexpr int NUM_THREADS = 192;     // producer warp, MMA warp, 4 epilogue warps
 constexpr int EPI_WARP0 = 2;
 constexpr int TMEM_COLS = 512;       // two accumulators at columns 0 and 256
@@ -90,25 +94,29 @@ struct KernelParams {
     unsigned long long *status;  // [0] first timed-out launch, [1] site, [2] last timed-out launch
 };
 
-// KS = K slabs per ring stage. One slab is a 64-wide K strip of A and B in the
-// 128-byte swizzle layout (4 MMAs of K = 16). A stage holds KS slabs of A then
-// KS slabs of B, so one barrier wait on the MMA thread covers 4 x KS MMAs.
-template <int CG, int BN, int KS>
+// KS = K slabs per ring stage, EB = operand element bytes (2: FP16/BF16, 1:
+// FP8). One slab is a 128-byte-wide K strip of A and B in the 128-byte swizzle
+// layout (64 K of 16-bit operands or 128 K of FP8: 4 MMAs either way). A stage
+// holds KS slabs of A then KS slabs of B, so one barrier wait on the MMA
+// thread covers 4 x KS MMAs. The byte layout does not depend on EB.
+template <int CG, int BN, int KS, int EB>
 struct TileConfig {
     static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
     static_assert(KS == 1 || KS == 2, "one or two K slabs per stage");
+    static_assert(EB == 1 || EB == 2, "8-bit or 16-bit operands");
     static constexpr int BN_CTA = BN / CG;   // B rows (K-major) or columns (MN-major) per CTA
     static_assert(BN % (16 * CG) == 0 && BN <= 256 && BN_CTA % 8 == 0, "invalid tile width");
-    static constexpr int A_SLAB = BLOCK_M_CTA * BLOCK_K * 2;
-    static constexpr int B_SLAB = BN_CTA * BLOCK_K * 2;
+    static constexpr int SLAB_K = slab_k(EB);
+    static constexpr int A_SLAB = BLOCK_M_CTA * SLAB_BYTES;
+    static constexpr int B_SLAB = BN_CTA * SLAB_BYTES;
     static constexpr int A_BYTES = KS * A_SLAB;
     static constexpr int STAGE_BYTES = KS * (A_SLAB + B_SLAB);
-    static constexpr int STAGE_K = KS * BLOCK_K;
+    static constexpr int STAGE_K = KS * SLAB_K;
     static_assert(A_SLAB % 1024 == 0 && B_SLAB % 1024 == 0, "slabs must stay 1024-byte aligned");
 };
 
 // Dynamic shared memory, from a 1024-byte aligned base:
-//   ring      stages x {KS slabs of A 128x64, KS slabs of B BN_CTA x 64} (128-byte swizzle)
+//   ring      stages x {KS slabs of A 128 x 128 B, KS slabs of B BN_CTA x 128 B} (128-byte swizzle)
 //   staging   4 epilogue warps x 2 buffers x staging_bytes (2 KB for 16-bit C, 4 KB for FP32 C)
 //   barriers  full[stages], empty[stages], tmem_full[2], tmem_empty[2], mma_done
 //   TMEM base address written by tcgen05.alloc
@@ -281,13 +289,13 @@ __device__ __forceinline__ void store_row_direct(const KernelParams &p, int row,
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int CG, int BN, int KS>
+template <int CG, int BN, int KS, int EB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
                     const __grid_constant__ CUtensorMap tmap_c, const KernelParams p)
 {
-    using Cfg = TileConfig<CG, BN, KS>;
+    using Cfg = TileConfig<CG, BN, KS, EB>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     if (base & 1023u) {
@@ -368,10 +376,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                             mbar_arrive_expect_tx(bar, Cfg::STAGE_BYTES);
 #pragma unroll
                             for (int j = 0; j < KS; ++j) {
-                                const int kj = k0 + j * BLOCK_K;
+                                const int kj = k0 + j * Cfg::SLAB_K;
                                 tma_load_2d(a_dst + j * Cfg::A_SLAB, &tmap_a, bar, kj, a_row);
                                 const uint32_t bj = b_dst + j * Cfg::B_SLAB;
-                                if (!p.b_mn_major)
+                                if (EB == 1 || !p.b_mn_major)
                                     tma_load_2d(bj, &tmap_b, bar, kj, b_off);
                                 else
                                     for (int i = 0; i < Cfg::BN_CTA / 64; ++i)
@@ -384,10 +392,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                 mbar_arrive_expect_tx(full_bar(s), 2u * Cfg::STAGE_BYTES);
 #pragma unroll
                             for (int j = 0; j < KS; ++j) {
-                                const int kj = k0 + j * BLOCK_K;
+                                const int kj = k0 + j * Cfg::SLAB_K;
                                 tma_load_2d_pair(a_dst + j * Cfg::A_SLAB, &tmap_a, bar, kj, a_row);
                                 const uint32_t bj = b_dst + j * Cfg::B_SLAB;
-                                if (!p.b_mn_major)
+                                if (EB == 1 || !p.b_mn_major)
                                     tma_load_2d_pair(bj, &tmap_b, bar, kj, b_off);
                                 else
                                     for (int i = 0; i < Cfg::BN_CTA / 64; ++i)
@@ -414,10 +422,11 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && (CG == 1 || rank == 0)) {
-            const bool b_mn = p.b_mn_major != 0;
-            // K-major: rows of 128 B in 8-row groups 1024 B apart; one K=16 step = 32 B.
-            // MN-major: 64-wide N atoms 8192 B apart (LBO), 8-row K groups 1024 B
-            // apart (SBO); one K=16 step = 16 rows = 2048 B.
+            // FP8 operands are K-major only (the host rejects MN-major FP8 B).
+            const bool b_mn = EB == 2 && p.b_mn_major != 0;
+            // K-major: rows of 128 B in 8-row groups 1024 B apart; one MMA step = 32 B.
+            // MN-major (16-bit): 64-wide N atoms 8192 B apart (LBO), 8-row K groups
+            // 1024 B apart (SBO); one K=16 step = 16 rows = 2048 B.
             const uint32_t b_lbo = b_mn ? 8192u : 16u;
             const uint32_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
             uint32_t s = 0, ph = 0, acc = 0, acc_ph = 0;
@@ -433,14 +442,14 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
 #pragma unroll
                         for (int j = 0; j < KS; ++j) {
                             // a slab wholly past K holds only TMA zero fill: skip its MMAs
-                            if (j > 0 && kb * Cfg::STAGE_K + j * BLOCK_K >= p.K)
+                            if (j > 0 && kb * Cfg::STAGE_K + j * Cfg::SLAB_K >= p.K)
                                 break;
                             const uint64_t a_desc = smem_desc_sw128(a_addr + j * Cfg::A_SLAB, 16u, 1024u);
                             const uint64_t b_desc = smem_desc_sw128(a_addr + Cfg::A_BYTES + j * Cfg::B_SLAB,
                                                                     b_lbo, 1024u);
 #pragma unroll
-                            for (uint32_t k = 0; k < BLOCK_K / UMMA_K; ++k)
-                                mma_f16<CG>(d_tmem, a_desc + 2u * k, b_desc + b_step * k, p.idesc,
+                            for (uint32_t k = 0; k < SLAB_MMAS; ++k)
+                                mma<CG, EB>(d_tmem, a_desc + 2u * k, b_desc + b_step * k, p.idesc,
                                             (kb > 0 || j > 0 || k > 0) ? 1u : 0u);
                         }
                         if constexpr (CG == 1)
@@ -565,11 +574,12 @@ __global__ void wait_selftest_kernel(uint64_t timeout_ns, unsigned long long lau
     }
 }
 
-// Copy a rows x cols matrix of 16-bit elements (row pitch `cols`, any 2-byte
-// alignment) to a buffer whose row pitch `ld_dst` is a multiple of 8 elements
-// and whose base is 256-byte aligned, so the TMA engine can describe it.
-__global__ void realign_rows_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst,
-                                    int64_t rows, int64_t cols, int64_t ld_dst)
+// Copy a rows x cols matrix of T (row pitch `cols`, any alignment of T) to a
+// buffer whose row pitch `ld_dst` is a multiple of 16 bytes and whose base is
+// 256-byte aligned, so the TMA engine can describe it.
+template <typename T>
+__global__ void realign_rows_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t rows,
+                                    int64_t cols, int64_t ld_dst)
 {
     const int64_t total = rows * cols;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;

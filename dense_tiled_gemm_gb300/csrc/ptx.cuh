@@ -250,21 +250,37 @@ __device__ __forceinline__ void tc_fence_after_sync()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] · B[smem], kind::f16 (FP16/BF16 in, FP32 accumulate).
-template <int CG>
-__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate)
+// D[tmem] (+)= A[smem] · B[smem] with an FP32 accumulator. EB is the operand
+// element width: 2 bytes -> kind::f16 (FP16/BF16, K = 16 per instruction),
+// 1 byte -> kind::f8f6f4 (E4M3/E5M2, K = 32 per instruction). Either way one
+// instruction consumes 32 bytes of K from every operand row.
+template <int CG, int EB>
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                    uint32_t accumulate)
 {
-    if constexpr (CG == 1)
+    static_assert(EB == 1 || EB == 2, "8-bit or 16-bit operands");
+    if constexpr (CG == 1 && EB == 2)
         asm volatile("{\n\t.reg .pred p;\n\t"
                      "setp.ne.b32 p, %4, 0;\n\t"
                      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
                      : "memory");
-    else
+    else if constexpr (CG == 2 && EB == 2)
         asm volatile("{\n\t.reg .pred p;\n\t"
                      "setp.ne.b32 p, %4, 0;\n\t"
                      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                     : "memory");
+    else if constexpr (CG == 1)
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                     : "memory");
+    else
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
                      : "memory");
 }
@@ -326,14 +342,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
     return d;
 }
 
-// Instruction descriptor for kind::f16 with an FP32 accumulator:
-// D format bits 4-5 (1 = F32), A format bits 7-9 and B format bits 10-12
-// (0 = F16, 1 = BF16), A major bit 15 (0 = K), B major bit 16 (1 = MN),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-__host__ __device__ constexpr uint32_t make_idesc_f16(uint32_t M, uint32_t N, uint32_t ab_bf16,
-                                                      uint32_t b_mn_major)
+// Instruction descriptor for kind::f16 and kind::f8f6f4 with an FP32
+// accumulator: D format bits 4-5 (1 = F32), A format bits 7-9 and B format
+// bits 10-12, A major bit 15 (0 = K), B major bit 16 (1 = MN), N >> 3 in bits
+// 17-22, M >> 4 in bits 24-28. The format code is 0 for F16 (kind::f16) or
+// E4M3 (kind::f8f6f4), 1 for BF16 or E5M2.
+__host__ __device__ constexpr uint32_t make_idesc(uint32_t M, uint32_t N, uint32_t ab_format,
+                                                  uint32_t b_mn_major)
 {
-    return (1u << 4) | (ab_bf16 << 7) | (ab_bf16 << 10) | (b_mn_major << 16) | ((N >> 3) << 17) |
+    return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (b_mn_major << 16) | ((N >> 3) << 17) |
            ((M >> 4) << 24);
 }
 

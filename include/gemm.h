@@ -1,12 +1,15 @@
 /*
  * gemm.h: C ABI of the GB300 (sm_103a) dense tiled GEMM library.
  *
- * The library computes C = A·B for FP16 or BF16 operands. It accumulates in
- * FP32 in tensor memory and casts on store to FP16, BF16 or FP32. The
- * operation is the tiled GEMM of "Two Waves, One Stage Apart:
+ * The library computes C = A·B for FP16, BF16 or FP8 (E4M3, E5M2) operands.
+ * It accumulates in FP32 in tensor memory and casts on store to FP16, BF16
+ * or FP32. The operation is the tiled GEMM of "Two Waves, One Stage Apart:
  * Warp-Pipelining Triton GEMMs on AMD Instinct" (opening paragraph: compute
- * on one pair of operand tiles while the next pair is prepared). Throughput
- * is counted as 2·M·N·K / elapsed time, as in that page's Table 1 caption.
+ * on one pair of operand tiles while the next pair is prepared). The FP8
+ * form is the GEMM of "Porting High-Performance HIP Kernels to FlyDSL"
+ * (section "A More Complex Kernel"): E4M3 operands whose block scales are
+ * all 1.0, so that C is the plain product. Throughput is counted as
+ * 2·M·N·K / elapsed time, as in the first page's Table 1 caption.
  *
  * Conventions shared by every entry point:
  *   - A is M x K, row-major (K contiguous, leading dimension K).
@@ -34,10 +37,16 @@
 extern "C" {
 #endif
 
+/* Element types. F16 and BF16 serve as input or output types, F32 only as an
+ * output type, E4M3 and E5M2 only as input types. E4M3 is the OCP 8-bit
+ * "FN" format (bias 7, no infinities, largest finite 448); E5M2 is the OCP
+ * 8-bit IEEE-style format (bias 15). */
 typedef enum {
     GEMM_F16 = 0,
     GEMM_BF16 = 1,
-    GEMM_F32 = 2
+    GEMM_F32 = 2,
+    GEMM_E4M3 = 3,
+    GEMM_E5M2 = 4
 } gemm_dtype_t;
 
 typedef enum {
@@ -58,19 +67,22 @@ typedef enum {
 /*
  * gemm: C = A·B on the current CUDA device.
  *
- *   A, B, C   device pointers (layouts above). A and B are FP16 or BF16, and
- *             they must share a type. C has type dtype_out.
+ *   A, B, C   device pointers (layouts above). A and B share one type,
+ *             dtype_in. C has type dtype_out.
  *   M, N, K   sizes, each >= 1. K = 0 is rejected (GEMM_ERR_INVALID_ARG).
- *   dtype_in  GEMM_F16 or GEMM_BF16: the type of both A and B.
+ *   dtype_in  GEMM_F16, GEMM_BF16, GEMM_E4M3 or GEMM_E5M2: the type of both
+ *             A and B (GEMM_F32 gives GEMM_ERR_UNSUPPORTED).
  *   dtype_out GEMM_F16, GEMM_BF16 or GEMM_F32. The FP32 accumulator is
- *             rounded to nearest-even when it is cast.
+ *             rounded to nearest-even when it is cast. An FP8 output type
+ *             gives GEMM_ERR_UNSUPPORTED.
  *   layoutA   must be GEMM_K_MAJOR (GEMM_MN_MAJOR gives GEMM_ERR_UNSUPPORTED).
- *   layoutB   GEMM_K_MAJOR or GEMM_MN_MAJOR.
+ *   layoutB   GEMM_K_MAJOR or GEMM_MN_MAJOR; FP8 operands need GEMM_K_MAJOR
+ *             (GEMM_MN_MAJOR gives GEMM_ERR_UNSUPPORTED).
  *   stream    cudaStream_t as void*.
  *
  * Alignment: the tensor-memory-access engine needs 16-byte-aligned bases and
- * row pitches. When A or B misses this (for example K*2 bytes not a multiple
- * of 16), the call first copies that operand into a padded, stream-ordered
+ * row pitches. When A or B misses this (for example K*2 bytes, or K bytes for
+ * FP8, not a multiple of 16), the call first copies that operand into a padded, stream-ordered
  * scratch buffer. It takes this buffer with cudaMallocAsync and frees it with
  * cudaFreeAsync on the same stream. When C misses it, the epilogue writes C
  * with ordinary stores instead of bulk tensor stores. Results do not depend
@@ -99,7 +111,9 @@ gemm_status_t gemm(const void *A, const void *B, void *C,
  *                 makes each CTA loop over many tiles.
  *   group_m       raster group height in tiles, for the swizzled tile order.
  *   timeout_ms    per-wait limit inside the kernel (default 2000).
- *   k_stage       K depth of one shared-memory ring stage: 64 or 128.
+ *   k_stage       K depth of one shared-memory ring stage, in elements: one or
+ *                 two 128-byte slabs, so 64 or 128 for FP16/BF16 and 128 or
+ *                 256 for FP8. Other values give GEMM_ERR_UNSUPPORTED.
  */
 typedef struct {
     int32_t cta_group;
@@ -126,7 +140,7 @@ typedef struct {
     int32_t cta_group;     /* CTAs per output tile */
     int32_t block_m;       /* rows per output tile (128 * cta_group) */
     int32_t block_n;       /* columns per output tile */
-    int32_t block_k;       /* K per pipeline stage (64 or 128) */
+    int32_t block_k;       /* K per pipeline stage (64/128 16-bit, 128/256 FP8) */
     int32_t stages;        /* shared-memory ring depth */
     int32_t num_tiles;     /* output tiles */
     int32_t grid_ctas;     /* persistent CTAs launched */
@@ -198,8 +212,8 @@ gemm_status_t gemm_selftest_wait_timeout(int32_t timeout_ms, void *stream);
  * loads it, GEMM_NO_ALLOC_SCRATCH_BYTES (32 MiB) in size, until the process
  * exits.
  *
- *   - Limit: the padded copies (rows x pitch rounded up to 8 elements x 2
- *     bytes, A then B, each started on a 256-byte boundary) must fit in
+ *   - Limit: the padded copies (rows x row bytes rounded up to 16, A then B,
+ *     each started on a 256-byte boundary) must fit in
  *     GEMM_NO_ALLOC_SCRATCH_BYTES. Otherwise the call returns
  *     GEMM_ERR_UNSUPPORTED and launches nothing. When no operand needs
  *     re-pitching the array is not used, and there is no size limit beyond

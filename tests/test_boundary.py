@@ -41,7 +41,8 @@ def test_library_exports_every_declared_function():
 
 def test_enums_match_header():
     text = header_text()
-    for name, val in (("GEMM_F16", 0), ("GEMM_BF16", 1), ("GEMM_F32", 2), ("GEMM_K_MAJOR", 0),
+    for name, val in (("GEMM_F16", 0), ("GEMM_BF16", 1), ("GEMM_F32", 2), ("GEMM_E4M3", 3),
+                      ("GEMM_E5M2", 4), ("GEMM_K_MAJOR", 0),
                       ("GEMM_MN_MAJOR", 1), ("GEMM_OK", 0), ("GEMM_ERR_INVALID_ARG", 1),
                       ("GEMM_ERR_UNSUPPORTED", 2), ("GEMM_ERR_CUDA", 3), ("GEMM_ERR_TIMEOUT", 4),
                       ("GEMM_ERR_NO_DEVICE", 5), ("GEMM_ERR_OUT_OF_MEMORY", 6)):
@@ -70,6 +71,9 @@ def call(M=64, N=64, K=64, din=0, dout=0, la=0, lb=0, a=FAKE, b=FAKE, c=FAKE):
     (dict(M=0), 1), (dict(N=0), 1), (dict(K=0), 1), (dict(M=-5), 1), (dict(K=2 ** 31), 1),
     (dict(din=7), 1), (dict(din=2), 2), (dict(dout=5), 1), (dict(dout=-1), 1),
     (dict(la=1), 2), (dict(la=3), 1), (dict(lb=2), 1),
+    (dict(dout=3), 2), (dict(dout=4), 2),                      # FP8 is an input type only
+    (dict(din=3, lb=1), 2), (dict(din=4, lb=1), 2),            # FP8 B must be K-major
+    (dict(din=3, lb=2), 1),
 ])
 def test_invalid_arguments_rejected_on_host(kwargs, expect):
     assert call(**kwargs) == expect
@@ -83,6 +87,24 @@ def test_invalid_options_rejected_on_host():
         setattr(o, field, val)
         rc = binding.lib.gemm_ex(FAKE, FAKE, FAKE, 64, 64, 64, 0, 0, 0, 0, ctypes.byref(o), None)
         assert rc == expect, field
+
+
+@pytest.mark.parametrize("din,k_stage,expect", [(0, 256, 2), (3, 64, 2), (4, 192, 2), (3, -128, 1)])
+def test_k_stage_depends_on_input_width(din, k_stage, expect):
+    """k_stage counts elements: one or two 128-byte slabs (64/128 for 16-bit, 128/256 for FP8)."""
+    o = binding.GemmOptions()
+    o.k_stage = k_stage
+    rc = binding.lib.gemm_ex(FAKE, FAKE, FAKE, 64, 64, 64, din, 0, 0, 0, ctypes.byref(o), None)
+    assert rc == expect
+
+
+def test_python_wrapper_accepts_fp8_types():
+    import torch
+    A = torch.zeros(4, 8, dtype=torch.float8_e4m3fn)
+    with pytest.raises(ValueError):
+        dtg.gemm(A, torch.zeros(5, 8, dtype=torch.float8_e4m3fn))   # CPU tensors, not a type error
+    with pytest.raises(TypeError):
+        dtg.gemm_from_host(A, torch.zeros(5, 8, dtype=torch.float8_e5m2))   # mixed FP8 types
 
 
 def test_plan_requires_output_struct():
