@@ -61,6 +61,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--compare-cublas", action="store_true",
                     help="also time torch.matmul (cuBLAS) the same way, as a labelled comparison")
+    ap.add_argument("--stream-k", choices=["auto", "off", "on"], default="auto",
+                    help="tail scheduling of the GEMM (gemm_options_t.stream_k); auto = the planner")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
@@ -330,9 +332,11 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
 
+    opts = None if args.stream_k == "auto" else {"stream_k": {"off": 1, "on": 2}[args.stream_k]}
+
     def step(i):
         j = i % n_sets
-        dtg.gemm(As[j], Bs[j], Cs[j], layout_b=w.layout_b, stream=stream)
+        dtg.gemm(As[j], Bs[j], Cs[j], layout_b=w.layout_b, stream=stream, options=opts)
 
     for i in range(args.warmup):
         step(i)
@@ -388,7 +392,7 @@ def run_ours(args):
     achieved = flops_step / (kernel_ms * 1e-3) / 1e12
     plan = dtg.gemm_plan(w.M, w.N, w.K, dtype_in=workloads.DTYPES[w.dtype_in], dtype_out=out_dt,
                          layout_b=w.layout_b, a_ptr=As[0].data_ptr(), b_ptr=Bs[0].data_ptr(),
-                         c_ptr=Cs[0].data_ptr())
+                         c_ptr=Cs[0].data_ptr(), options=opts)
 
     cublas = None
     if args.compare_cublas:

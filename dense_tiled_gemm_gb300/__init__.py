@@ -15,12 +15,12 @@ import torch
 
 from . import binding
 from .binding import (GEMM_BF16, GEMM_E4M3, GEMM_E5M2, GEMM_F16, GEMM_F32, GEMM_K_MAJOR,
-                      GEMM_MN_MAJOR, GEMM_OK, GEMM_ERR_TIMEOUT, GemmError, GemmOptions, GemmPlan,
-                      STATUS_NAMES)
+                      GEMM_MN_MAJOR, GEMM_OK, GEMM_ERR_TIMEOUT, GEMM_JOB_FULL, GEMM_JOB_OWNER,
+                      GEMM_JOB_WRITER, GemmError, GemmJob, GemmOptions, GemmPlan, STATUS_NAMES)
 
 __all__ = ["gemm", "gemm_ex", "gemm_plan", "gemm_from_host", "gemm_release_workspace",
            "gemm_last_device_status", "gemm_selftest_wait_timeout", "gemm_status_string",
-           "gemm_launch_count", "GemmError", "GemmOptions", "GemmPlan"]
+           "gemm_launch_count", "gemm_schedule_jobs", "GemmError", "GemmOptions", "GemmPlan"]
 
 _DT_IN = {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16,
           torch.float8_e4m3fn: GEMM_E4M3, torch.float8_e5m2: GEMM_E5M2}
@@ -112,7 +112,8 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *,
 
 
 def gemm_ex(A, B, C=None, *, options=None, **kw) -> torch.Tensor:
-    """gemm with gemm_ex overrides (cta_group, block_n, max_clusters, group_m, timeout_ms)."""
+    """gemm with gemm_ex overrides (cta_group, block_n, max_clusters, group_m, timeout_ms,
+    k_stage, stream_k)."""
     return gemm(A, B, C, options=options if options is not None else GemmOptions(), **kw)
 
 
@@ -168,6 +169,19 @@ def gemm_status_string(status: int) -> str:
 
 def gemm_launch_count() -> int:
     return int(binding.lib.gemm_launch_count())
+
+
+def gemm_schedule_jobs(num_tiles: int, units: int, k_blocks: int, sk_tiles: int,
+                       unit: int) -> list[tuple[int, int, int, int]]:
+    """The kernel's work list for one unit, as (tile, kb_begin, kb_end, kind) tuples in
+    run order; kind is GEMM_JOB_FULL, GEMM_JOB_WRITER or GEMM_JOB_OWNER. No GPU needed."""
+    n = ctypes.c_int32(0)
+    _check(binding.lib.gemm_schedule_jobs(num_tiles, units, k_blocks, sk_tiles, unit, None, 0,
+                                          ctypes.byref(n)), "gemm_schedule_jobs")
+    jobs = (GemmJob * max(1, n.value))()
+    _check(binding.lib.gemm_schedule_jobs(num_tiles, units, k_blocks, sk_tiles, unit, jobs, n.value,
+                                          ctypes.byref(n)), "gemm_schedule_jobs")
+    return [(j.tile, j.kb_begin, j.kb_end, j.kind) for j in jobs[:n.value]]
 
 
 def gemm_no_alloc(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *, layout_b: str = "k",

@@ -30,7 +30,7 @@ class GemmOptions(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int32), ("block_n", ctypes.c_int32),
                 ("max_clusters", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("timeout_ms", ctypes.c_int32), ("k_stage", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("stream_k", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 class GemmPlan(ctypes.Structure):
@@ -40,10 +40,19 @@ class GemmPlan(ctypes.Structure):
                 ("grid_ctas", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("realign_a", ctypes.c_int32), ("realign_b", ctypes.c_int32),
                 ("direct_store", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
-                ("num_sms", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("num_sms", ctypes.c_int32), ("sk_tiles", ctypes.c_int32),
+                ("workspace_bytes", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+
+
+class GemmJob(ctypes.Structure):
+    _fields_ = [("tile", ctypes.c_int32), ("kb_begin", ctypes.c_int32),
+                ("kb_end", ctypes.c_int32), ("kind", ctypes.c_int32)]
+
+
+GEMM_JOB_FULL, GEMM_JOB_WRITER, GEMM_JOB_OWNER = 0, 1, 2
 
 
 class GemmError(RuntimeError):
@@ -74,6 +83,9 @@ def _declare(lib):
     lib.gemm_status_string.argtypes = [c_int]
     lib.gemm_launch_count.restype = ctypes.c_uint64
     lib.gemm_launch_count.argtypes = []
+    lib.gemm_schedule_jobs.restype = c_int
+    lib.gemm_schedule_jobs.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(GemmJob), i32,
+                                       ctypes.POINTER(i32)]
     return lib
 
 

@@ -15,6 +15,7 @@
 #include <climits>
 #include <cstring>
 #include <mutex>
+#include <random>
 
 #include "gemm.h"
 #include "gemm_kernel.cuh"
@@ -93,7 +94,26 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[MAX_DEVICES];
 std::atomic<uint64_t> g_launches{0};
-std::atomic<unsigned long long> g_next_id{1};
+// Launch ids start at a random 64-bit value. Stream-K flags are compared with
+// the launch id, and a per-call workspace may hold any old bytes: a random
+// start makes an accidental match with a stale word vanishingly unlikely
+// (ids of this library's own earlier launches never match).
+unsigned long long first_launch_id()
+{
+    std::random_device rd;
+    unsigned long long v = (static_cast<unsigned long long>(rd()) << 32) ^ rd();
+    return v ? v : 1;
+}
+std::atomic<unsigned long long> g_next_id{first_launch_id()};
+
+unsigned long long next_launch_id()
+{
+    unsigned long long id;
+    do
+        id = g_next_id.fetch_add(1, std::memory_order_relaxed);
+    while (id == 0);   // 0 means "no timeout" in the device status word
+    return id;
+}
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool is_fp8(int dtype) { return dtype == GEMM_E4M3 || dtype == GEMM_E5M2; }
@@ -200,8 +220,10 @@ gemm_status_t validate(const void *A, const void *B, const void *C, int64_t M, i
             return GEMM_ERR_INVALID_ARG;
         if (o->block_n != 0 && o->block_n != 224 && o->block_n != 256)
             return GEMM_ERR_UNSUPPORTED;
-        if (o->k_stage < 0)
+        if (o->k_stage < 0 || o->stream_k < 0 || o->reserved != 0)
             return GEMM_ERR_INVALID_ARG;
+        if (o->stream_k > 2)
+            return GEMM_ERR_UNSUPPORTED;
         const int sk = slab_k(in_bytes(dtype_in));
         if (o->k_stage != 0 && o->k_stage != sk && o->k_stage != 2 * sk)
             return GEMM_ERR_UNSUPPORTED;
@@ -214,8 +236,45 @@ struct Plan {
     int num_m, num_n, num_tiles, num_kb;
     int grid_ctas;
     int group_m;
+    int sk_tiles;          // trailing tiles split along K
+    size_t ws_bytes;       // stream-K workspace: flags, then partial sums
     bool realign_a, realign_b, direct_store;
 };
+
+// Stream-K workspace of a launch: one flag per (CTA, epilogue warp), then one
+// partial-sum slot per CTA (128 rows x block_n FP32).
+size_t sk_flag_bytes(int grid_ctas) { return (static_cast<size_t>(grid_ctas) * 4 * 8 + 255) / 256 * 256; }
+size_t sk_workspace_bytes(int grid_ctas, int bn)
+{
+    return sk_flag_bytes(grid_ctas) + static_cast<size_t>(grid_ctas) * BLOCK_M_CTA * bn * 4;
+}
+
+// Stream-K tiles for T tiles on U units: the last partial wave plus one full
+// wave (so every tile is cut at most once while units >= tiles), or all
+// tiles when there are fewer than two waves.
+int sk_tiles_for(int64_t T, int64_t U) { return static_cast<int>(T < 2 * U ? T : U + T % U); }
+
+// Relative time of a plan, in whole-tile times of a block_n-wide tile:
+// data-parallel waves, or DP waves + an equal stream-K share + the owner's
+// reads of partial sums. A partial slot of 128 x block_n FP32 read from L2 at
+// ~100 GB/s per SM takes about 600 / (K bytes) of a tile's MMA time.
+struct Cost {
+    double dp, sk;
+    int sk_tiles;
+};
+
+Cost plan_cost(int64_t T, int64_t U, int64_t KB, int64_t K, int eb)
+{
+    Cost c;
+    c.dp = static_cast<double>((T + U - 1) / U);
+    const int64_t S = sk_tiles_for(T, U);
+    c.sk_tiles = static_cast<int>(S);
+    const int64_t L = (S * KB + U - 1) / U;                    // k-blocks per unit
+    const int64_t writers = L >= KB ? 1 : (KB + L - 1) / L;    // other units per split tile
+    const double F = 600.0 / static_cast<double>(K * eb);
+    c.sk = static_cast<double>((T - S) / U) + static_cast<double>(L) / KB + writers * F;
+    return c;
+}
 
 bool misaligned(const void *p, int64_t row_elems, int elem_bytes)
 {
@@ -231,7 +290,8 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
 {
     const bool b_mn = layoutB == GEMM_MN_MAJOR;
     const int eb = in_bytes(dtype_in);
-    int best = -1;
+    const int mode = o ? o->stream_k : 0;
+    int best = -1, best_sk = 0;
     double best_cost = 0;
     for (int v = 0; v < NUM_VARIANTS; ++v) {
         const Variant &var = kVariants[v];
@@ -251,11 +311,16 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
         if (units < 1)
             continue;
         const int64_t tiles = ((M + 128 * var.cg - 1) / (128 * var.cg)) * ((N + var.bn - 1) / var.bn);
-        const int64_t waves = (tiles + units - 1) / units;
-        const double cost = static_cast<double>(waves) * var.bn * (var.cg == 1 ? 1.15 : 1.0);
+        const int64_t kb = (K + static_cast<int64_t>(slab_k(eb)) * var.ks - 1) / (static_cast<int64_t>(slab_k(eb)) * var.ks);
+        const Cost c = plan_cost(tiles, units, kb, K, eb);
+        const double scale = var.bn * (var.cg == 1 ? 1.15 : 1.0);
+        // stream-K only where it saves more than 3%, or when asked for
+        const bool sk = mode == 2 || (mode == 0 && tiles % units != 0 && c.sk < 0.97 * c.dp);
+        const double cost = (sk ? c.sk : c.dp) * scale;
         if (best < 0 || cost < best_cost) {
             best = v;
             best_cost = cost;
+            best_sk = sk ? c.sk_tiles : 0;
         }
     }
     if (best < 0)
@@ -273,7 +338,10 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
     pl->num_tiles = static_cast<int>(tiles);
     const int64_t stage_k = static_cast<int64_t>(slab_k(eb)) * var.ks;
     pl->num_kb = static_cast<int>((K + stage_k - 1) / stage_k);
-    pl->grid_ctas = static_cast<int>(std::min<int64_t>(tiles, units)) * var.cg;
+    pl->sk_tiles = best_sk;
+    // with stream-K every unit takes a share; otherwise no more units than tiles
+    pl->grid_ctas = static_cast<int>(best_sk ? units : std::min<int64_t>(tiles, units)) * var.cg;
+    pl->ws_bytes = best_sk ? sk_workspace_bytes(pl->grid_ctas, var.bn) : 0;
     pl->group_m = (o && o->group_m) ? o->group_m : 8;
     pl->realign_a = misaligned(A, K, eb);
     pl->realign_b = misaligned(B, b_mn ? N : K, eb);
@@ -395,7 +463,8 @@ cudaError_t launch_any(const Variant &v, int grid_ctas, uint32_t smem, const CUt
 // elements), and launch the plan's kernel on `st`.
 gemm_status_t encode_and_launch(const DeviceState &d, const Plan &pl, const void *a_ptr, int64_t lda,
                                 const void *b_ptr, int64_t ldb, void *C, int64_t M, int64_t N, int64_t K,
-                                int dtype_in, int dtype_out, bool b_mn, uint64_t timeout_ms, cudaStream_t st)
+                                int dtype_in, int dtype_out, bool b_mn, uint64_t timeout_ms, void *workspace,
+                                cudaStream_t st)
 {
     const Variant &var = kVariants[pl.variant];
     const int eb = var.eb;
@@ -432,8 +501,13 @@ gemm_status_t encode_and_launch(const DeviceState &d, const Plan &pl, const void
     kp.stages = lay.stages;
     kp.staging_bytes = lay.staging_bytes;
     kp.C = C;
+    kp.sk_tiles = pl.sk_tiles;
+    if (pl.sk_tiles) {
+        kp.flags = static_cast<unsigned long long *>(workspace);
+        kp.partials = reinterpret_cast<float4 *>(static_cast<char *>(workspace) + sk_flag_bytes(pl.grid_ctas));
+    }
     kp.timeout_ns = timeout_ms * 1000000ull;
-    kp.launch_id = g_next_id.fetch_add(1, std::memory_order_relaxed);
+    kp.launch_id = next_launch_id();
     kp.status = d.status;
 
     if (launch_any(var, pl.grid_ctas, lay.smem, ta, tb, tc, kp, st) != cudaSuccess) {
@@ -462,13 +536,19 @@ gemm_status_t run(const void *A, const void *B, void *C, int64_t M, int64_t N, i
 
     const void *a_ptr = A, *b_ptr = B;
     int64_t lda = K, ldb = b_mn ? N : K;
-    void *a_tmp = nullptr, *b_tmp = nullptr;
+    void *a_tmp = nullptr, *b_tmp = nullptr, *ws = nullptr;
     auto release = [&]() {
         if (a_tmp)
             cudaFreeAsync(a_tmp, st);
         if (b_tmp)
             cudaFreeAsync(b_tmp, st);
+        if (ws)
+            cudaFreeAsync(ws, st);
     };
+    if (pl.ws_bytes && cudaMallocAsync(&ws, pl.ws_bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_OUT_OF_MEMORY;
+    }
     if (pl.realign_a && (rc = realign(A, M, K, eb, d->sms, st, &a_tmp, &lda)) != GEMM_OK) {
         release();
         return rc;
@@ -485,7 +565,8 @@ gemm_status_t run(const void *A, const void *B, void *C, int64_t M, int64_t N, i
 
     const uint64_t timeout_ms = opts && opts->timeout_ms ? static_cast<uint64_t>(opts->timeout_ms)
                                                          : DEFAULT_TIMEOUT_MS;
-    rc = encode_and_launch(*d, pl, a_ptr, lda, b_ptr, ldb, C, M, N, K, dtype_in, dtype_out, b_mn, timeout_ms, st);
+    rc = encode_and_launch(*d, pl, a_ptr, lda, b_ptr, ldb, C, M, N, K, dtype_in, dtype_out, b_mn, timeout_ms, ws,
+                           st);
     release();
     return rc;
 }
@@ -540,6 +621,8 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype
     plan->direct_store = pl.direct_store;
     plan->smem_bytes = static_cast<int32_t>(lay.smem);
     plan->num_sms = d->sms;
+    plan->sk_tiles = pl.sk_tiles;
+    plan->workspace_bytes = static_cast<int32_t>(pl.ws_bytes);
     return GEMM_OK;
 }
 
@@ -648,7 +731,7 @@ gemm_status_t gemm_selftest_wait_timeout(int32_t timeout_ms, void *stream)
     if (rc != GEMM_OK)
         return rc;
     wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<uint64_t>(timeout_ms) * 1000000ull, g_next_id.fetch_add(1), d->status);
+        static_cast<uint64_t>(timeout_ms) * 1000000ull, next_launch_id(), d->status);
     if (cudaGetLastError() != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
@@ -669,6 +752,22 @@ const char *gemm_status_string(int status)
 }
 
 uint64_t gemm_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+gemm_status_t gemm_schedule_jobs(int32_t num_tiles, int32_t units, int32_t k_blocks, int32_t sk_tiles,
+                                 int32_t unit, gemm_job_t *jobs, int32_t max_jobs, int32_t *n_jobs)
+{
+    if (num_tiles < 1 || units < 1 || unit < 0 || unit >= units || k_blocks < 1 || sk_tiles < 0 ||
+        sk_tiles > num_tiles || (!jobs && max_jobs > 0) || !n_jobs)
+        return GEMM_ERR_INVALID_ARG;
+    const UnitSchedule sch(unit, units, num_tiles, k_blocks, sk_tiles);
+    const int32_t n = sch.num_jobs();
+    for (int32_t i = 0; i < n && i < max_jobs; ++i) {
+        const Job j = sch.job(i);
+        jobs[i] = {j.tile, j.kb0, j.kb1, j.kind};
+    }
+    *n_jobs = n;
+    return GEMM_OK;
+}
 
 } // extern "C"
 
@@ -728,7 +827,8 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
     const bool b_mn = layoutB == GEMM_MN_MAJOR;
     const int eb = in_bytes(dtype_in);
 
-    // Scratch layout: padded A at offset 0, padded B at the next 256-byte boundary.
+    // Scratch layout: padded A at offset 0, padded B and then the stream-K
+    // workspace, each at the next 256-byte boundary.
     const int64_t b_rows = b_mn ? K : N, b_cols = b_mn ? N : K;
     const int64_t lda_pad = padded_pitch(K, eb), ldb_pad = padded_pitch(b_cols, eb);
     const uint64_t a_bytes = pl.realign_a ? static_cast<uint64_t>(M) * lda_pad * eb : 0;
@@ -736,14 +836,25 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
     const uint64_t b_bytes = pl.realign_b ? static_cast<uint64_t>(b_rows) * ldb_pad * eb : 0;
     if (b_off + b_bytes > GEMM_NO_ALLOC_SCRATCH_BYTES)
         return GEMM_ERR_UNSUPPORTED;   // padded operands exceed the fixed scratch array
+    const uint64_t ws_off = (b_off + b_bytes + 255) / 256 * 256;
+    if (pl.sk_tiles && ws_off + pl.ws_bytes > GEMM_NO_ALLOC_SCRATCH_BYTES) {
+        // no room for the partial sums: keep every tile whole
+        gemm_options_t dp = {};
+        dp.stream_k = 1;
+        if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, &dp, &pl)) != GEMM_OK)
+            return rc;
+    }
 
     const void *a_ptr = A, *b_ptr = B;
     int64_t lda = K, ldb = b_cols;
-    if (pl.realign_a || pl.realign_b) {
+    void *ws = nullptr;
+    if (pl.realign_a || pl.realign_b || pl.sk_tiles) {
         void *scratch = nullptr;
         if ((rc = no_alloc_scratch(&scratch)) != GEMM_OK)
             return rc;
         char *base = static_cast<char *>(scratch);
+        if (pl.sk_tiles)
+            ws = base + ws_off;
         if (pl.realign_a) {
             if ((rc = realign_into(A, M, K, lda_pad, eb, d->sms, st, base)) != GEMM_OK)
                 return rc;
@@ -758,7 +869,7 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
         }
     }
     return encode_and_launch(*d, pl, a_ptr, lda, b_ptr, ldb, C, M, N, K, dtype_in, dtype_out, b_mn,
-                             DEFAULT_TIMEOUT_MS, st);
+                             DEFAULT_TIMEOUT_MS, ws, st);
 }
 
 } // namespace

@@ -47,6 +47,7 @@
 #include <cuda_fp16.h>
 
 #include "ptx.cuh"
+#include "schedule.cuh"
 
 namespace dtg {
 
@@ -76,6 +77,7 @@ enum : uint32_t {
     SITE_MMA_DONE = 0x105,
     SITE_EPI_TMEM_FULL = 0x206,
     SITE_SELFTEST = 0x307,
+    SITE_EPI_PARTIAL = 0x209,  // an owner waiting for another unit's partial sum
     SITE_SMEM_ALIGN = 0x008,   // dynamic shared memory not 1024-byte aligned: nothing ran
 };
 
@@ -89,6 +91,9 @@ struct KernelParams {
     uint32_t stages;           // ring depth (2 .. MAX_STAGES)
     uint32_t staging_bytes;    // one epilogue staging buffer: 32 rows x 32 columns of C
     void *C;                   // used by the direct-store path
+    int32_t sk_tiles;          // trailing tiles scheduled stream-K (0: all tiles data-parallel)
+    float4 *partials;          // stream-K partial sums: one slot per CTA (128 rows x block_n FP32)
+    unsigned long long *flags; // stream-K: per (CTA, epilogue warp), the id of the launch that filled it
     uint64_t timeout_ns;       // per-wait limit
     unsigned long long launch_id;
     unsigned long long *status;  // [0] first timed-out launch, [1] site, [2] last timed-out launch
@@ -204,6 +209,39 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t 
             return;
         }
     }
+}
+
+// Wait until *flag == id (another CTA of this launch has published its
+// partial sum). Returns false after a timeout of this or another thread of
+// the launch, recording the site in the first case.
+__device__ __noinline__ bool wait_flag_slow(const unsigned long long *flag, uint64_t limit_ns,
+                                            unsigned long long id, unsigned long long *status, uint32_t site)
+{
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (ld_acquire_gpu(flag) == id)
+            return true;
+        if ((n & 15u) == 0) {
+            const volatile unsigned long long *st = status;
+            if (st[2] == id)
+                return false;
+            if (global_timer_ns() - t0 > limit_ns) {
+                record_timeout(status, id, site);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_flag_bounded(WaitCtx &w, const unsigned long long *flag, uint32_t site)
+{
+    if (w.aborted)
+        return false;
+    if (ld_acquire_gpu(flag) == w.id)
+        return true;
+    if (!wait_flag_slow(flag, w.limit_ns, w.id, w.status, site))
+        w.aborted = true;
+    return !w.aborted;
 }
 
 // ------------------------------------------------------------------ tile order
@@ -353,6 +391,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
     grid_launch_dependents();
 
     WaitCtx w{p.timeout_ns, p.launch_id, p.status, false};
+    // This unit's jobs: whole tiles and, with stream-K, at most one writer and
+    // one owner segment. Every role walks the same list.
+    const UnitSchedule sch(cluster_id, num_clusters, p.num_tiles, p.num_k_blocks, p.sk_tiles);
+    const int num_jobs = sch.num_jobs();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -360,12 +402,13 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
             prefetch_tensor_map(&tmap_a);
             prefetch_tensor_map(&tmap_b);
             uint32_t s = 0, ph = 0, pend_mask = 0, pend_par = 0;
-            for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+            for (int i = 0; i < num_jobs; ++i) {
+                const Job jb = sch.job(i);
                 int m_blk, n_blk;
-                tile_coords(p, t, m_blk, n_blk);
+                tile_coords(p, jb.tile, m_blk, n_blk);
                 const int a_row = m_blk * (BLOCK_M_CTA * CG) + static_cast<int>(rank) * BLOCK_M_CTA;
                 const int b_off = n_blk * BN + static_cast<int>(rank) * Cfg::BN_CTA;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = jb.kb0; kb < jb.kb1; ++kb) {
                     wait_bounded<CG == 2>(w, empty_bar(s), ph ^ 1u, SITE_PRODUCER_EMPTY);
                     if (!w.aborted) {
                         const uint32_t a_dst = base + s * Cfg::STAGE_BYTES;
@@ -430,11 +473,12 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const uint32_t b_lbo = b_mn ? 8192u : 16u;
             const uint32_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
             uint32_t s = 0, ph = 0, acc = 0, acc_ph = 0;
-            for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+            for (int i = 0; i < num_jobs; ++i) {
+                const Job jb = sch.job(i);
                 wait_bounded<CG == 2>(w, tempty_bar(acc), acc_ph ^ 1u, SITE_MMA_TMEM_EMPTY);
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = jb.kb0; kb < jb.kb1; ++kb) {
                     wait_bounded<CG == 2>(w, full_bar(s), ph, SITE_MMA_FULL);
                     tc_fence_after_sync();
                     if (!w.aborted) {
@@ -450,7 +494,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
 #pragma unroll
                             for (uint32_t k = 0; k < SLAB_MMAS; ++k)
                                 mma<CG, EB>(d_tmem, a_desc + 2u * k, b_desc + b_step * k, p.idesc,
-                                            (kb > 0 || j > 0 || k > 0) ? 1u : 0u);
+                                            (kb > jb.kb0 || j > 0 || k > 0) ? 1u : 0u);
                         }
                         if constexpr (CG == 1)
                             mma_commit(empty_bar(s));
@@ -485,11 +529,32 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
         const uint32_t quarter = warp & 3u;      // the TMEM lane quarter this warp may access
         const uint32_t staging = base + staging_off + (warp - EPI_WARP0) * 2u * p.staging_bytes;
         const uint64_t c_policy = l2_evict_first_policy();   // C is written once: keep A and B in L2
+        constexpr int CHUNKS = BN / EPI_COLS;
+        // Stream-K partial slot of CTA `cta`, this warp's 32 rows, chunk c: 32 lanes x 8 float4,
+        // laid out so that each float4 store or load of the warp covers 512 contiguous bytes.
+        auto partial_chunk = [&](int cta, int c) {
+            return p.partials + ((static_cast<size_t>(cta) * 4u + quarter) * CHUNKS + c) * 256u + lane;
+        };
         uint32_t acc = 0, acc_ph = 0, sb = 0;
-        for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
+        for (int i = 0; i < num_jobs; ++i) {
+            const Job jb = sch.job(i);
             int m_blk, n_blk;
-            tile_coords(p, t, m_blk, n_blk);
+            tile_coords(p, jb.tile, m_blk, n_blk);
             wait_bounded<CG == 2>(w, tfull_bar(acc), acc_ph, SITE_EPI_TMEM_FULL);
+            // An owner needs every writer's partial for its rows first. The
+            // writers did their segments at the start of their work lists.
+            int w_first = cluster_id;
+            if (jb.kind == JOB_OWNER && !w.aborted) {
+                w_first = sch.first_writer();
+                if (lane == 0)
+                    for (int v = cluster_id - 1; v >= w_first; --v)
+                        if (sch.has_range(v) &&
+                            !wait_flag_bounded(w, &p.flags[(static_cast<size_t>(v) * CG + rank) * 4u + quarter],
+                                               SITE_EPI_PARTIAL))
+                            break;
+                w.aborted = __shfl_sync(0xffffffffu, w.aborted ? 1 : 0, 0) != 0;
+                __syncwarp();   // lane 0's acquire loads come before every lane's partial reads
+            }
             const bool skip = __any_sync(0xffffffffu, w.aborted);   // warp-uniform
             w.aborted = skip;
             tc_fence_after_sync();
@@ -498,13 +563,13 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const int col0 = n_blk * BN;
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + acc * ACC_STRIDE;
 #pragma unroll 1
-            for (int c = 0; c < BN / EPI_COLS; ++c) {
+            for (int c = 0; c < CHUNKS; ++c) {
                 uint32_t v[32];
                 if (!skip) {
                     tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * EPI_COLS), v);
                     tmem_ld_wait();
                 }
-                if (c == BN / EPI_COLS - 1) {
+                if (c == CHUNKS - 1) {
                     // accumulator fully read: hand it back to the MMA issuer
                     tc_fence_before_sync();
                     __syncwarp();
@@ -518,6 +583,31 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const int gcol = col0 + c * EPI_COLS;
                 if (skip || gcol >= p.N)
                     continue;
+                if (jb.kind == JOB_WRITER) {
+                    float4 *dst = partial_chunk(static_cast<int>(blockIdx.x), c);
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4)
+                        __stcg(dst + 32 * j4, make_float4(__uint_as_float(v[4 * j4]), __uint_as_float(v[4 * j4 + 1]),
+                                                          __uint_as_float(v[4 * j4 + 2]),
+                                                          __uint_as_float(v[4 * j4 + 3])));
+                    continue;
+                }
+                if (jb.kind == JOB_OWNER) {
+                    // add the writers' partial sums, nearest k-range first
+                    for (int u = cluster_id - 1; u >= w_first; --u) {
+                        if (!sch.has_range(u))
+                            continue;
+                        const float4 *src = partial_chunk(u * CG + static_cast<int>(rank), c);
+#pragma unroll
+                        for (int j4 = 0; j4 < 8; ++j4) {
+                            const float4 x = __ldcg(src + 32 * j4);
+                            v[4 * j4] = __float_as_uint(__uint_as_float(v[4 * j4]) + x.x);
+                            v[4 * j4 + 1] = __float_as_uint(__uint_as_float(v[4 * j4 + 1]) + x.y);
+                            v[4 * j4 + 2] = __float_as_uint(__uint_as_float(v[4 * j4 + 2]) + x.z);
+                            v[4 * j4 + 3] = __float_as_uint(__uint_as_float(v[4 * j4 + 3]) + x.w);
+                        }
+                    }
+                }
                 if (p.direct_store) {
                     store_row_direct(p, row0 + static_cast<int>(lane), gcol, v);
                     continue;
@@ -534,6 +624,14 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     bulk_commit_group();
                 }
                 sb ^= 1u;
+            }
+            if (jb.kind == JOB_WRITER && !skip) {
+                // publish: every lane's partial stores, then the flag
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    st_release_gpu(&p.flags[static_cast<size_t>(blockIdx.x) * 4u + quarter], p.launch_id);
+                }
             }
             if (++acc == 2) {
                 acc = 0;

@@ -80,6 +80,17 @@ typedef enum {
  *             (GEMM_MN_MAJOR gives GEMM_ERR_UNSUPPORTED).
  *   stream    cudaStream_t as void*.
  *
+ * Tail scheduling: the grid is persistent, one unit (CTA or CTA pair) per
+ * resident slot. When the tile count leaves the last wave part-empty, the
+ * planner may split the last tiles along K (stream-K): each unit then gets an
+ * equal share of their k-blocks, and the units that end a split tile add the
+ * FP32 partial sums of the others before the cast. The partial sums and their
+ * flags live in a per-call workspace (plan->workspace_bytes) taken with
+ * cudaMallocAsync and freed with cudaFreeAsync on the same stream. For a
+ * given device and problem the split points are fixed, so results are
+ * reproducible from run to run. The split tiles are run first, so that the
+ * whole tiles after them proceed in step across the machine.
+ *
  * Alignment: the tensor-memory-access engine needs 16-byte-aligned bases and
  * row pitches. When A or B misses this (for example K*2 bytes, or K bytes for
  * FP8, not a multiple of 16), the call first copies that operand into a padded, stream-ordered
@@ -114,6 +125,11 @@ gemm_status_t gemm(const void *A, const void *B, void *C,
  *   k_stage       K depth of one shared-memory ring stage, in elements: one or
  *                 two 128-byte slabs, so 64 or 128 for FP16/BF16 and 128 or
  *                 256 for FP8. Other values give GEMM_ERR_UNSUPPORTED.
+ *   stream_k      tail scheduling: 0 lets the planner choose, 1 keeps every
+ *                 tile whole (data-parallel), 2 forces stream-K on the last
+ *                 tiles (see gemm_schedule_jobs). Other values give
+ *                 GEMM_ERR_INVALID_ARG (negative) or GEMM_ERR_UNSUPPORTED.
+ *   reserved      must be 0.
  */
 typedef struct {
     int32_t cta_group;
@@ -122,7 +138,8 @@ typedef struct {
     int32_t group_m;
     int32_t timeout_ms;
     int32_t k_stage;
-    int32_t reserved[2];
+    int32_t stream_k;
+    int32_t reserved;
 } gemm_options_t;
 
 /* gemm with overrides. opts may be NULL. An unsupported override combination
@@ -150,7 +167,9 @@ typedef struct {
     int32_t direct_store;  /* 1 if C is written with ordinary stores */
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t num_sms;       /* multiprocessors on the current device */
-    int32_t reserved[3];
+    int32_t sk_tiles;      /* trailing tiles split along K (stream-K); 0 = none */
+    int32_t workspace_bytes; /* stream-K partial sums and flags, taken per call */
+    int32_t reserved;
 } gemm_plan_t;
 
 /* Fill *plan for a problem on the current device. Same validation and
@@ -216,8 +235,11 @@ gemm_status_t gemm_selftest_wait_timeout(int32_t timeout_ms, void *stream);
  *     each started on a 256-byte boundary) must fit in
  *     GEMM_NO_ALLOC_SCRATCH_BYTES. Otherwise the call returns
  *     GEMM_ERR_UNSUPPORTED and launches nothing. When no operand needs
- *     re-pitching the array is not used, and there is no size limit beyond
- *     gemm's.
+ *     re-pitching the array is not used for them, and there is no size limit
+ *     beyond gemm's.
+ *   - Stream-K: when the plan splits tiles along K, the partial sums and
+ *     flags go into the same array after the copies. When they do not fit,
+ *     the call keeps every tile whole instead (same result bound).
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current. Make this first call
  *     before any stream capture.
@@ -234,6 +256,38 @@ gemm_status_t gemm_no_alloc(const void *A, const void *B, void *C,
                             int64_t M, int64_t N, int64_t K,
                             int dtype_in, int dtype_out, int layoutA, int layoutB,
                             void *stream);
+
+/*
+ * gemm_schedule_jobs: the work list that unit `unit` of a launch walks, as
+ * computed by the kernel itself (no GPU needed). Tiles [0, sk_tiles) (the
+ * first in the swizzled raster order) are laid end to end in k-blocks
+ * (k_blocks per tile) and cut into `units` equal ranges, one per unit; tiles
+ * [sk_tiles, num_tiles) are whole and dealt round-robin to the units. Each
+ * job covers k-blocks [kb_begin, kb_end) of one tile and is
+ *   GEMM_JOB_FULL   the whole K range: the unit stores C for the tile;
+ *   GEMM_JOB_WRITER a leading or middle part: the unit leaves an FP32 partial;
+ *   GEMM_JOB_OWNER  the trailing part: the unit adds the writers' partials
+ *                   (units unit-1, unit-2, ... that share the tile) and stores C.
+ * Jobs are listed in the order the unit runs them: the writer job, the whole
+ * stream-K tiles, the owner job, then the whole round-robin tiles. Writes at most max_jobs
+ * entries to `jobs` and the full count to *n_jobs. Returns
+ * GEMM_ERR_INVALID_ARG for inconsistent sizes (num_tiles < 1, units < 1,
+ * unit outside [0, units), k_blocks < 1, sk_tiles outside [0, num_tiles],
+ * jobs NULL with max_jobs > 0, or n_jobs NULL). The planner always makes
+ * num_tiles - sk_tiles a multiple of units, so that every unit gets the same
+ * number of whole tiles.
+ */
+typedef enum { GEMM_JOB_FULL = 0, GEMM_JOB_WRITER = 1, GEMM_JOB_OWNER = 2 } gemm_job_kind_t;
+
+typedef struct {
+    int32_t tile;
+    int32_t kb_begin;
+    int32_t kb_end;
+    int32_t kind;
+} gemm_job_t;
+
+gemm_status_t gemm_schedule_jobs(int32_t num_tiles, int32_t units, int32_t k_blocks, int32_t sk_tiles,
+                                 int32_t unit, gemm_job_t *jobs, int32_t max_jobs, int32_t *n_jobs);
 
 /* Human-readable name of a status code. Never NULL. */
 const char *gemm_status_string(int status);

@@ -82,7 +82,8 @@ def test_invalid_arguments_rejected_on_host(kwargs, expect):
 def test_invalid_options_rejected_on_host():
     for field, val, expect in (("cta_group", 3, 1), ("cta_group", -1, 1), ("block_n", 128, 2),
                                ("max_clusters", -2, 1), ("group_m", -1, 1), ("timeout_ms", -1, 1),
-                               ("k_stage", 96, 2), ("k_stage", -64, 1)):
+                               ("k_stage", 96, 2), ("k_stage", -64, 1), ("stream_k", 3, 2),
+                               ("stream_k", -1, 1), ("reserved", 1, 1)):
         o = binding.GemmOptions()
         setattr(o, field, val)
         rc = binding.lib.gemm_ex(FAKE, FAKE, FAKE, 64, 64, 64, 0, 0, 0, 0, ctypes.byref(o), None)

@@ -71,3 +71,32 @@ def test_no_alloc_rejects_operands_beyond_its_array(lib):
     assert _call(lib.gemm_no_alloc, A, B, C, M, N, K, "bf16", "f32", "k") == 2   # UNSUPPORTED
     torch.cuda.synchronize()
     assert torch.count_nonzero(C).item() == 0
+
+
+def test_no_alloc_stream_k_workspace(lib):
+    """Stream-K partial sums go into the fixed array after the re-pitched copies.
+    3000 x 5000 x 2050 (A re-pitched, 12.3 MB; partials ~20 MB) fits: same plan and
+    the same bits as gemm. 6000 x 5000 x 2050 (A re-pitched, 24.7 MB) leaves no room
+    for the partials: the call keeps every tile whole and stays within the bound."""
+    import ctypes
+    import dense_tiled_gemm_gb300 as dtg
+    for M, fits in ((3000, True), (6000, False)):
+        N, K = 5000, 2050
+        assert dtg.gemm_plan(M, N, K, dtype_in=torch.bfloat16, dtype_out=torch.float32,
+                             layout_b="mn")["sk_tiles"] > 0
+        A, B = workloads.make_operands(M, N, K, "bf16", "mn", ("uniform", -2.0, 2.0), 40 + M)
+        Ad, Bd = A.cuda(), B.cuda()
+        C_gemm = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        C_new = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        assert _call(lib.gemm, Ad, Bd, C_gemm, M, N, K, "bf16", "f32", "mn") == 0
+        assert _call(lib.gemm_no_alloc, Ad, Bd, C_new, M, N, K, "bf16", "f32", "mn") == 0
+        torch.cuda.synchronize()
+        detail = ctypes.c_uint32(0)
+        assert lib.gemm_last_device_status(None, ctypes.byref(detail)) == 0
+        if fits:
+            assert torch.equal(C_new, C_gemm)
+        else:
+            C_abs = (A.double().abs() @ B.double().abs()).numpy()
+            ok, ratio, n_bad, first = tolerance.check(C_new.double().cpu().numpy(),
+                                                      C_gemm.double().cpu().numpy(), C_abs, "f32")
+            assert ok, f"{n_bad} elements differ beyond the bound, first {first}"
