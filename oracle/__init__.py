@@ -12,6 +12,10 @@ FP16/BF16 or FP8 (E4M3/E5M2) operand values (k ascending), plus
 C_abs[i][j] = sum_k |a·b|. FP8 operands carry the identity block scale
 (1.0) of "Porting High-Performance HIP Kernels to FlyDSL", section "A More
 Complex Kernel", so their products are the plain products.
+``gemm_ref_mx`` is the block-scaled (MX) form measured in "Two Waves, One Stage
+Apart" (section "MI450", Table 1): E4M3/E5M2 or packed E2M1 elements, each
+run of 32 consecutive K elements of a row of A (and of a column of B) scaled
+by one E8M0 value 2^(e-127).
 It follows "Two Waves, One Stage Apart" (opening paragraph: a tiled GEMM
 sums operand-tile products) and counts 2·M·N·K flops as in that page's
 Table 1 caption.
@@ -31,11 +35,13 @@ _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F16, BF16, E4M3, E5M2 = 0, 1, 3, 4
+F16, BF16, E4M3, E5M2, E2M1 = 0, 1, 3, 4, 5
+MX_BLOCK = 32
 K_MAJOR, MN_MAJOR = 0, 1
-_DTYPE = {"f16": F16, "bf16": BF16, "e4m3": E4M3, "e5m2": E5M2}
+_DTYPE = {"f16": F16, "bf16": BF16, "e4m3": E4M3, "e5m2": E5M2, "e2m1": E2M1}
 # numpy type of the raw operand patterns for each input type
-_STORAGE = {"f16": np.uint16, "bf16": np.uint16, "e4m3": np.uint8, "e5m2": np.uint8}
+_STORAGE = {"f16": np.uint16, "bf16": np.uint16, "e4m3": np.uint8, "e5m2": np.uint8,
+            "e2m1": np.uint8, "e8m0": np.uint8}
 _LAYOUT = {"k": K_MAJOR, "mn": MN_MAJOR}
 
 
@@ -64,9 +70,13 @@ def load_library(path: str):
     lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
     lib.oracle_decode_bf16.restype = ctypes.c_double
     lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
-    for name in ("oracle_decode_e4m3", "oracle_decode_e5m2"):
+    for name in ("oracle_decode_e4m3", "oracle_decode_e5m2", "oracle_decode_e2m1",
+                 "oracle_decode_e8m0"):
         getattr(lib, name).restype = ctypes.c_double
         getattr(lib, name).argtypes = [ctypes.c_uint8]
+    lib.oracle_gemm_mx.restype = ctypes.c_int
+    lib.oracle_gemm_mx.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, ctypes.c_int,
+                                   ctypes.c_void_p, i64, dp, dp, ctypes.c_int]
     return lib
 
 
@@ -86,8 +96,8 @@ def host_threads() -> int:
 
 
 def decode(bits, dtype: str, lib=None) -> np.ndarray:
-    """Decode FP16/BF16 (16-bit) or E4M3/E5M2 (8-bit) patterns to FP64 with
-    the oracle's own decoders."""
+    """Decode FP16/BF16 (16-bit), E4M3/E5M2/E8M0 (8-bit) or E2M1 (4-bit, one
+    pattern per array entry) patterns to FP64 with the oracle's own decoders."""
     lib = lib or _load()
     fn = getattr(lib, f"oracle_decode_{dtype}")
     flat = np.asarray(bits, dtype=_STORAGE[dtype]).ravel()
@@ -127,4 +137,48 @@ def gemm_ref(A_bits: np.ndarray, B_bits: np.ndarray, M: int, N: int, K: int,
                          int(threads or host_threads()))
     if rc != 0:
         raise RuntimeError(f"oracle_gemm failed with code {rc}")
+    return C, C_abs
+
+
+def mx_blocks(K: int) -> int:
+    """E8M0 scales per row: one per 32 consecutive K elements."""
+    return (K + MX_BLOCK - 1) // MX_BLOCK
+
+
+def gemm_ref_mx(A_bits: np.ndarray, B_bits: np.ndarray, SFA: np.ndarray, SFB: np.ndarray,
+                M: int, N: int, K: int, dtype_in: str, rows=None, threads: int | None = None,
+                lib=None):
+    """FP64 reference rows of the block-scaled C = (SFA o A)(SFB o B) and its C_abs.
+
+    A_bits: M x K bytes ("e4m3"/"e5m2") or M x ceil(K/2) bytes of packed E2M1
+    ("e2m1", lower k in the low nibble). B_bits: N x K (K-major), same element
+    layout. SFA: M x ceil(K/32), SFB: N x ceil(K/32) E8M0 bytes.
+    """
+    lib = lib or _load()
+    width = (K + 1) // 2 if dtype_in == "e2m1" else K
+    A = np.ascontiguousarray(A_bits, dtype=np.uint8)
+    B = np.ascontiguousarray(B_bits, dtype=np.uint8)
+    sa = np.ascontiguousarray(SFA, dtype=np.uint8)
+    sb = np.ascontiguousarray(SFB, dtype=np.uint8)
+    nb = mx_blocks(K)
+    if A.size != M * width or B.size != N * width or sa.size != M * nb or sb.size != N * nb:
+        raise ValueError("operand or scale sizes do not match M, N, K")
+    if rows is None:
+        n_rows, rows_ptr = M, None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n_rows = int(rows_arr.size)
+        rows_ptr = rows_arr.ctypes.data_as(ctypes.c_void_p)
+    C = np.empty((n_rows, N), dtype=np.float64)
+    C_abs = np.empty((n_rows, N), dtype=np.float64)
+    if n_rows == 0:
+        return C, C_abs
+    dp = ctypes.POINTER(ctypes.c_double)
+    vp = ctypes.c_void_p
+    rc = lib.oracle_gemm_mx(A.ctypes.data_as(vp), B.ctypes.data_as(vp), sa.ctypes.data_as(vp),
+                            sb.ctypes.data_as(vp), M, N, K, _DTYPE[dtype_in], rows_ptr, n_rows,
+                            C.ctypes.data_as(dp), C_abs.ctypes.data_as(dp),
+                            int(threads or host_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_mx failed with code {rc}")
     return C, C_abs

@@ -23,6 +23,17 @@
  * sum. No blocking or reordering: one plain i-k-j loop per output row, with
  * rows shared among threads.
  *
+ * Block-scaled (MX) inputs: "Two Waves, One Stage Apart" (section "MI450",
+ * Table 1) measures MXFP8 and MXFP4 GEMMs without defining the formats; the
+ * reading taken is OCP Microscaling: elements E4M3/E5M2 (MXFP8) or E2M1
+ * (MXFP4), and one E8M0 scale 2^(e-127) shared by each run of 32 consecutive
+ * K elements of a row of A, and of a column of B. oracle_gemm_mx computes
+ *
+ *     C[i][j] = sum_k (sa[i][k/32] * a[i][k]) * (sb[j][k/32] * b[k][j])
+ *
+ * with each scaled operand formed exactly in FP64 before the product (the
+ * scaled values are powers of two times short significands).
+ *
  * FP8 inputs follow "Porting High-Performance HIP Kernels to FlyDSL"
  * (section "A More Complex Kernel"): E4M3 operands, FP32 accumulation and a
  * block scale of 1.0 on every operand (the identity scale), so the scaled
@@ -47,7 +58,8 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 3, ORACLE_E5M2 = 4 };
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 3, ORACLE_E5M2 = 4, ORACLE_E2M1 = 5 };
+enum { ORACLE_MX_BLOCK = 32 };
 enum { ORACLE_K_MAJOR = 0, ORACLE_MN_MAJOR = 1 };
 
 /* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
@@ -126,15 +138,40 @@ double oracle_decode_e5m2(uint8_t h)
     return sign ? -v : v;
 }
 
+/* FP4 E2M1 (OCP): 1 sign bit, 2 exponent bits (bias 1), 1 fraction bit, no
+ * infinities or NaNs; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+ * Normal:    (2 + f) * 2^(e - 1 - 1)
+ * Subnormal: f * 2^(1 - 1 - 1) = f * 0.5                                    */
+double oracle_decode_e2m1(uint8_t h)
+{
+    int sign = (h >> 3) & 1;
+    int e = (h >> 1) & 0x3;
+    int f = h & 0x1;
+    double v = e == 0 ? ldexp((double)f, -1) : ldexp((double)(2 + f), e - 2);
+    return sign ? -v : v;
+}
+
+/* E8M0 scale (OCP): an 8-bit biased exponent, value 2^(e - 127); 0xFF is NaN. */
+double oracle_decode_e8m0(uint8_t e)
+{
+    return e == 0xFF ? NAN : ldexp(1.0, (int)e - 127);
+}
+
 static int is_fp8(int dtype)
 {
     return dtype == ORACLE_E4M3 || dtype == ORACLE_E5M2;
 }
 
-/* element idx of an operand array holding dtype's patterns */
+/* element idx of an operand array holding dtype's patterns. E2M1 elements
+ * are packed two per byte, the lower index in the low nibble; `idx` then
+ * counts nibbles. */
 static double decode(const void *base, int64_t idx, int dtype)
 {
     switch (dtype) {
+    case ORACLE_E2M1: {
+        const uint8_t byte = ((const uint8_t *)base)[idx >> 1];
+        return oracle_decode_e2m1((idx & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF));
+    }
     case ORACLE_BF16: return oracle_decode_bf16(((const uint16_t *)base)[idx]);
     case ORACLE_E4M3: return oracle_decode_e4m3(((const uint8_t *)base)[idx]);
     case ORACLE_E5M2: return oracle_decode_e5m2(((const uint8_t *)base)[idx]);
@@ -147,6 +184,9 @@ typedef struct {
     const void *A;
     const double *Bd;      /* decoded b[k][j], K x N row-major */
     const void *B;         /* raw B, for the decode phase */
+    const uint8_t *sfa, *sfb;  /* MX scales (E8M0), rows x n_blocks; NULL: unscaled */
+    int64_t n_blocks;      /* scale blocks per row = ceil(K / 32) */
+    int64_t row_elems;     /* element slots per stored row (K, or K rounded up to even for E2M1) */
     int64_t M, N, K;
     int dtype, layout_b;
     const int64_t *rows;
@@ -162,8 +202,11 @@ static void decode_b_rows(const job_t *j)
     double *Bd = (double *)j->Bd;
     for (int64_t k = j->lo; k < j->hi; ++k)
         for (int64_t c = 0; c < j->N; ++c) {
-            int64_t idx = j->layout_b == ORACLE_K_MAJOR ? c * j->K + k : k * j->N + c;
-            Bd[k * j->N + c] = decode(j->B, idx, j->dtype);
+            int64_t idx = j->layout_b == ORACLE_K_MAJOR ? c * j->row_elems + k : k * j->N + c;
+            double v = decode(j->B, idx, j->dtype);
+            if (j->sfb)
+                v *= oracle_decode_e8m0(j->sfb[c * j->n_blocks + k / ORACLE_MX_BLOCK]);
+            Bd[k * j->N + c] = v;
         }
 }
 
@@ -179,7 +222,9 @@ static void gemm_rows(const job_t *j)
             cabs[col] = 0.0;
         }
         for (int64_t k = 0; k < K; ++k) {
-            const double a = decode(j->A, i * K + k, j->dtype);
+            double a = decode(j->A, i * j->row_elems + k, j->dtype);
+            if (j->sfa)
+                a *= oracle_decode_e8m0(j->sfa[i * j->n_blocks + k / ORACLE_MX_BLOCK]);
             const double *b = j->Bd + k * N;
             for (int64_t col = 0; col < N; ++col) {
                 const double p = a * b[col];
@@ -235,6 +280,54 @@ static int run_threads(job_t *base, int64_t count, int n_threads)
     return 0;
 }
 
+static int run_gemm(const void *A, const void *B, const uint8_t *sfa, const uint8_t *sfb, int64_t M,
+                    int64_t N, int64_t K, int dtype, int layout_b, const int64_t *rows, int64_t n_rows,
+                    double *C, double *C_abs, int n_threads)
+{
+    if (rows) {
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (rows[r] < 0 || rows[r] >= M)
+                return -1;
+    } else {
+        n_rows = M;
+    }
+    if (n_threads <= 0) {
+        long n = sysconf(_SC_NPROCESSORS_ONLN);
+        n_threads = n > 0 ? (int)n : 1;
+    }
+    double *Bd = (double *)malloc((size_t)K * (size_t)N * sizeof(double));
+    if (!Bd)
+        return -2;
+    job_t base;
+    memset(&base, 0, sizeof(base));
+    base.A = A;
+    base.B = B;
+    base.Bd = Bd;
+    base.sfa = sfa;
+    base.sfb = sfb;
+    base.n_blocks = (K + ORACLE_MX_BLOCK - 1) / ORACLE_MX_BLOCK;
+    base.row_elems = dtype == ORACLE_E2M1 ? (K + 1) / 2 * 2 : K;
+    base.M = M;
+    base.N = N;
+    base.K = K;
+    base.dtype = dtype;
+    base.layout_b = layout_b;
+    base.rows = rows;
+    base.n_rows = n_rows;
+    base.C = C;
+    base.C_abs = C_abs;
+
+    /* phase 0 decodes (and scales) b[k][j] into FP64 once; phase 1 runs the row loops */
+    base.phase = 0;
+    int rc = run_threads(&base, K, n_threads);
+    if (rc == 0) {
+        base.phase = 1;
+        rc = run_threads(&base, n_rows, n_threads);
+    }
+    free(Bd);
+    return rc;
+}
+
 /*
  * Compute selected rows of C = A·B in FP64.
  *   A, B      : raw operand patterns (16-bit words for ORACLE_F16 and
@@ -258,42 +351,26 @@ int oracle_gemm(const void *A, const void *B, int64_t M, int64_t N, int64_t K,
         return -1;
     if (layout_b != ORACLE_K_MAJOR && layout_b != ORACLE_MN_MAJOR)
         return -1;
-    if (rows) {
-        for (int64_t r = 0; r < n_rows; ++r)
-            if (rows[r] < 0 || rows[r] >= M)
-                return -1;
-    } else {
-        n_rows = M;
-    }
-    if (n_threads <= 0) {
-        long n = sysconf(_SC_NPROCESSORS_ONLN);
-        n_threads = n > 0 ? (int)n : 1;
-    }
-    double *Bd = (double *)malloc((size_t)K * (size_t)N * sizeof(double));
-    if (!Bd)
-        return -2;
-    job_t base;
-    memset(&base, 0, sizeof(base));
-    base.A = A;
-    base.B = B;
-    base.Bd = Bd;
-    base.M = M;
-    base.N = N;
-    base.K = K;
-    base.dtype = dtype;
-    base.layout_b = layout_b;
-    base.rows = rows;
-    base.n_rows = n_rows;
-    base.C = C;
-    base.C_abs = C_abs;
+    return run_gemm(A, B, NULL, NULL, M, N, K, dtype, layout_b, rows, n_rows, C, C_abs, n_threads);
+}
 
-    /* phase 0 decodes b[k][j] into FP64 once; phase 1 runs the row loops */
-    base.phase = 0;
-    int rc = run_threads(&base, K, n_threads);
-    if (rc == 0) {
-        base.phase = 1;
-        rc = run_threads(&base, n_rows, n_threads);
-    }
-    free(Bd);
-    return rc;
+/*
+ * Block-scaled (MX) GEMM rows in FP64: C = (SFA ∘ A)·(SFB ∘ B), see the top
+ * of this file.
+ *   A         : M x K elements, row-major; bytes for ORACLE_E4M3/ORACLE_E5M2,
+ *               or E2M1 nibbles packed two per byte with each row padded to a
+ *               whole byte (row pitch ceil(K/2) bytes), lower k in the low nibble
+ *   B         : N x K (K-major, the same element layout as A)
+ *   sfa, sfb  : E8M0 scales, M x ceil(K/32) and N x ceil(K/32) bytes, row-major
+ *   other arguments as for oracle_gemm (B must be K-major)
+ */
+int oracle_gemm_mx(const void *A, const void *B, const uint8_t *sfa, const uint8_t *sfb, int64_t M,
+                   int64_t N, int64_t K, int dtype, const int64_t *rows, int64_t n_rows, double *C,
+                   double *C_abs, int n_threads)
+{
+    if (!A || !B || !sfa || !sfb || !C || !C_abs || M <= 0 || N <= 0 || K <= 0)
+        return -1;
+    if (!is_fp8(dtype) && dtype != ORACLE_E2M1)
+        return -1;
+    return run_gemm(A, B, sfa, sfb, M, N, K, dtype, ORACLE_K_MAJOR, rows, n_rows, C, C_abs, n_threads);
 }

@@ -14,6 +14,7 @@ from __future__ import annotations
 import math
 import os
 import subprocess
+import sys
 import tempfile
 from fractions import Fraction
 
@@ -307,8 +308,149 @@ def _pin_row_subset(lib):
     return out
 
 
+# ---------------------------------------------------------------- block-scaled (MX) pins
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]   # magnitudes of codes 0..7 (OCP E2M1)
+MX_TYPES = ("e4m3", "e5m2", "e2m1")
+
+
+def e2m1_value(code: int) -> float:
+    v = E2M1_TABLE[code & 7]
+    return -v if code & 8 else v
+
+
+def pack_e2m1(codes: np.ndarray) -> np.ndarray:
+    """Rows of 4-bit codes -> bytes, two per byte, lower k in the low nibble (odd K padded)."""
+    rows, K = codes.shape
+    padded = np.zeros((rows, K + (K & 1)), dtype=np.uint8)
+    padded[:, :K] = codes
+    return (padded[:, 0::2] | (padded[:, 1::2] << 4)).astype(np.uint8)
+
+
+def random_mx_elements(rng, rows, K, dtype):
+    """(storage array, exact values) for random finite elements of an MX type."""
+    if dtype == "e2m1":
+        codes = rng.integers(0, 16, (rows, K)).astype(np.uint8)
+        return pack_e2m1(codes), np.vectorize(e2m1_value)(codes)
+    bits = random_finite_bits(rng, rows * K, dtype).reshape(rows, K)
+    return bits, np.vectorize(lambda b: exact_value(int(b), dtype))(bits)
+
+
+def _pin_mx_fixtures(lib):
+    out = []
+    for name, dtype in (("e2m1_values.txt", "e2m1"), ("e8m0_values.txt", "e8m0")):
+        for bits, val in _parse_format_fixture(name):
+            got = float(oracle.decode(np.array([bits]), dtype, lib=lib)[0])
+            if not (got == val or (math.isnan(got) and math.isnan(val))):
+                out.append(f"fixture_{dtype}_{bits:#04x}")
+    e8 = oracle.decode(np.arange(255), "e8m0", lib=lib)
+    if not all(e8[e] == math.ldexp(1.0, e - 127) for e in range(255)):
+        out.append("decoder_e8m0")
+    e2 = oracle.decode(np.arange(16), "e2m1", lib=lib)
+    if not all(e2[c] == e2m1_value(c) for c in range(16)):
+        out.append("decoder_e2m1")
+    return out
+
+
+def _pin_mx_brute_force(lib):
+    """Random elements and scales on tiny shapes, K across block edges and odd
+    (E2M1 rows padded), against exact Fraction sums of the scaled products."""
+    out = []
+    rng = np.random.default_rng(77)
+    for (M, N, K) in ((1, 1, 1), (2, 3, 33), (3, 2, 64), (4, 5, 65), (2, 2, 97)):
+        nb = oracle.mx_blocks(K)
+        for dtype in MX_TYPES:
+            Ast, Av = random_mx_elements(rng, M, K, dtype)
+            Bst, Bv = random_mx_elements(rng, N, K, dtype)
+            sfa = rng.integers(110, 145, (M, nb)).astype(np.uint8)
+            sfb = rng.integers(110, 145, (N, nb)).astype(np.uint8)
+            got, gabs = oracle.gemm_ref_mx(Ast, Bst, sfa, sfb, M, N, K, dtype, lib=lib)
+            for i in range(M):
+                for j in range(N):
+                    terms = [Fraction(Av[i, k]) * Fraction(2) ** (int(sfa[i, k // 32]) - 127)
+                             * Fraction(Bv[j, k]) * Fraction(2) ** (int(sfb[j, k // 32]) - 127)
+                             for k in range(K)]
+                    ex, ea = sum(terms), sum(abs(t) for t in terms)
+                    lim = Fraction(gamma(K) * float(ea))
+                    if abs(Fraction(got[i, j]) - ex) > lim or abs(Fraction(gabs[i, j]) - ea) > lim:
+                        out.append(f"mx_brute_{M}x{N}x{K}_{dtype}")
+                        break
+                else:
+                    continue
+                break
+    return out
+
+
+def _pin_mx_unit_scales(lib):
+    """Scales of 1.0 (E8M0 127) reduce the MX GEMM to the plain FP8 GEMM, bit for bit."""
+    out = []
+    rng = np.random.default_rng(78)
+    M, N, K = 9, 7, 100
+    for dtype in ("e4m3", "e5m2"):
+        A = random_finite_bits(rng, M * K, dtype).reshape(M, K)
+        B = random_finite_bits(rng, N * K, dtype).reshape(N, K)
+        ones_a = np.full((M, oracle.mx_blocks(K)), 127, np.uint8)
+        ones_b = np.full((N, oracle.mx_blocks(K)), 127, np.uint8)
+        mx, mxa = oracle.gemm_ref_mx(A, B, ones_a, ones_b, M, N, K, dtype, lib=lib)
+        plain, pa = oracle.gemm_ref(A, B, M, N, K, dtype, "k", lib=lib)
+        if not (np.array_equal(mx, plain) and np.array_equal(mxa, pa)):
+            out.append(f"mx_unit_scales_{dtype}")
+    return out
+
+
+def _pin_mx_block_scaling(lib):
+    """Closed form: raising one row's scale for one 32-block by 2^t adds
+    (2^t - 1) times that block's partial sum, and a column scale scales the
+    whole column; with small integers every sum is exact."""
+    out = []
+    rng = np.random.default_rng(79)
+    M, N, K = 4, 6, 96
+    for dtype in MX_TYPES:
+        ints = rng.integers(-3, 4, (M, K)).astype(np.float64)
+        intb = rng.integers(-3, 4, (N, K)).astype(np.float64)
+        if dtype == "e2m1":
+            enc = {0: 0, 1: 2, 2: 4, 3: 5, -1: 10, -2: 12, -3: 13}
+            Ast = pack_e2m1(np.vectorize(enc.get)(ints.astype(int)).astype(np.uint8))
+            Bst = pack_e2m1(np.vectorize(enc.get)(intb.astype(int)).astype(np.uint8))
+        else:
+            Ast, Bst = bits_of(ints, dtype), bits_of(intb, dtype)
+        nb = oracle.mx_blocks(K)
+        sfa = np.full((M, nb), 127, np.uint8)
+        sfb = np.full((N, nb), 127, np.uint8)
+        base, _ = oracle.gemm_ref_mx(Ast, Bst, sfa, sfb, M, N, K, dtype, lib=lib)
+        sfa2 = sfa.copy()
+        sfa2[2, 1] = 127 + 3                       # row 2, k in [32, 64): x 8
+        sfb2 = sfb.copy()
+        sfb2[4, :] = 127 - 2                       # column 4: x 1/4
+        got, _ = oracle.gemm_ref_mx(Ast, Bst, sfa2, sfb2, M, N, K, dtype, lib=lib)
+        expect = base.copy()
+        expect[2, :] += 7 * (ints[2, 32:64] @ intb[:, 32:64].T)
+        expect[:, 4] *= 0.25
+        if not np.array_equal(got, expect):
+            out.append(f"mx_block_scaling_{dtype}")
+    return out
+
+
+def _pin_mx_nibble_order(lib):
+    """E2M1 packing: code 2 (1.0) at k = 0 of row 0 sits in the low nibble of
+    byte 0; at k = 1 in the high nibble. A one-hot row picks one k of B."""
+    out = []
+    K, N = 8, 3
+    for k_hot in (0, 1, 6, 7):
+        codes_a = np.zeros((1, K), np.uint8)
+        codes_a[0, k_hot] = 2
+        codes_b = (np.arange(N * K).reshape(N, K) % 8).astype(np.uint8)
+        sf = np.full((1, 1), 127, np.uint8)
+        got, _ = oracle.gemm_ref_mx(pack_e2m1(codes_a), pack_e2m1(codes_b), sf,
+                                    np.full((N, 1), 127, np.uint8), 1, N, K, "e2m1", lib=lib)
+        if not np.array_equal(got[0], [E2M1_TABLE[c] for c in codes_b[:, k_hot]]):
+            out.append(f"mx_nibble_{k_hot}")
+    return out
+
+
 PINS = [_pin_decoders, _pin_format_fixtures, _pin_hand_gemm, _pin_brute_force,
-        _pin_closed_forms, _pin_integers, _pin_torch_matmul, _pin_row_subset]
+        _pin_closed_forms, _pin_integers, _pin_torch_matmul, _pin_row_subset,
+        _pin_mx_fixtures, _pin_mx_brute_force, _pin_mx_unit_scales, _pin_mx_block_scaling,
+        _pin_mx_nibble_order]
 
 
 def pin_battery(lib):
@@ -360,7 +502,7 @@ def test_threads_do_not_change_bits(lib):
 # Each entry plants one plausible mistake in a copy of the oracle's source.
 MUTANTS = {
     "dropped_term": ("for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = 1; k < K; ++k) {"),
-    "transposed_b": ("j->layout_b == ORACLE_K_MAJOR ? c * j->K + k : k * j->N + c",
+    "transposed_b": ("j->layout_b == ORACLE_K_MAJOR ? c * j->row_elems + k : k * j->N + c",
                      "j->layout_b == ORACLE_K_MAJOR ? k * j->N + c : k * j->N + c"),
     "wrong_sign": ("c[col] += p;", "c[col] -= p;"),
     "f16_bias": ("e - 25", "e - 24"),
@@ -369,14 +511,23 @@ MUTANTS = {
     "bf16_hidden_bit": ("(double)(128 + f)", "(double)(f)"),
     "abs_dropped": ("cabs[col] += fabs(p);", "cabs[col] += p;"),
     "row_map_ignored": ("j->rows ? j->rows[r] : r", "r"),
-    "a_index_reversed": ("decode(j->A, i * K + k, j->dtype)",
-                         "decode(j->A, i * K + (K - 1 - k), j->dtype)"),
+    "a_index_reversed": ("decode(j->A, i * j->row_elems + k, j->dtype)",
+                         "decode(j->A, i * j->row_elems + (K - 1 - k), j->dtype)"),
     "e4m3_bias": ("e - 10", "e - 11"),
     "e4m3_subnormal": ("ldexp((double)f, -9)", "ldexp((double)f, -10)"),
     "e4m3_top_binade_as_nan": ("e == 0xf && f == 0x7", "e == 0xf"),
     "e4m3_fraction_width": ("int f = h & 0x7;", "int f = h & 0x3;"),
     "e5m2_bias": ("e - 17", "e - 16"),
     "e5m2_hidden_bit": ("(double)(4 + f)", "(double)(8 + f)"),
+    "e2m1_bias": ("ldexp((double)(2 + f), e - 2)", "ldexp((double)(2 + f), e - 1)"),
+    "e2m1_subnormal": ("ldexp((double)f, -1) :", "ldexp((double)f, 0) :"),
+    "e2m1_nibble_order": ("(idx & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF)",
+                          "(idx & 1) ? (uint8_t)(byte & 0xF) : (uint8_t)(byte >> 4)"),
+    "e2m1_row_pitch": ("dtype == ORACLE_E2M1 ? (K + 1) / 2 * 2 : K", "K"),
+    "e8m0_bias": ("ldexp(1.0, (int)e - 127)", "ldexp(1.0, (int)e - 128)"),
+    "mx_scale_a_ignored": ("if (j->sfa)", "if (!j->sfa)"),
+    "mx_scale_b_wrong_row": ("j->sfb[c * j->n_blocks", "j->sfb[0 * j->n_blocks"),
+    "mx_block_size": ("enum { ORACLE_MX_BLOCK = 32 };", "enum { ORACLE_MX_BLOCK = 64 };"),
     "fp8_read_as_16bit": ("case ORACLE_E4M3: return oracle_decode_e4m3(((const uint8_t *)base)[idx]);",
                           "case ORACLE_E4M3: return oracle_decode_e4m3((uint8_t)((const uint16_t *)base)[idx]);"),
 }
@@ -393,8 +544,15 @@ def test_planted_mistakes(name, tmp_path):
     subprocess.run(["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
                     "-pthread", "-D_POSIX_C_SOURCE=200809L", "-o", str(so), str(path), "-lm"],
                    check=True)
-    mutant = oracle.load_library(str(so))
-    assert pin_battery(mutant), f"no pin caught the planted mistake {name}"
+    # The battery runs in a child process: a mutant that reads out of bounds may
+    # crash, and a crash counts as a caught mistake.
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = ("import sys; sys.path[:0] = [%r, %r]; import oracle, test_oracle as t; "
+            "failed = t.pin_battery(oracle.load_library(%r)); print(len(failed)); "
+            "sys.exit(0 if failed else 3)") % (here, os.path.dirname(here), str(so))
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    assert res.returncode != 3, f"no pin caught the planted mistake {name}"
+    assert res.returncode == 0 or res.returncode < 0 or "Error" in res.stderr, res.stderr[-2000:]
 
 
 # ---------------------------------------------------------------- tolerance

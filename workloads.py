@@ -13,6 +13,12 @@ Recipe (the pages fix no generator; this is the plain reading):
   * rounded to FP16/BF16 or FP8 (E4M3 "FN", E5M2) with round-to-nearest-even
     (``Tensor.to``); the draws stay well inside each type's finite range.
 
+Block-scaled (MX) operands (``make_mx_operands``) are drawn already
+quantised: elements as above (E2M1 rounds to nearest, ties to the even
+code, and saturates at 6), packed two per byte for E2M1 (lower k in the low
+nibble, rows padded to whole bytes), then E8M0 scale exponents drawn
+uniformly from [127 - r, 127 + r], A's then B's, from the same generator.
+
 The workloads are the five GEMM shapes the tiled-GEMM pages measure or that
 exercise the method's edge paths (a small 256³ check, the compute-bound
 4096×4096×8192 FP16 shape of "Two Waves, One Stage Apart", §"MI350 Series",
@@ -31,6 +37,8 @@ import torch
 DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
           "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 FP8 = ("e4m3", "e5m2")
+MX_ELEMENT = {"mxfp8": "e4m3", "mxfp8_e5m2": "e5m2", "mxfp4": "e2m1"}   # MX type -> element type
+MX_BLOCK = 32
 
 
 @dataclass(frozen=True)
@@ -73,7 +81,12 @@ WORKLOADS = {w.name: w for w in [
              ("normal", 1.0), 9, "FP8 E4M3 square"),
     Workload("gemm_12288_e4m3", 12288, 12288, 12288, "e4m3", "bf16", "k",
              ("normal", 1.0), 10, "FP8 E4M3 square"),
+    Workload("gemm_4096x4096x65536_mxfp8", 4096, 4096, 65536, "mxfp8", "bf16", "k",
+             ("normal", 1.0), 11, "MXFP8, long K"),
+    Workload("gemm_4096x4096x65536_mxfp4", 4096, 4096, 65536, "mxfp4", "bf16", "k",
+             ("normal", 2.0), 12, "MXFP4, long K"),
 ]}
+MX_SCALE_RANGE = 3      # scale exponents 2^-3 .. 2^3 around 1.0
 
 HEADLINE = "gemm_4096x4096x8192_f16"
 
@@ -110,17 +123,69 @@ def make_operands(M: int, N: int, K: int, dtype_in: str, layout_b: str,
     return A, B
 
 
-def workload_operands(w: Workload) -> tuple[torch.Tensor, torch.Tensor]:
+def workload_operands(w: Workload):
+    """(A, B) for plain workloads, (A, B, SFA, SFB) for block-scaled (MX) ones."""
+    if w.dtype_in in MX_ELEMENT:
+        return make_mx_operands(w.M, w.N, w.K, w.dtype_in, w.dist, w.seed)
     return make_operands(w.M, w.N, w.K, w.dtype_in, w.layout_b, w.dist, w.seed)
 
 
+_E2M1_GRID = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)   # magnitudes of codes 0..7
+
+
+def round_e2m1(x: torch.Tensor) -> torch.Tensor:
+    """FP32 values -> E2M1 codes (uint8, 0..15): nearest grid magnitude, ties to the
+    code with a zero fraction bit (even), saturating at 6; sign in bit 3."""
+    mag = x.abs().clamp(max=6.0)
+    grid = torch.tensor(_E2M1_GRID)
+    dist = (mag[..., None] - grid).abs()
+    best = dist.min(dim=-1, keepdim=True).values
+    tie_ok = dist == best
+    # prefer even codes (fraction bit 0) among the nearest: codes 0, 2, 4, 6
+    even = torch.tensor([c % 2 == 0 for c in range(8)])
+    score = tie_ok.to(torch.int8) * 2 + (tie_ok & even).to(torch.int8)
+    code = score.argmax(dim=-1).to(torch.uint8)
+    return code | ((x < 0) & (code != 0)).to(torch.uint8) << 3
+
+
+def pack_e2m1(codes: torch.Tensor) -> torch.Tensor:
+    """rows x K codes -> rows x ceil(K/2) bytes, lower k in the low nibble."""
+    rows, K = codes.shape
+    if K % 2:
+        codes = torch.cat([codes, torch.zeros((rows, 1), dtype=torch.uint8)], dim=1)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).contiguous()
+
+
+def make_mx_operands(M: int, N: int, K: int, mx_type: str, dist: tuple, seed: int,
+                     scale_range: int = MX_SCALE_RANGE):
+    """CPU tensors (A, B, SFA, SFB) of a block-scaled GEMM.
+
+    A: M x K float8 (MXFP8) or M x ceil(K/2) uint8 of packed E2M1 (MXFP4);
+    B: N x K (K-major), same element layout. SFA: M x ceil(K/32), SFB:
+    N x ceil(K/32) uint8 E8M0 scale exponents."""
+    gen = torch.Generator().manual_seed(int(seed))
+    elem = MX_ELEMENT[mx_type]
+    a = _draw(gen, M * K, dist).reshape(M, K)
+    b = _draw(gen, N * K, dist).reshape(N, K)
+    if elem == "e2m1":
+        A, B = pack_e2m1(round_e2m1(a)), pack_e2m1(round_e2m1(b))
+    else:
+        A, B = a.to(DTYPES[elem]), b.to(DTYPES[elem])
+    nb = (K + MX_BLOCK - 1) // MX_BLOCK
+    lo, hi = 127 - scale_range, 127 + scale_range
+    SFA = torch.randint(lo, hi + 1, (M, nb), generator=gen).to(torch.uint8)
+    SFB = torch.randint(lo, hi + 1, (N, nb), generator=gen).to(torch.uint8)
+    return A, B, SFA, SFB
+
+
 def as_bits(t: torch.Tensor):
-    """Raw patterns of a CPU tensor: numpy uint16 for FP16/BF16, uint8 for FP8."""
+    """Raw patterns of a CPU tensor: numpy uint16 for FP16/BF16, uint8 for FP8 and
+    for byte tensors (packed E2M1, E8M0 scales)."""
     import numpy as np
     assert t.device.type == "cpu"
     if t.dtype in (torch.float16, torch.bfloat16):
         return t.contiguous().view(torch.int16).numpy().view(np.uint16)
-    assert t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2), t.dtype
+    assert t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2, torch.uint8), t.dtype
     return t.contiguous().view(torch.uint8).numpy()
 
 
