@@ -14,11 +14,11 @@ import ctypes
 import torch
 
 from . import binding
-from .binding import (GEMM_BF16, GEMM_E4M3, GEMM_E5M2, GEMM_F16, GEMM_F32, GEMM_K_MAJOR,
+from .binding import (GEMM_BF16, GEMM_E2M1, GEMM_E4M3, GEMM_E5M2, GEMM_F16, GEMM_F32, GEMM_K_MAJOR,
                       GEMM_MN_MAJOR, GEMM_OK, GEMM_ERR_TIMEOUT, GEMM_JOB_FULL, GEMM_JOB_OWNER,
                       GEMM_JOB_WRITER, GemmError, GemmJob, GemmOptions, GemmPlan, STATUS_NAMES)
 
-__all__ = ["gemm", "gemm_ex", "gemm_plan", "gemm_from_host", "gemm_release_workspace",
+__all__ = ["gemm", "gemm_ex", "gemm_mx", "gemm_plan", "gemm_from_host", "gemm_release_workspace",
            "gemm_last_device_status", "gemm_selftest_wait_timeout", "gemm_status_string",
            "gemm_launch_count", "gemm_schedule_jobs", "GemmError", "GemmOptions", "GemmPlan"]
 
@@ -115,6 +115,53 @@ def gemm_ex(A, B, C=None, *, options=None, **kw) -> torch.Tensor:
     """gemm with gemm_ex overrides (cta_group, block_n, max_clusters, group_m, timeout_ms,
     k_stage, stream_k)."""
     return gemm(A, B, C, options=options if options is not None else GemmOptions(), **kw)
+
+
+def gemm_mx(A: torch.Tensor, B: torch.Tensor, SFA: torch.Tensor, SFB: torch.Tensor,
+            C: torch.Tensor | None = None, *, K: int | None = None,
+            out_dtype: torch.dtype = torch.bfloat16, stream=None, options=None) -> torch.Tensor:
+    """Block-scaled C = (SFA o A)(SFB o B) on A's CUDA device (gemm_mx / gemm_mx_ex).
+
+    MXFP8: A (M, K) and B (N, K) float8_e4m3fn or float8_e5m2. MXFP4: A (M, ceil(K/2))
+    and B (N, ceil(K/2)) uint8 holding packed E2M1 pairs (lower k in the low nibble);
+    K defaults to twice the byte width. SFA (M, ceil(K/32)) and SFB (N, ceil(K/32))
+    uint8 E8M0 scale exponents. C: (M, N) of ``out_dtype``, allocated when not given.
+    """
+    for name, t in (("A", A), ("B", B), ("SFA", SFA), ("SFB", SFB)):
+        if t.device.type != "cuda" or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError(f"{name} must be a contiguous 2-D CUDA tensor")
+    if A.dtype != B.dtype:
+        raise TypeError("A and B must have the same dtype")
+    if A.dtype in _FP8:
+        dtype_in, K_ = _DT_IN[A.dtype], int(A.shape[1])
+        if K is not None and K != K_:
+            raise ValueError("K must equal A.shape[1] for FP8 elements")
+    elif A.dtype == torch.uint8:
+        dtype_in, K_ = GEMM_E2M1, int(K if K is not None else 2 * A.shape[1])
+        if (K_ + 1) // 2 != A.shape[1]:
+            raise ValueError("packed E2M1 rows must hold ceil(K/2) bytes")
+    else:
+        raise TypeError("A must be float8_e4m3fn, float8_e5m2 or uint8 (packed E2M1)")
+    M, N = int(A.shape[0]), int(B.shape[0])
+    nb = (K_ + 31) // 32
+    if tuple(B.shape) != (N, A.shape[1]):
+        raise ValueError("B must be (N, K) like A")
+    if tuple(SFA.shape) != (M, nb) or tuple(SFB.shape) != (N, nb) or SFA.dtype != torch.uint8 \
+            or SFB.dtype != torch.uint8:
+        raise ValueError(f"SFA must be uint8 ({M}, {nb}) and SFB uint8 ({N}, {nb})")
+    if C is None:
+        C = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    if C.dtype not in _DT_OUT or tuple(C.shape) != (M, N) or not C.is_contiguous():
+        raise ValueError("C must be a contiguous (M, N) float16/bfloat16/float32 tensor")
+    opts = _options(options)
+    args = (A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(), C.data_ptr(), M, N, K_,
+            dtype_in, _DT_OUT[C.dtype], GEMM_K_MAJOR, GEMM_K_MAJOR)
+    with torch.cuda.device(A.device):
+        if opts is None:
+            _check(binding.lib.gemm_mx(*args, _stream_ptr(stream)), "gemm_mx")
+        else:
+            _check(binding.lib.gemm_mx_ex(*args, ctypes.byref(opts), _stream_ptr(stream)), "gemm_mx_ex")
+    return C
 
 
 def gemm_plan(M: int, N: int, K: int, *, dtype_in=torch.float16, dtype_out=torch.float16,

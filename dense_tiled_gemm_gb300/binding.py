@@ -11,7 +11,7 @@ import os
 
 from .build import LIB_PATH
 
-GEMM_F16, GEMM_BF16, GEMM_F32, GEMM_E4M3, GEMM_E5M2 = 0, 1, 2, 3, 4
+GEMM_F16, GEMM_BF16, GEMM_F32, GEMM_E4M3, GEMM_E5M2, GEMM_E2M1 = 0, 1, 2, 3, 4, 5
 GEMM_K_MAJOR, GEMM_MN_MAJOR = 0, 1
 STATUS_NAMES = {
     0: "GEMM_OK",
@@ -68,6 +68,11 @@ def _declare(lib):
     lib.gemm.argtypes = gemm_args + [vp]
     lib.gemm_ex.restype = c_int
     lib.gemm_ex.argtypes = gemm_args + [ctypes.POINTER(GemmOptions), vp]
+    mx_args = [vp, vp, vp, vp, vp, i64, i64, i64, c_int, c_int, c_int, c_int]
+    lib.gemm_mx.restype = c_int
+    lib.gemm_mx.argtypes = mx_args + [vp]
+    lib.gemm_mx_ex.restype = c_int
+    lib.gemm_mx_ex.argtypes = mx_args + [ctypes.POINTER(GemmOptions), vp]
     lib.gemm_plan.restype = c_int
     lib.gemm_plan.argtypes = [i64, i64, i64, c_int, c_int, c_int, c_int, vp, vp, vp,
                               ctypes.POINTER(GemmOptions), ctypes.POINTER(GemmPlan)]

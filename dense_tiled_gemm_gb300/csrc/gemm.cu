@@ -35,30 +35,35 @@ constexpr uint64_t DEFAULT_TIMEOUT_MS = 2000;
 // pairs (8 MMAs per barrier wait; the MMA issuer's wait costs ~60-100 cycles
 // of tensor idle, so fewer waits per MMA pay), 64 for single CTAs (a 128-deep
 // stage leaves room for only two of them).
-int default_k_slabs(int cg) { return cg == 2 ? 2 : 1; }
+int default_k_slabs(int cg, int kind)
+{
+    // packed FP4 slabs already hold 256 K: one per stage keeps the TMEM scale buffer small
+    return kind == KIND_MXF4 ? 1 : cg == 2 ? 2 : 1;
+}
 
 struct Variant {
     int cg;
     int bn;
     int ks;            // K slabs (128 bytes of K each) per ring stage
-    int eb;            // operand element bytes: 2 (FP16/BF16) or 1 (FP8)
-    int stage_bytes;   // one ring slot: A and B tiles of one stage (per CTA)
+    int kind;          // KIND_F16, KIND_F8, KIND_MXF8 or KIND_MXF4
+    int stage_bytes;   // one ring slot: A and B tiles (and scales) of one stage, per CTA
     const void *fn;
     bool b_mn_ok;      // MN-major B needs 64-column TMA boxes per CTA (16-bit only)
 };
 
-template <int CG, int BN, int KS, int EB>
+template <int CG, int BN, int KS, int KIND>
 constexpr Variant variant(bool b_mn_ok)
 {
-    return {CG, BN, KS, EB, TileConfig<CG, BN, KS, EB>::STAGE_BYTES,
-            reinterpret_cast<const void *>(&gemm_tcgen05_kernel<CG, BN, KS, EB>), b_mn_ok};
+    return {CG, BN, KS, KIND, TileConfig<CG, BN, KS, KIND>::STAGE_BYTES,
+            reinterpret_cast<const void *>(&gemm_tcgen05_kernel<CG, BN, KS, KIND>), b_mn_ok};
 }
 
 const Variant kVariants[] = {
-    variant<2, 256, 1, 2>(true),  variant<2, 224, 1, 2>(false), variant<1, 256, 1, 2>(true),
-    variant<2, 256, 2, 2>(true),  variant<2, 224, 2, 2>(false), variant<1, 256, 2, 2>(true),
-    variant<2, 256, 1, 1>(false), variant<2, 224, 1, 1>(false), variant<1, 256, 1, 1>(false),
-    variant<2, 256, 2, 1>(false), variant<2, 224, 2, 1>(false), variant<1, 256, 2, 1>(false),
+    variant<2, 256, 1, KIND_F16>(true),  variant<2, 224, 1, KIND_F16>(false), variant<1, 256, 1, KIND_F16>(true),
+    variant<2, 256, 2, KIND_F16>(true),  variant<2, 224, 2, KIND_F16>(false), variant<1, 256, 2, KIND_F16>(true),
+    variant<2, 256, 1, KIND_F8>(false),  variant<2, 224, 1, KIND_F8>(false),  variant<1, 256, 1, KIND_F8>(false),
+    variant<2, 256, 2, KIND_F8>(false),  variant<2, 224, 2, KIND_F8>(false),  variant<1, 256, 2, KIND_F8>(false),
+    variant<2, 224, 2, KIND_MXF8>(false), variant<2, 224, 1, KIND_MXF4>(false),
 };
 constexpr int NUM_VARIANTS = sizeof(kVariants) / sizeof(kVariants[0]);
 
@@ -74,7 +79,8 @@ Layout layout_for(const Variant &v, int dtype_out)
 {
     Layout l;
     l.staging_bytes = dtype_out == GEMM_F32 ? 4096u : 2048u;
-    l.stages = MAX_STAGES;
+    // block-scaled kinds keep one TMEM scale slot per ring stage (MX_MAX_STAGES of them)
+    l.stages = kind_scaled(v.kind) ? MX_MAX_STAGES : MAX_STAGES;
     while (l.stages > 2 && smem_bytes_for(v.stage_bytes, l.stages, l.staging_bytes) > SMEM_LIMIT)
         --l.stages;
     l.smem = smem_bytes_for(v.stage_bytes, l.stages, l.staging_bytes);
@@ -117,10 +123,27 @@ unsigned long long next_launch_id()
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 bool is_fp8(int dtype) { return dtype == GEMM_E4M3 || dtype == GEMM_E5M2; }
-int in_bytes(int dtype_in) { return is_fp8(dtype_in) ? 1 : 2; }
 int out_bytes(int dtype_out) { return dtype_out == GEMM_F32 ? 4 : 2; }
 
-// Row pitch, in elements, that makes a row of `cols` elements a multiple of 16 bytes.
+// The MMA kind for an input type, plain (gemm) or block-scaled (gemm_mx).
+int kind_for(int dtype_in, bool scaled)
+{
+    if (dtype_in == GEMM_E2M1)
+        return KIND_MXF4;
+    if (is_fp8(dtype_in))
+        return scaled ? KIND_MXF8 : KIND_F8;
+    return KIND_F16;
+}
+
+// Bytes of one stored row of `elems` operand elements (packed FP4 rows are
+// padded to whole bytes), and the TMA element size.
+int64_t row_bytes(int kind, int64_t elems)
+{
+    return kind == KIND_F16 ? 2 * elems : kind == KIND_MXF4 ? (elems + 1) / 2 : elems;
+}
+int tma_elem_bytes(int kind) { return kind == KIND_F16 ? 2 : 1; }
+
+// Row pitch, in TMA elements, that makes a row of `cols` such elements a multiple of 16 bytes.
 int64_t padded_pitch(int64_t cols, int eb)
 {
     const int64_t q = 16 / eb;
@@ -196,14 +219,18 @@ gemm_status_t device_state(DeviceState **out)
 }
 
 gemm_status_t validate(const void *A, const void *B, const void *C, int64_t M, int64_t N, int64_t K,
-                       int dtype_in, int dtype_out, int layoutA, int layoutB, const gemm_options_t *o)
+                       int dtype_in, int dtype_out, int layoutA, int layoutB, const gemm_options_t *o,
+                       bool scaled = false)
 {
     if (!A || !B || !C)
         return GEMM_ERR_INVALID_ARG;
     if (M < 1 || N < 1 || K < 1 || M > INT_MAX || N > INT_MAX || K > INT_MAX)
         return GEMM_ERR_INVALID_ARG;
-    if (dtype_in != GEMM_F16 && dtype_in != GEMM_BF16 && !is_fp8(dtype_in))
+    if (dtype_in != GEMM_F16 && dtype_in != GEMM_BF16 && !is_fp8(dtype_in) && dtype_in != GEMM_E2M1)
         return dtype_in == GEMM_F32 ? GEMM_ERR_UNSUPPORTED : GEMM_ERR_INVALID_ARG;
+    // block-scaled products take 8- or 4-bit elements; packed FP4 only comes block-scaled
+    if (scaled ? (!is_fp8(dtype_in) && dtype_in != GEMM_E2M1) : dtype_in == GEMM_E2M1)
+        return GEMM_ERR_UNSUPPORTED;
     if (dtype_out != GEMM_F16 && dtype_out != GEMM_BF16 && dtype_out != GEMM_F32)
         return is_fp8(dtype_out) ? GEMM_ERR_UNSUPPORTED : GEMM_ERR_INVALID_ARG;
     if (layoutA != GEMM_K_MAJOR && layoutA != GEMM_MN_MAJOR)
@@ -212,7 +239,7 @@ gemm_status_t validate(const void *A, const void *B, const void *C, int64_t M, i
         return GEMM_ERR_UNSUPPORTED;
     if (layoutB != GEMM_K_MAJOR && layoutB != GEMM_MN_MAJOR)
         return GEMM_ERR_INVALID_ARG;
-    if (is_fp8(dtype_in) && layoutB == GEMM_MN_MAJOR)
+    if ((is_fp8(dtype_in) || dtype_in == GEMM_E2M1) && layoutB == GEMM_MN_MAJOR)
         return GEMM_ERR_UNSUPPORTED;
     if (o) {
         if (o->cta_group < 0 || o->cta_group > 2 || o->max_clusters < 0 || o->group_m < 0 ||
@@ -224,7 +251,7 @@ gemm_status_t validate(const void *A, const void *B, const void *C, int64_t M, i
             return GEMM_ERR_INVALID_ARG;
         if (o->stream_k > 2)
             return GEMM_ERR_UNSUPPORTED;
-        const int sk = slab_k(in_bytes(dtype_in));
+        const int sk = kind_slab_k(kind_for(dtype_in, scaled));
         if (o->k_stage != 0 && o->k_stage != sk && o->k_stage != 2 * sk)
             return GEMM_ERR_UNSUPPORTED;
     }
@@ -263,7 +290,7 @@ struct Cost {
     int sk_tiles;
 };
 
-Cost plan_cost(int64_t T, int64_t U, int64_t KB, int64_t K, int eb)
+Cost plan_cost(int64_t T, int64_t U, int64_t KB, int64_t k_bytes)
 {
     Cost c;
     c.dp = static_cast<double>((T + U - 1) / U);
@@ -271,7 +298,7 @@ Cost plan_cost(int64_t T, int64_t U, int64_t KB, int64_t K, int eb)
     c.sk_tiles = static_cast<int>(S);
     const int64_t L = (S * KB + U - 1) / U;                    // k-blocks per unit
     const int64_t writers = L >= KB ? 1 : (KB + L - 1) / L;    // other units per split tile
-    const double F = 600.0 / static_cast<double>(K * eb);
+    const double F = 600.0 / static_cast<double>(k_bytes);
     c.sk = static_cast<double>((T - S) / U) + static_cast<double>(L) / KB + writers * F;
     return c;
 }
@@ -286,22 +313,24 @@ bool misaligned(const void *p, int64_t row_elems, int elem_bytes)
 // Single-CTA tiles pay ~15% for their higher shared-memory read rate per flop.
 gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, int dtype_in,
                         int dtype_out, int layoutB, const void *A, const void *B, const void *C,
-                        const gemm_options_t *o, Plan *pl)
+                        const gemm_options_t *o, Plan *pl, bool scaled = false)
 {
     const bool b_mn = layoutB == GEMM_MN_MAJOR;
-    const int eb = in_bytes(dtype_in);
+    const int kind = kind_for(dtype_in, scaled);
+    const int sk_elems = kind_slab_k(kind);
+    const int64_t k_bytes = row_bytes(kind, K);
     const int mode = o ? o->stream_k : 0;
     int best = -1, best_sk = 0;
     double best_cost = 0;
     for (int v = 0; v < NUM_VARIANTS; ++v) {
         const Variant &var = kVariants[v];
-        if (var.eb != eb)
+        if (var.kind != kind)
             continue;
         if (o && o->cta_group && o->cta_group != var.cg)
             continue;
         if (o && o->block_n && o->block_n != var.bn)
             continue;
-        if (var.ks != ((o && o->k_stage) ? o->k_stage / slab_k(eb) : default_k_slabs(var.cg)))
+        if (var.ks != ((o && o->k_stage) ? o->k_stage / sk_elems : default_k_slabs(var.cg, var.kind)))
             continue;
         if (b_mn && !var.b_mn_ok)
             continue;
@@ -311,8 +340,8 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
         if (units < 1)
             continue;
         const int64_t tiles = ((M + 128 * var.cg - 1) / (128 * var.cg)) * ((N + var.bn - 1) / var.bn);
-        const int64_t kb = (K + static_cast<int64_t>(slab_k(eb)) * var.ks - 1) / (static_cast<int64_t>(slab_k(eb)) * var.ks);
-        const Cost c = plan_cost(tiles, units, kb, K, eb);
+        const int64_t kb = (K + static_cast<int64_t>(sk_elems) * var.ks - 1) / (static_cast<int64_t>(sk_elems) * var.ks);
+        const Cost c = plan_cost(tiles, units, kb, k_bytes);
         const double scale = var.bn * (var.cg == 1 ? 1.15 : 1.0);
         // stream-K only where it saves more than 3%, or when asked for
         const bool sk = mode == 2 || (mode == 0 && tiles % units != 0 && c.sk < 0.97 * c.dp);
@@ -336,15 +365,15 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
     if (tiles > INT_MAX)
         return GEMM_ERR_UNSUPPORTED;
     pl->num_tiles = static_cast<int>(tiles);
-    const int64_t stage_k = static_cast<int64_t>(slab_k(eb)) * var.ks;
+    const int64_t stage_k = static_cast<int64_t>(sk_elems) * var.ks;
     pl->num_kb = static_cast<int>((K + stage_k - 1) / stage_k);
     pl->sk_tiles = best_sk;
     // with stream-K every unit takes a share; otherwise no more units than tiles
     pl->grid_ctas = static_cast<int>(best_sk ? units : std::min<int64_t>(tiles, units)) * var.cg;
     pl->ws_bytes = best_sk ? sk_workspace_bytes(pl->grid_ctas, var.bn) : 0;
     pl->group_m = (o && o->group_m) ? o->group_m : 8;
-    pl->realign_a = misaligned(A, K, eb);
-    pl->realign_b = misaligned(B, b_mn ? N : K, eb);
+    pl->realign_a = misaligned(A, row_bytes(kind, K), 1);
+    pl->realign_b = misaligned(B, b_mn ? row_bytes(kind, N) : row_bytes(kind, K), 1);
     pl->direct_store = misaligned(C, N, out_bytes(dtype_out));
     return GEMM_OK;
 }
@@ -368,7 +397,8 @@ CUtensorMapDataType tma_dtype(int dtype)
     case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     case GEMM_F32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     case GEMM_E4M3:
-    case GEMM_E5M2: return CU_TENSOR_MAP_DATA_TYPE_UINT8;   // bytes are moved, not converted
+    case GEMM_E5M2:
+    case GEMM_E2M1: return CU_TENSOR_MAP_DATA_TYPE_UINT8;   // bytes are moved, not converted
     default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     }
 }
@@ -409,9 +439,9 @@ gemm_status_t realign(const void *src, int64_t rows, int64_t cols, int eb, int s
     return realign_into(src, rows, cols, ld, eb, sms, st, *out);
 }
 
-template <int CG, int BN, int KS, int EB>
-cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap &ta, const CUtensorMap &tb,
-                           const CUtensorMap &tc, const KernelParams &kp, cudaStream_t st)
+template <int CG, int BN, int KS, int KIND>
+cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap *maps, const KernelParams &kp,
+                           cudaStream_t st)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas));
@@ -433,53 +463,97 @@ cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap &ta, 
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<CG, BN, KS, EB>, ta, tb, tc, kp);
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<CG, BN, KS, KIND>, maps[0], maps[1], maps[2], maps[3],
+                              maps[4], kp);
 }
 
-cudaError_t launch_any(const Variant &v, int grid_ctas, uint32_t smem, const CUtensorMap &ta,
-                       const CUtensorMap &tb, const CUtensorMap &tc, const KernelParams &kp, cudaStream_t st)
+cudaError_t launch_any(const Variant &v, int grid_ctas, uint32_t smem, const CUtensorMap *maps,
+                       const KernelParams &kp, cudaStream_t st)
 {
-#define DTG_LAUNCH(CG, BN, KS, EB)                                                                 \
-    if (v.cg == CG && v.bn == BN && v.ks == KS && v.eb == EB)                                      \
-        return launch_variant<CG, BN, KS, EB>(grid_ctas, smem, ta, tb, tc, kp, st);
-    DTG_LAUNCH(2, 256, 1, 2)
-    DTG_LAUNCH(2, 224, 1, 2)
-    DTG_LAUNCH(1, 256, 1, 2)
-    DTG_LAUNCH(2, 256, 2, 2)
-    DTG_LAUNCH(2, 224, 2, 2)
-    DTG_LAUNCH(1, 256, 2, 2)
-    DTG_LAUNCH(2, 256, 1, 1)
-    DTG_LAUNCH(2, 224, 1, 1)
-    DTG_LAUNCH(1, 256, 1, 1)
-    DTG_LAUNCH(2, 256, 2, 1)
-    DTG_LAUNCH(2, 224, 2, 1)
-    DTG_LAUNCH(1, 256, 2, 1)
+#define DTG_LAUNCH(CG, BN, KS, KIND)                                                               \
+    if (v.cg == CG && v.bn == BN && v.ks == KS && v.kind == KIND)                                  \
+        return launch_variant<CG, BN, KS, KIND>(grid_ctas, smem, maps, kp, st);
+    DTG_LAUNCH(2, 256, 1, KIND_F16)
+    DTG_LAUNCH(2, 224, 1, KIND_F16)
+    DTG_LAUNCH(1, 256, 1, KIND_F16)
+    DTG_LAUNCH(2, 256, 2, KIND_F16)
+    DTG_LAUNCH(2, 224, 2, KIND_F16)
+    DTG_LAUNCH(1, 256, 2, KIND_F16)
+    DTG_LAUNCH(2, 256, 1, KIND_F8)
+    DTG_LAUNCH(2, 224, 1, KIND_F8)
+    DTG_LAUNCH(1, 256, 1, KIND_F8)
+    DTG_LAUNCH(2, 256, 2, KIND_F8)
+    DTG_LAUNCH(2, 224, 2, KIND_F8)
+    DTG_LAUNCH(1, 256, 2, KIND_F8)
+    DTG_LAUNCH(2, 224, 2, KIND_MXF8)
+    DTG_LAUNCH(2, 224, 1, KIND_MXF4)
 #undef DTG_LAUNCH
     return cudaErrorInvalidValue;
 }
 
-// Build the three tensor maps and the kernel parameters for operands already
-// at TMA-describable addresses (a_ptr/b_ptr with row pitches lda/ldb in
-// elements), and launch the plan's kernel on `st`.
-gemm_status_t encode_and_launch(const DeviceState &d, const Plan &pl, const void *a_ptr, int64_t lda,
-                                const void *b_ptr, int64_t ldb, void *C, int64_t M, int64_t N, int64_t K,
-                                int dtype_in, int dtype_out, bool b_mn, uint64_t timeout_ms, void *workspace,
-                                cudaStream_t st)
+// Packed-scale geometry of one operand: row blocks of R rows (128 for A, the
+// CTA's B rows for B), `stages` ring stages along K, `groups` atoms per stage.
+struct SfGeometry {
+    int R;
+    int64_t row_blocks, stages;
+    int groups, atoms;   // groups of 4 blocks per stage, 128-row atoms per group
+    int64_t atom_rows;   // 16-byte rows in the packed tensor
+    int64_t bytes() const { return atom_rows * SF_ROW_BYTES; }
+    int box_rows() const { return groups * atoms * SF_ATOM_ROWS; }
+};
+
+// A: row blocks of 128 rows (one CTA's rows), one atom per group. B: row
+// blocks of the whole tile width (every CTA of a pair holds all of it).
+SfGeometry sf_geometry(const Variant &var, const Plan &pl, int64_t rows, bool is_b)
+{
+    SfGeometry g;
+    g.R = is_b ? var.bn : BLOCK_M_CTA;
+    g.atoms = (g.R + 127) / 128;
+    g.row_blocks = (rows + g.R - 1) / g.R;
+    g.stages = pl.num_kb;
+    g.groups = kind_slab_k(var.kind) * var.ks / 128;
+    g.atom_rows = g.row_blocks * g.stages * g.groups * g.atoms * SF_ATOM_ROWS;
+    return g;
+}
+
+// An operand ready for the tensor maps: base and row pitch in TMA elements
+// (FP16/BF16 elements, or bytes for the 8- and 4-bit kinds).
+struct Operand {
+    const void *ptr;
+    int64_t ld;
+};
+
+// Build the tensor maps and the kernel parameters for operands already at
+// TMA-describable addresses, and launch the plan's kernel on `st`. For the
+// block-scaled kinds sfa/sfb are the packed scales (rows x num_kb x 16 bytes).
+gemm_status_t encode_and_launch(const DeviceState &d, const Plan &pl, Operand a, Operand b, const void *sfa,
+                                const void *sfb, void *C, int64_t M, int64_t N, int64_t K, int dtype_in,
+                                int dtype_out, bool b_mn, uint64_t timeout_ms, void *workspace, cudaStream_t st)
 {
     const Variant &var = kVariants[pl.variant];
-    const int eb = var.eb;
-    const uint32_t sk = static_cast<uint32_t>(slab_k(eb));
-    alignas(64) CUtensorMap ta, tb, tc;
-    std::memset(&tc, 0, sizeof(tc));
+    const int eb = tma_elem_bytes(var.kind);
+    const int64_t width = row_bytes(var.kind, K) / eb;   // K in TMA elements
+    const uint32_t box_k = var.kind == KIND_F16 ? 64 : 128;
+    alignas(64) CUtensorMap maps[5];
+    std::memset(maps, 0, sizeof(maps));
     const CUtensorMapDataType in_dt = tma_dtype(dtype_in);
-    bool ok = encode_2d(&ta, in_dt, a_ptr, K, M, lda * eb, sk, BLOCK_M_CTA, CU_TENSOR_MAP_SWIZZLE_128B);
+    bool ok = encode_2d(&maps[0], in_dt, a.ptr, width, M, a.ld * eb, box_k, BLOCK_M_CTA, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!b_mn)
-        ok = ok && encode_2d(&tb, in_dt, b_ptr, K, N, ldb * eb, sk, var.bn / var.cg, CU_TENSOR_MAP_SWIZZLE_128B);
+        ok = ok && encode_2d(&maps[1], in_dt, b.ptr, width, N, b.ld * eb, box_k, var.bn / var.cg,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
     else
-        ok = ok && encode_2d(&tb, in_dt, b_ptr, N, K, ldb * eb, 64, sk, CU_TENSOR_MAP_SWIZZLE_128B);
+        ok = ok && encode_2d(&maps[1], in_dt, b.ptr, N, K, b.ld * eb, 64, box_k, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!pl.direct_store)
-        ok = ok && encode_2d(&tc, tma_dtype(dtype_out), C, N, M, N * out_bytes(dtype_out), EPI_COLS, 32,
+        ok = ok && encode_2d(&maps[2], tma_dtype(dtype_out), C, N, M, N * out_bytes(dtype_out), EPI_COLS, 32,
                              dtype_out == GEMM_F32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+    if (kind_scaled(var.kind)) {
+        // packed scales: 16-byte rows, one box = this stage's atoms of one row block
+        const SfGeometry ga = sf_geometry(var, pl, M, false), gb = sf_geometry(var, pl, N, true);
+        ok = ok && encode_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_UINT8, sfa, SF_ROW_BYTES, ga.atom_rows, SF_ROW_BYTES,
+                             SF_ROW_BYTES, ga.box_rows(), CU_TENSOR_MAP_SWIZZLE_NONE);
+        ok = ok && encode_2d(&maps[4], CU_TENSOR_MAP_DATA_TYPE_UINT8, sfb, SF_ROW_BYTES, gb.atom_rows, SF_ROW_BYTES,
+                             SF_ROW_BYTES, gb.box_rows(), CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
     if (!ok)
         return GEMM_ERR_CUDA;
 
@@ -492,8 +566,14 @@ gemm_status_t encode_and_launch(const DeviceState &d, const Plan &pl, const void
     kp.num_tiles = pl.num_tiles;
     kp.num_k_blocks = pl.num_kb;
     kp.group_m = pl.group_m;
-    const uint32_t fmt = (dtype_in == GEMM_BF16 || dtype_in == GEMM_E5M2) ? 1u : 0u;
-    kp.idesc = make_idesc(128u * var.cg, static_cast<uint32_t>(var.bn), fmt, b_mn ? 1u : 0u);
+    if (kind_scaled(var.kind)) {
+        // mxf8f6f4: E4M3 = 0, E5M2 = 1; mxf4: E2M1 = 1
+        const uint32_t fmt = (dtype_in == GEMM_E5M2 || dtype_in == GEMM_E2M1) ? 1u : 0u;
+        kp.idesc = make_idesc_mx(128u * var.cg, static_cast<uint32_t>(var.bn), fmt);
+    } else {
+        const uint32_t fmt = (dtype_in == GEMM_BF16 || dtype_in == GEMM_E5M2) ? 1u : 0u;
+        kp.idesc = make_idesc(128u * var.cg, static_cast<uint32_t>(var.bn), fmt, b_mn ? 1u : 0u);
+    }
     kp.out_dtype = dtype_out == GEMM_F32 ? OUT_F32 : (dtype_out == GEMM_BF16 ? OUT_BF16 : OUT_F16);
     kp.b_mn_major = b_mn ? 1u : 0u;
     kp.direct_store = pl.direct_store ? 1u : 0u;
@@ -510,7 +590,7 @@ gemm_status_t encode_and_launch(const DeviceState &d, const Plan &pl, const void
     kp.launch_id = next_launch_id();
     kp.status = d.status;
 
-    if (launch_any(var, pl.grid_ctas, lay.smem, ta, tb, tc, kp, st) != cudaSuccess) {
+    if (launch_any(var, pl.grid_ctas, lay.smem, maps, kp, st) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -518,55 +598,88 @@ gemm_status_t encode_and_launch(const DeviceState &d, const Plan &pl, const void
     return GEMM_OK;
 }
 
-gemm_status_t run(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
-                  int dtype_in, int dtype_out, int layoutA, int layoutB, const gemm_options_t *opts,
-                  cudaStream_t st)
+// Repack one operand's scales (rows x ceil(K/32) bytes) into the kernel's
+// atoms (see pack_scales_kernel) at dst.
+gemm_status_t pack_scales(const uint8_t *sf, int64_t rows, int64_t K, const SfGeometry &g, int sms,
+                          cudaStream_t st, void *dst)
 {
-    gemm_status_t rc = validate(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, opts);
+    const int64_t total = g.atom_rows;
+    const unsigned blocks = static_cast<unsigned>(
+        std::max<int64_t>(std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(sms) * 8), 1));
+    pack_scales_kernel<<<blocks, 256, 0, st>>>(sf, static_cast<uint8_t *>(dst), rows, (K + 31) / 32, g.R,
+                                               g.row_blocks, g.stages, g.groups, g.atoms);
+    if (cudaGetLastError() != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return GEMM_OK;
+}
+
+gemm_status_t run(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C, int64_t M,
+                  int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB,
+                  const gemm_options_t *opts, cudaStream_t st)
+{
+    const bool scaled = SFA != nullptr;
+    gemm_status_t rc = validate(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, opts, scaled);
     if (rc != GEMM_OK)
         return rc;
     DeviceState *d = nullptr;
     if ((rc = device_state(&d)) != GEMM_OK)
         return rc;
     Plan pl;
-    if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, opts, &pl)) != GEMM_OK)
+    if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, opts, &pl, scaled)) != GEMM_OK)
         return rc;
+    const Variant &var = kVariants[pl.variant];
     const bool b_mn = layoutB == GEMM_MN_MAJOR;
-    const int eb = in_bytes(dtype_in);
+    const int eb = tma_elem_bytes(var.kind);
+    const int64_t a_width = row_bytes(var.kind, K) / eb;
+    const int64_t b_rows = b_mn ? K : N, b_width = b_mn ? N : a_width;
 
-    const void *a_ptr = A, *b_ptr = B;
-    int64_t lda = K, ldb = b_mn ? N : K;
-    void *a_tmp = nullptr, *b_tmp = nullptr, *ws = nullptr;
+    Operand a{A, a_width}, b{B, b_width};
+    void *a_tmp = nullptr, *b_tmp = nullptr, *ws = nullptr, *sf_tmp = nullptr;
     auto release = [&]() {
-        if (a_tmp)
-            cudaFreeAsync(a_tmp, st);
-        if (b_tmp)
-            cudaFreeAsync(b_tmp, st);
-        if (ws)
-            cudaFreeAsync(ws, st);
+        for (void *q : {a_tmp, b_tmp, ws, sf_tmp})
+            if (q)
+                cudaFreeAsync(q, st);
     };
     if (pl.ws_bytes && cudaMallocAsync(&ws, pl.ws_bytes, st) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_OUT_OF_MEMORY;
     }
-    if (pl.realign_a && (rc = realign(A, M, K, eb, d->sms, st, &a_tmp, &lda)) != GEMM_OK) {
+    if (pl.realign_a && (rc = realign(A, M, a_width, eb, d->sms, st, &a_tmp, &a.ld)) != GEMM_OK) {
         release();
         return rc;
     }
     if (a_tmp)
-        a_ptr = a_tmp;
-    if (pl.realign_b &&
-        (rc = realign(B, b_mn ? K : N, b_mn ? N : K, eb, d->sms, st, &b_tmp, &ldb)) != GEMM_OK) {
+        a.ptr = a_tmp;
+    if (pl.realign_b && (rc = realign(B, b_rows, b_width, eb, d->sms, st, &b_tmp, &b.ld)) != GEMM_OK) {
         release();
         return rc;
     }
     if (b_tmp)
-        b_ptr = b_tmp;
+        b.ptr = b_tmp;
+    const void *sfa = nullptr, *sfb = nullptr;
+    if (scaled) {
+        const SfGeometry ga = sf_geometry(var, pl, M, false), gb = sf_geometry(var, pl, N, true);
+        const size_t a_bytes = static_cast<size_t>(ga.bytes()), b_bytes = static_cast<size_t>(gb.bytes());
+        const size_t b_off = (a_bytes + 255) / 256 * 256;
+        if (cudaMallocAsync(&sf_tmp, b_off + b_bytes, st) != cudaSuccess) {
+            cudaGetLastError();
+            sf_tmp = nullptr;
+            release();
+            return GEMM_ERR_OUT_OF_MEMORY;
+        }
+        sfa = sf_tmp;
+        sfb = static_cast<char *>(sf_tmp) + b_off;
+        if ((rc = pack_scales(SFA, M, K, ga, d->sms, st, const_cast<void *>(sfa))) != GEMM_OK ||
+            (rc = pack_scales(SFB, N, K, gb, d->sms, st, const_cast<void *>(sfb))) != GEMM_OK) {
+            release();
+            return rc;
+        }
+    }
 
     const uint64_t timeout_ms = opts && opts->timeout_ms ? static_cast<uint64_t>(opts->timeout_ms)
                                                          : DEFAULT_TIMEOUT_MS;
-    rc = encode_and_launch(*d, pl, a_ptr, lda, b_ptr, ldb, C, M, N, K, dtype_in, dtype_out, b_mn, timeout_ms, ws,
-                           st);
+    rc = encode_and_launch(*d, pl, a, b, sfa, sfb, C, M, N, K, dtype_in, dtype_out, b_mn, timeout_ms, ws, st);
     release();
     return rc;
 }
@@ -578,7 +691,7 @@ extern "C" {
 gemm_status_t gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int dtype_in,
                    int dtype_out, int layoutA, int layoutB, void *stream)
 {
-    return run(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, nullptr,
+    return run(A, B, nullptr, nullptr, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, nullptr,
                static_cast<cudaStream_t>(stream));
 }
 
@@ -586,7 +699,26 @@ gemm_status_t gemm_ex(const void *A, const void *B, void *C, int64_t M, int64_t 
                       int dtype_in, int dtype_out, int layoutA, int layoutB, const gemm_options_t *opts,
                       void *stream)
 {
-    return run(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, opts,
+    return run(A, B, nullptr, nullptr, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, opts,
+               static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_mx(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C, int64_t M,
+                      int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB, void *stream)
+{
+    if (!SFA || !SFB)
+        return GEMM_ERR_INVALID_ARG;
+    return run(A, B, SFA, SFB, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, nullptr,
+               static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_mx_ex(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C,
+                         int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB,
+                         const gemm_options_t *opts, void *stream)
+{
+    if (!SFA || !SFB)
+        return GEMM_ERR_INVALID_ARG;
+    return run(A, B, SFA, SFB, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, opts,
                static_cast<cudaStream_t>(stream));
 }
 
@@ -610,7 +742,7 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype
     plan->cta_group = var.cg;
     plan->block_m = 128 * var.cg;
     plan->block_n = var.bn;
-    plan->block_k = slab_k(var.eb) * var.ks;
+    plan->block_k = kind_slab_k(var.kind) * var.ks;
     const Layout lay = layout_for(var, dtype_out);
     plan->stages = static_cast<int32_t>(lay.stages);
     plan->num_tiles = pl.num_tiles;
@@ -638,8 +770,9 @@ gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_hos
         return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     auto up256 = [](size_t x) { return (x + 255) / 256 * 256; };
-    const int eb = in_bytes(dtype_in);
-    const size_t a_bytes = static_cast<size_t>(M * K * eb), b_bytes = static_cast<size_t>(N * K * eb);
+    const int kind = kind_for(dtype_in, false);
+    const size_t a_bytes = static_cast<size_t>(M * row_bytes(kind, K));
+    const size_t b_bytes = static_cast<size_t>(layoutB == GEMM_MN_MAJOR ? K * row_bytes(kind, N) : N * row_bytes(kind, K));
     const size_t c_bytes = static_cast<size_t>(M * N * out_bytes(dtype_out));
     const size_t need = up256(a_bytes) + up256(b_bytes) + up256(c_bytes);
     std::lock_guard<std::mutex> lock(d->ws_mu);
@@ -664,7 +797,7 @@ gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_hos
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
-    rc = run(dA, dB, dC, M, N, K, dtype_in, dtype_out, layoutA, layoutB, nullptr, st);
+    rc = run(dA, dB, nullptr, nullptr, dC, M, N, K, dtype_in, dtype_out, layoutA, layoutB, nullptr, st);
     if (rc != GEMM_OK)
         return rc;
     if (cudaMemcpyAsync(C_host, dC, c_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
@@ -825,12 +958,14 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
     if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, nullptr, &pl)) != GEMM_OK)
         return rc;
     const bool b_mn = layoutB == GEMM_MN_MAJOR;
-    const int eb = in_bytes(dtype_in);
+    const int kind = kind_for(dtype_in, false);
+    const int eb = tma_elem_bytes(kind);
 
     // Scratch layout: padded A at offset 0, padded B and then the stream-K
     // workspace, each at the next 256-byte boundary.
-    const int64_t b_rows = b_mn ? K : N, b_cols = b_mn ? N : K;
-    const int64_t lda_pad = padded_pitch(K, eb), ldb_pad = padded_pitch(b_cols, eb);
+    const int64_t a_cols = row_bytes(kind, K) / eb;
+    const int64_t b_rows = b_mn ? K : N, b_cols = b_mn ? N : a_cols;
+    const int64_t lda_pad = padded_pitch(a_cols, eb), ldb_pad = padded_pitch(b_cols, eb);
     const uint64_t a_bytes = pl.realign_a ? static_cast<uint64_t>(M) * lda_pad * eb : 0;
     const uint64_t b_off = (a_bytes + 255) / 256 * 256;
     const uint64_t b_bytes = pl.realign_b ? static_cast<uint64_t>(b_rows) * ldb_pad * eb : 0;
@@ -845,8 +980,7 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
             return rc;
     }
 
-    const void *a_ptr = A, *b_ptr = B;
-    int64_t lda = K, ldb = b_cols;
+    Operand a{A, a_cols}, b{B, b_cols};
     void *ws = nullptr;
     if (pl.realign_a || pl.realign_b || pl.sk_tiles) {
         void *scratch = nullptr;
@@ -856,19 +990,17 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
         if (pl.sk_tiles)
             ws = base + ws_off;
         if (pl.realign_a) {
-            if ((rc = realign_into(A, M, K, lda_pad, eb, d->sms, st, base)) != GEMM_OK)
+            if ((rc = realign_into(A, M, a_cols, lda_pad, eb, d->sms, st, base)) != GEMM_OK)
                 return rc;
-            a_ptr = base;
-            lda = lda_pad;
+            a = {base, lda_pad};
         }
         if (pl.realign_b) {
             if ((rc = realign_into(B, b_rows, b_cols, ldb_pad, eb, d->sms, st, base + b_off)) != GEMM_OK)
                 return rc;
-            b_ptr = base + b_off;
-            ldb = ldb_pad;
+            b = {base + b_off, ldb_pad};
         }
     }
-    return encode_and_launch(*d, pl, a_ptr, lda, b_ptr, ldb, C, M, N, K, dtype_in, dtype_out, b_mn,
+    return encode_and_launch(*d, pl, a, b, nullptr, nullptr, C, M, N, K, dtype_in, dtype_out, b_mn,
                              DEFAULT_TIMEOUT_MS, ws, st);
 }
 

@@ -1,7 +1,8 @@
 // gemm_kernel.cuh: the persistent, warp-specialised tcgen05 GEMM for sm_103a.
 //
-// C = A·B with FP16/BF16 or FP8 (E4M3/E5M2) operands, an FP32 accumulator in
-// tensor memory (TMEM) and a cast on store. "Two Waves, One Stage Apart" (sections "Why the Matrix
+// C = A·B with FP16/BF16 or FP8 (E4M3/E5M2) operands, or the block-scaled
+// (MX) C = (SFA ∘ A)·(SFB ∘ B) with MXFP8/MXFP4 operands, an FP32 accumulator
+// in tensor memory (TMEM) and a cast on store. "Two Waves, One Stage Apart" (sections "Why the Matrix
 // Pipeline Drains" and "Two Waves, One Stage Apart") keeps the matrix unit
 // busy by holding data preparation one stage ahead of matrix work. Here that
 // offset comes from fixed warp roles linked by shared-memory barriers, not
@@ -56,8 +57,29 @@ constexpr int BLOCK_M_CTA = 128;     // accumulator rows per CTA = TMEM lanes
 constexpr int MMA_K_BYTES = 32;      // K bytes of one tcgen05.mma (K = 16 FP16/BF16, 32 FP8)
 constexpr int SLAB_MMAS = SLAB_BYTES / MMA_K_BYTES;
 
-// K elements in one slab: 64 for 16-bit operands, 128 for FP8.
-__host__ __device__ constexpr int slab_k(int elem_bytes) { return SLAB_BYTES / elem_bytes; }
+// K elements in one slab: 64 for 16-bit operands, 128 for FP8, 256 for packed FP4.
+__host__ __device__ constexpr int kind_slab_k(int kind) { return kind == KIND_F16 ? 64 : kind == KIND_MXF4 ? 256 : 128; }
+
+// Block-scaled kinds. The E8M0 scales of up to 128 rows and 4 consecutive
+// 32-K blocks form one 512-byte atom: byte m32 * 16 + m4 * 4 + k4 holds the
+// scale of row m4 * 32 + m32, block k4. tcgen05.cp (32x128b.warpx4) turns
+// an atom into 4 TMEM columns, lane m32 of every lane quarter, column m4,
+// byte k4. A block-scaled MMA reads the scale of row m of A at column m / 32
+// from its A-scale address (each CTA of a pair holds its own 128 rows), and
+// the scale of column n of B at column n / 32 from its B-scale address, for
+// all N columns of the instruction (each CTA of a pair holds all of them), in
+// the byte its descriptor's scale-ID picks. A ring stage carries SF_GROUPS
+// groups of 4 blocks: per group one atom of A and SFB_ATOMS atoms of B (the
+// whole tile width). The MMA thread copies them into one TMEM scale buffer at
+// columns SF_COL0.. before the stage's MMAs (tcgen05.cp and tcgen05.mma of
+// one thread run in issue order, so the next stage's copies cannot overtake
+// this stage's MMAs). Accumulators use columns [0, BN) and [256, 256 + BN),
+// so block-scaled tiles are at most 224 wide.
+constexpr int SF_ATOM_BYTES = 512;
+constexpr int SF_ATOM_ROWS = 32;
+constexpr int SF_ROW_BYTES = 16;
+constexpr uint32_t SF_COL0 = 224;
+constexpr int MX_MAX_STAGES = 8;
 constexpr int NUM_THREADS = 192;     // producer warp, MMA warp, 4 epilogue warps
 constexpr int EPI_WARP0 = 2;
 constexpr int TMEM_COLS = 512;       // two accumulators at columns 0 and 256
@@ -99,24 +121,41 @@ struct KernelParams {
     unsigned long long *status;  // [0] first timed-out launch, [1] site, [2] last timed-out launch
 };
 
-// KS = K slabs per ring stage, EB = operand element bytes (2: FP16/BF16, 1:
-// FP8). One slab is a 128-byte-wide K strip of A and B in the 128-byte swizzle
-// layout (64 K of 16-bit operands or 128 K of FP8: 4 MMAs either way). A stage
-// holds KS slabs of A then KS slabs of B, so one barrier wait on the MMA
-// thread covers 4 x KS MMAs. The byte layout does not depend on EB.
-template <int CG, int BN, int KS, int EB>
+// KS = K slabs per ring stage, KIND = operand kind (KIND_F16, KIND_F8,
+// KIND_MXF8, KIND_MXF4). One slab is a 128-byte-wide K strip of A and B in
+// the 128-byte swizzle layout (64 K of 16-bit operands, 128 K of FP8, 256 K
+// of packed FP4: 4 MMAs in every case). A stage holds KS slabs of A, KS slabs
+// of B and, for the block-scaled kinds, the scale blocks of A and B, so one
+// barrier wait on the MMA thread covers 4 x KS MMAs.
+template <int CG, int BN, int KS, int KIND>
 struct TileConfig {
     static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
     static_assert(KS == 1 || KS == 2, "one or two K slabs per stage");
-    static_assert(EB == 1 || EB == 2, "8-bit or 16-bit operands");
+    static constexpr bool SCALED = kind_scaled(KIND);
     static constexpr int BN_CTA = BN / CG;   // B rows (K-major) or columns (MN-major) per CTA
     static_assert(BN % (16 * CG) == 0 && BN <= 256 && BN_CTA % 8 == 0, "invalid tile width");
-    static constexpr int SLAB_K = slab_k(EB);
+    static_assert(!SCALED || (BN <= 224 && BN_CTA <= 128), "block-scaled tiles: <= 224 wide, <= 128 B rows per CTA");
+    static constexpr int SLAB_K = kind_slab_k(KIND);
     static constexpr int A_SLAB = BLOCK_M_CTA * SLAB_BYTES;
     static constexpr int B_SLAB = BN_CTA * SLAB_BYTES;
     static constexpr int A_BYTES = KS * A_SLAB;
-    static constexpr int STAGE_BYTES = KS * (A_SLAB + B_SLAB);
+    static constexpr int AB_BYTES = KS * (A_SLAB + B_SLAB);
     static constexpr int STAGE_K = KS * SLAB_K;
+    // scale groups per stage (4 blocks of 32 K each), B atoms per group (whole tile width)
+    static constexpr int SF_GROUPS = SCALED ? STAGE_K / 128 : 0;
+    static constexpr int SFB_ATOMS = (BN + 127) / 128;
+    static constexpr int SFA_BYTES = SF_GROUPS * SF_ATOM_BYTES;
+    static constexpr int SFB_BYTES = SF_GROUPS * SFB_ATOMS * SF_ATOM_BYTES;
+    static constexpr int STAGE_BYTES = AB_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int STAGE_TX = STAGE_BYTES;   // bytes the TMA engine delivers per stage and CTA
+    // TMEM scale buffer: A at SF_COL0 + 4g, B at SF_COL0 + 4 * SF_GROUPS + 4 * (g * SFB_ATOMS + atom)
+    static constexpr uint32_t SFB_COL = SF_COL0 + 4u * SF_GROUPS;
+    static_assert(!SCALED || (SF_GROUPS >= 1 && SFB_COL + 4u * SF_GROUPS * SFB_ATOMS <= 256u),
+                  "the TMEM scale buffer fits between the two accumulators");
+    // TMA x coordinate units per slab: FP16/BF16 elements, or bytes for the 8- and 4-bit kinds
+    static constexpr int SLAB_X = KIND == KIND_F16 ? 64 : 128;
+    // K blocks of 32 per MMA: 2 for packed FP4 (K = 64), else 1 (K <= 32)
+    static constexpr int MMA_SF_BLOCKS = KIND == KIND_MXF4 ? 2 : 1;
     static_assert(A_SLAB % 1024 == 0 && B_SLAB % 1024 == 0, "slabs must stay 1024-byte aligned");
 };
 
@@ -244,6 +283,14 @@ __device__ __forceinline__ bool wait_flag_bounded(WaitCtx &w, const unsigned lon
     return !w.aborted;
 }
 
+// Row of the packed scale tensor (16-byte rows) where the atoms of row block
+// rb for ring stage kb start: blocks are row-block major, then stage, then
+// atom, 32 rows of 16 bytes per atom.
+__device__ __forceinline__ int sf_atom_row(int rb, int kb, int num_kb, int groups)
+{
+    return ((rb * num_kb + kb) * groups) * SF_ATOM_ROWS;
+}
+
 // ------------------------------------------------------------------ tile order
 // Persistent tile t -> (m_blk, n_blk). Tiles run in groups of group_m tile
 // rows. Inside a group, the tile row changes fastest, so tiles running at the
@@ -327,13 +374,15 @@ __device__ __forceinline__ void store_row_direct(const KernelParams &p, int row,
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int CG, int BN, int KS, int EB>
+template <int CG, int BN, int KS, int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
-                    const __grid_constant__ CUtensorMap tmap_c, const KernelParams p)
+                    const __grid_constant__ CUtensorMap tmap_c,
+                    const __grid_constant__ CUtensorMap tmap_sfa,   // block-scaled kinds only
+                    const __grid_constant__ CUtensorMap tmap_sfb, const KernelParams p)
 {
-    using Cfg = TileConfig<CG, BN, KS, EB>;
+    using Cfg = TileConfig<CG, BN, KS, KIND>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     if (base & 1023u) {
@@ -401,6 +450,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
         if (lane == 0) {
             prefetch_tensor_map(&tmap_a);
             prefetch_tensor_map(&tmap_b);
+            if constexpr (Cfg::SCALED) {
+                prefetch_tensor_map(&tmap_sfa);
+                prefetch_tensor_map(&tmap_sfb);
+            }
             uint32_t s = 0, ph = 0, pend_mask = 0, pend_par = 0;
             for (int i = 0; i < num_jobs; ++i) {
                 const Job jb = sch.job(i);
@@ -413,36 +466,51 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     if (!w.aborted) {
                         const uint32_t a_dst = base + s * Cfg::STAGE_BYTES;
                         const uint32_t b_dst = a_dst + Cfg::A_BYTES;
-                        const int k0 = kb * Cfg::STAGE_K;
+                        const int x0 = kb * KS * Cfg::SLAB_X;
                         if constexpr (CG == 1) {
                             const uint32_t bar = full_bar(s);
-                            mbar_arrive_expect_tx(bar, Cfg::STAGE_BYTES);
+                            mbar_arrive_expect_tx(bar, Cfg::STAGE_TX);
 #pragma unroll
                             for (int j = 0; j < KS; ++j) {
-                                const int kj = k0 + j * Cfg::SLAB_K;
+                                const int kj = x0 + j * Cfg::SLAB_X;
                                 tma_load_2d(a_dst + j * Cfg::A_SLAB, &tmap_a, bar, kj, a_row);
                                 const uint32_t bj = b_dst + j * Cfg::B_SLAB;
-                                if (EB == 1 || !p.b_mn_major)
+                                if (KIND != KIND_F16 || !p.b_mn_major)
                                     tma_load_2d(bj, &tmap_b, bar, kj, b_off);
                                 else
                                     for (int i = 0; i < Cfg::BN_CTA / 64; ++i)
                                         tma_load_2d(bj + i * 8192u, &tmap_b, bar, b_off + 64 * i, kj);
                             }
+                            if constexpr (Cfg::SCALED) {
+                                // this stage's scale atoms of the CTA's A and B row blocks
+                                tma_load_2d(a_dst + Cfg::AB_BYTES, &tmap_sfa, bar, 0,
+                                            sf_atom_row(a_row / BLOCK_M_CTA, kb, p.num_k_blocks, Cfg::SF_GROUPS));
+                                tma_load_2d(a_dst + Cfg::AB_BYTES + Cfg::SFA_BYTES, &tmap_sfb, bar, 0,
+                                            sf_atom_row(n_blk, kb, p.num_k_blocks, Cfg::SF_GROUPS * Cfg::SFB_ATOMS));
+                            }
                         } else {
                             // both CTAs' boxes complete on the even CTA's full barrier
                             const uint32_t bar = map_to_cta(full_bar(s), 0);
                             if (rank == 0)
-                                mbar_arrive_expect_tx(full_bar(s), 2u * Cfg::STAGE_BYTES);
+                                mbar_arrive_expect_tx(full_bar(s), 2u * Cfg::STAGE_TX);
 #pragma unroll
                             for (int j = 0; j < KS; ++j) {
-                                const int kj = k0 + j * Cfg::SLAB_K;
+                                const int kj = x0 + j * Cfg::SLAB_X;
                                 tma_load_2d_pair(a_dst + j * Cfg::A_SLAB, &tmap_a, bar, kj, a_row);
                                 const uint32_t bj = b_dst + j * Cfg::B_SLAB;
-                                if (EB == 1 || !p.b_mn_major)
+                                if (KIND != KIND_F16 || !p.b_mn_major)
                                     tma_load_2d_pair(bj, &tmap_b, bar, kj, b_off);
                                 else
                                     for (int i = 0; i < Cfg::BN_CTA / 64; ++i)
                                         tma_load_2d_pair(bj + i * 8192u, &tmap_b, bar, b_off + 64 * i, kj);
+                            }
+                            if constexpr (Cfg::SCALED) {
+                                // both CTAs load the B scales of the whole tile width
+                                tma_load_2d_pair(a_dst + Cfg::AB_BYTES, &tmap_sfa, bar, 0,
+                                                 sf_atom_row(a_row / BLOCK_M_CTA, kb, p.num_k_blocks, Cfg::SF_GROUPS));
+                                tma_load_2d_pair(a_dst + Cfg::AB_BYTES + Cfg::SFA_BYTES, &tmap_sfb, bar, 0,
+                                                 sf_atom_row(n_blk, kb, p.num_k_blocks,
+                                                             Cfg::SF_GROUPS * Cfg::SFB_ATOMS));
                             }
                         }
                         pend_mask |= 1u << s;
@@ -465,8 +533,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0 && (CG == 1 || rank == 0)) {
-            // FP8 operands are K-major only (the host rejects MN-major FP8 B).
-            const bool b_mn = EB == 2 && p.b_mn_major != 0;
+            // 8-bit and 4-bit operands are K-major only (the host rejects MN-major B for them).
+            const bool b_mn = KIND == KIND_F16 && p.b_mn_major != 0;
             // K-major: rows of 128 B in 8-row groups 1024 B apart; one MMA step = 32 B.
             // MN-major (16-bit): 64-wide N atoms 8192 B apart (LBO), 8-row K groups
             // 1024 B apart (SBO); one K=16 step = 16 rows = 2048 B.
@@ -483,6 +551,15 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     tc_fence_after_sync();
                     if (!w.aborted) {
                         const uint32_t a_addr = base + s * Cfg::STAGE_BYTES;
+                        const uint32_t sf_a = tmem_base + SF_COL0, sf_b = tmem_base + Cfg::SFB_COL;
+                        if constexpr (Cfg::SCALED) {
+                            // this stage's scale atoms into TMEM, in smem order (A's, then B's);
+                            // later MMAs of this thread see them
+                            const uint32_t src = a_addr + Cfg::AB_BYTES;
+#pragma unroll
+                            for (int t = 0; t < Cfg::SF_GROUPS * (1 + Cfg::SFB_ATOMS); ++t)
+                                tmem_cp_32x128b_warpx4<CG>(sf_a + 4u * t, smem_desc_plain(src + t * SF_ATOM_BYTES, 128u));
+                        }
 #pragma unroll
                         for (int j = 0; j < KS; ++j) {
                             // a slab wholly past K holds only TMA zero fill: skip its MMAs
@@ -492,9 +569,19 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                             const uint64_t b_desc = smem_desc_sw128(a_addr + Cfg::A_BYTES + j * Cfg::B_SLAB,
                                                                     b_lbo, 1024u);
 #pragma unroll
-                            for (uint32_t k = 0; k < SLAB_MMAS; ++k)
-                                mma<CG, EB>(d_tmem, a_desc + 2u * k, b_desc + b_step * k, p.idesc,
-                                            (kb > jb.kb0 || j > 0 || k > 0) ? 1u : 0u);
+                            for (uint32_t k = 0; k < SLAB_MMAS; ++k) {
+                                const uint32_t acc_in = (kb > jb.kb0 || j > 0 || k > 0) ? 1u : 0u;
+                                if constexpr (Cfg::SCALED) {
+                                    // first 32-K block of this MMA within the stage: its scales
+                                    // are byte blk % 4 of atom blk / 4 (4 TMEM columns)
+                                    const uint32_t blk = (j * SLAB_MMAS + k) * Cfg::MMA_SF_BLOCKS;
+                                    mma_scaled<CG, KIND>(d_tmem, a_desc + 2u * k, b_desc + b_step * k,
+                                                         p.idesc | mx_sf_id(blk % 4u), sf_a + 4u * (blk / 4u),
+                                                         sf_b + 4u * Cfg::SFB_ATOMS * (blk / 4u), acc_in);
+                                } else {
+                                    mma<CG, KIND>(d_tmem, a_desc + 2u * k, b_desc + b_step * k, p.idesc, acc_in);
+                                }
+                            }
                         }
                         if constexpr (CG == 1)
                             mma_commit(empty_bar(s));
@@ -669,6 +756,41 @@ __global__ void wait_selftest_kernel(uint64_t timeout_ns, unsigned long long lau
     if (threadIdx.x == 0) {
         WaitCtx w{timeout_ns, launch_id, status, false};
         wait_bounded<false>(w, smem_u32(&bar), 0, SITE_SELFTEST);
+    }
+}
+
+// Repack E8M0 scales (rows x n_blocks bytes, row-major: one byte per 32 K)
+// into the kernel's atoms: row blocks of R rows, and per row block and ring
+// stage `groups` groups of 4 blocks, each group `atoms` atoms of 128 rows
+// (see SF_ATOM_BYTES). Missing rows and blocks are zero. out has row_blocks x
+// stages x groups x atoms x 32 rows of 16 bytes; each thread writes one row.
+__global__ void pack_scales_kernel(const uint8_t *__restrict__ sf, uint8_t *__restrict__ out, int64_t rows,
+                                   int64_t n_blocks, int R, int64_t row_blocks, int64_t stages, int groups,
+                                   int atoms)
+{
+    const int64_t total = row_blocks * stages * groups * atoms * SF_ATOM_ROWS;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int m32 = static_cast<int>(i % SF_ATOM_ROWS);
+        int64_t t = i / SF_ATOM_ROWS;
+        const int a = static_cast<int>(t % atoms);
+        t /= atoms;
+        const int g = static_cast<int>(t % groups);
+        t /= groups;
+        const int64_t st = t % stages, rb = t / stages;
+        uint32_t w[4] = {0, 0, 0, 0};
+        for (int m4 = 0; m4 < 4; ++m4) {
+            const int m = a * 128 + m4 * SF_ATOM_ROWS + m32;
+            const int64_t row = rb * R + m;
+            if (m >= R || row >= rows)
+                continue;
+            for (int k4 = 0; k4 < 4; ++k4) {
+                const int64_t blk = (st * groups + g) * 4 + k4;
+                if (blk < n_blocks)
+                    w[m4] |= static_cast<uint32_t>(sf[row * n_blocks + blk]) << (8 * k4);
+            }
+        }
+        reinterpret_cast<uint4 *>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 

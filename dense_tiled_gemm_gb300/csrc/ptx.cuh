@@ -265,22 +265,29 @@ __device__ __forceinline__ void tc_fence_after_sync()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] · B[smem] with an FP32 accumulator. EB is the operand
-// element width: 2 bytes -> kind::f16 (FP16/BF16, K = 16 per instruction),
-// 1 byte -> kind::f8f6f4 (E4M3/E5M2, K = 32 per instruction). Either way one
-// instruction consumes 32 bytes of K from every operand row.
-template <int CG, int EB>
+// Operand kinds of the MMA:
+//   KIND_F16   kind::f16,      FP16/BF16,          K = 16 per instruction
+//   KIND_F8    kind::f8f6f4,   E4M3/E5M2,          K = 32
+//   KIND_MXF8  kind::mxf8f6f4, E4M3/E5M2 + E8M0 scale per 32 K (scale_vec::1X), K = 32
+//   KIND_MXF4  kind::mxf4,     packed E2M1 + E8M0 scale per 32 K (scale_vec::2X), K = 64
+// Every instruction consumes 32 bytes of K from each operand row.
+enum : int { KIND_F16 = 0, KIND_F8 = 1, KIND_MXF8 = 2, KIND_MXF4 = 3 };
+
+__host__ __device__ constexpr bool kind_scaled(int kind) { return kind == KIND_MXF8 || kind == KIND_MXF4; }
+
+// D[tmem] (+)= A[smem] · B[smem] with an FP32 accumulator (unscaled kinds).
+template <int CG, int KIND>
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                     uint32_t accumulate)
 {
-    static_assert(EB == 1 || EB == 2, "8-bit or 16-bit operands");
-    if constexpr (CG == 1 && EB == 2)
+    static_assert(KIND == KIND_F16 || KIND == KIND_F8, "unscaled kinds only");
+    if constexpr (CG == 1 && KIND == KIND_F16)
         asm volatile("{\n\t.reg .pred p;\n\t"
                      "setp.ne.b32 p, %4, 0;\n\t"
                      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
                      : "memory");
-    else if constexpr (CG == 2 && EB == 2)
+    else if constexpr (CG == 2 && KIND == KIND_F16)
         asm volatile("{\n\t.reg .pred p;\n\t"
                      "setp.ne.b32 p, %4, 0;\n\t"
                      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
@@ -298,6 +305,58 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b
                      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
                      : "memory");
+}
+
+// Block-scaled MMA: D[tmem] (+)= (SFA ∘ A)·(SFB ∘ B). sfa_tmem / sfb_tmem are
+// the tensor-memory addresses of the 32-bit columns that hold this
+// instruction's E8M0 scales (one byte per row, picked by the scale-ID fields
+// of idesc).
+template <int CG, int KIND>
+__device__ __forceinline__ void mma_scaled(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    static_assert(kind_scaled(KIND), "block-scaled kinds only");
+    if constexpr (CG == 1 && KIND == KIND_MXF8)
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+                     "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+                     : "memory");
+    else if constexpr (CG == 2 && KIND == KIND_MXF8)
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+                     "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+                     : "memory");
+    else if constexpr (CG == 1)
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X "
+                     "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+                     : "memory");
+    else
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "setp.ne.b32 p, %6, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X "
+                     "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+                     : "memory");
+}
+
+// Copy 32 rows x 16 bytes from shared memory (matrix descriptor) into TMEM
+// lanes 0-31 at 4 columns from taddr, replicated into each of the four lane
+// quarters (.warpx4). With cta_group::2 the copy is made in both CTAs of the
+// pair, each from its own shared memory into its own TMEM.
+template <int CG>
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t s_desc)
+{
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+    else
+        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05 operation this thread issued
@@ -357,6 +416,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
     return d;
 }
 
+// Shared-memory matrix descriptor without swizzling: 8-row x 16-byte core
+// matrices, SBO bytes between core matrices along the rows (LBO along K is
+// unused for a single 16-byte column).
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t addr, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;   // layout type 0 (no swizzle) in bits 61-63
+}
+
 // Instruction descriptor for kind::f16 and kind::f8f6f4 with an FP32
 // accumulator: D format bits 4-5 (1 = F32), A format bits 7-9 and B format
 // bits 10-12, A major bit 15 (0 = K), B major bit 16 (1 = MN), N >> 3 in bits
@@ -368,5 +439,19 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t M, uint32_t N, uint32
     return (1u << 4) | (ab_format << 7) | (ab_format << 10) | (b_mn_major << 16) | ((N >> 3) << 17) |
            ((M >> 4) << 24);
 }
+
+// Instruction descriptor for the block-scaled kinds (kind::mxf8f6f4,
+// kind::mxf4): B scale-factor ID bits 4-5, A format bits 7-9, B format bits
+// 10-12, A and B K-major, N >> 3 in bits 17-22, scale type bit 23 (1 = E8M0),
+// M >> 4 in bits 24-28, A scale-factor ID bits 29-30. The scale IDs (the
+// byte of each 32-bit scale column an instruction starts at) are added per
+// instruction: mx_sf_id(). Format codes: mxf8f6f4 E4M3 = 0, E5M2 = 1;
+// mxf4 E2M1 = 1.
+__host__ __device__ constexpr uint32_t make_idesc_mx(uint32_t M, uint32_t N, uint32_t ab_format)
+{
+    return (ab_format << 7) | (ab_format << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t mx_sf_id(uint32_t id) { return (id << 29) | (id << 4); }
 
 } // namespace dtg

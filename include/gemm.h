@@ -38,15 +38,18 @@ extern "C" {
 #endif
 
 /* Element types. F16 and BF16 serve as input or output types, F32 only as an
- * output type, E4M3 and E5M2 only as input types. E4M3 is the OCP 8-bit
- * "FN" format (bias 7, no infinities, largest finite 448); E5M2 is the OCP
- * 8-bit IEEE-style format (bias 15). */
+ * output type, E4M3 and E5M2 only as input types, E2M1 only as the input
+ * type of gemm_mx. E4M3 is the OCP 8-bit "FN" format (bias 7, no
+ * infinities, largest finite 448); E5M2 is the OCP 8-bit IEEE-style format
+ * (bias 15); E2M1 is the OCP 4-bit format (bias 1, largest 6), stored two per
+ * byte, the lower K index in the low nibble, each row padded to whole bytes. */
 typedef enum {
     GEMM_F16 = 0,
     GEMM_BF16 = 1,
     GEMM_F32 = 2,
     GEMM_E4M3 = 3,
-    GEMM_E5M2 = 4
+    GEMM_E5M2 = 4,
+    GEMM_E2M1 = 5
 } gemm_dtype_t;
 
 typedef enum {
@@ -110,7 +113,36 @@ gemm_status_t gemm(const void *A, const void *B, void *C,
                    void *stream);
 
 /*
- * gemm_options_t: overrides for gemm_ex. A zero field means the library
+ * gemm_mx: block-scaled (MX) C = (SFA ∘ A)·(SFB ∘ B) on the current device.
+ *
+ * The MXFP8 and MXFP4 GEMMs of "Two Waves, One Stage Apart" (section "MI450",
+ * Table 1), in the OCP Microscaling form: every run of 32 consecutive K
+ * elements of a row of A, and of a column of B, shares one E8M0 scale
+ * 2^(e-127); the product accumulates in FP32 and is cast on store.
+ *
+ *   A, B      device pointers. A is M x K, B is N x K (layoutB must be
+ *             GEMM_K_MAJOR; GEMM_MN_MAJOR gives GEMM_ERR_UNSUPPORTED).
+ *             Elements are dtype_in: GEMM_E4M3 or GEMM_E5M2 (MXFP8, one byte
+ *             each, row pitch K bytes) or GEMM_E2M1 (MXFP4, packed, row pitch
+ *             ceil(K/2) bytes).
+ *   SFA, SFB  device pointers to the E8M0 scale exponents, one byte per 32 K:
+ *             SFA is M x ceil(K/32) bytes, SFB is N x ceil(K/32) bytes, both
+ *             row-major and densely packed. NULL gives GEMM_ERR_INVALID_ARG.
+ *             The value 0xFF (NaN) is not handled specially.
+ *   C, M, N, K, dtype_out, layoutA, stream: as for gemm.
+ *
+ * The call first repacks the scales into the kernel's per-stage layout, in
+ * stream-ordered scratch (cudaMallocAsync / cudaFreeAsync on `stream`,
+ * (M + N) x ceil(K / stage K) x 16 bytes), and re-pitches A or B like gemm
+ * when their row pitch is not a multiple of 16 bytes. Tiles are 256 x 224,
+ * computed by CTA pairs. Errors as for gemm.
+ */
+gemm_status_t gemm_mx(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C,
+                      int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA,
+                      int layoutB, void *stream);
+
+/*
+ * gemm_options_t: overrides for gemm_ex and gemm_mx_ex. A zero field means the library
  * chooses that value.
  *   cta_group     1: each output tile is 128 x block_n and one CTA owns it.
  *                 2: tiles are 256 x block_n, and a cluster of two CTAs
@@ -148,6 +180,12 @@ gemm_status_t gemm_ex(const void *A, const void *B, void *C,
                       int64_t M, int64_t N, int64_t K,
                       int dtype_in, int dtype_out, int layoutA, int layoutB,
                       const gemm_options_t *opts, void *stream);
+
+/* gemm_mx with overrides (cta_group must be 0 or 2, block_n 0 or 224,
+ * k_stage 0 or the one offered depth: 256 for MXFP8, 256 for MXFP4). */
+gemm_status_t gemm_mx_ex(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C,
+                         int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA,
+                         int layoutB, const gemm_options_t *opts, void *stream);
 
 /*
  * gemm_plan_t: the launch gemm_ex would make for a problem. Filled by

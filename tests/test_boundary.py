@@ -42,7 +42,7 @@ def test_library_exports_every_declared_function():
 def test_enums_match_header():
     text = header_text()
     for name, val in (("GEMM_F16", 0), ("GEMM_BF16", 1), ("GEMM_F32", 2), ("GEMM_E4M3", 3),
-                      ("GEMM_E5M2", 4), ("GEMM_K_MAJOR", 0),
+                      ("GEMM_E5M2", 4), ("GEMM_E2M1", 5), ("GEMM_K_MAJOR", 0),
                       ("GEMM_MN_MAJOR", 1), ("GEMM_OK", 0), ("GEMM_ERR_INVALID_ARG", 1),
                       ("GEMM_ERR_UNSUPPORTED", 2), ("GEMM_ERR_CUDA", 3), ("GEMM_ERR_TIMEOUT", 4),
                       ("GEMM_ERR_NO_DEVICE", 5), ("GEMM_ERR_OUT_OF_MEMORY", 6)):
@@ -74,6 +74,7 @@ def call(M=64, N=64, K=64, din=0, dout=0, la=0, lb=0, a=FAKE, b=FAKE, c=FAKE):
     (dict(dout=3), 2), (dict(dout=4), 2),                      # FP8 is an input type only
     (dict(din=3, lb=1), 2), (dict(din=4, lb=1), 2),            # FP8 B must be K-major
     (dict(din=3, lb=2), 1),
+    (dict(din=5), 2),                                          # packed FP4 only through gemm_mx
 ])
 def test_invalid_arguments_rejected_on_host(kwargs, expect):
     assert call(**kwargs) == expect
@@ -106,6 +107,32 @@ def test_python_wrapper_accepts_fp8_types():
         dtg.gemm(A, torch.zeros(5, 8, dtype=torch.float8_e4m3fn))   # CPU tensors, not a type error
     with pytest.raises(TypeError):
         dtg.gemm_from_host(A, torch.zeros(5, 8, dtype=torch.float8_e5m2))   # mixed FP8 types
+
+
+def mx_call(din=3, dout=1, lb=0, sfa=FAKE, sfb=FAKE, opts=None, M=64, N=64, K=64):
+    if opts is None:
+        return binding.lib.gemm_mx(FAKE, FAKE, sfa, sfb, FAKE, M, N, K, din, dout, 0, lb, None)
+    return binding.lib.gemm_mx_ex(FAKE, FAKE, sfa, sfb, FAKE, M, N, K, din, dout, 0, lb,
+                                  ctypes.byref(opts), None)
+
+
+@pytest.mark.parametrize("kwargs,expect", [
+    (dict(sfa=None), 1), (dict(sfb=None), 1), (dict(din=0), 2), (dict(din=1), 2), (dict(din=2), 2),
+    (dict(din=9), 1), (dict(lb=1), 2), (dict(din=5, lb=1), 2), (dict(dout=3), 2), (dict(K=0), 1),
+])
+def test_gemm_mx_rejects_on_host(kwargs, expect):
+    assert mx_call(**kwargs) == expect
+
+
+def test_gemm_mx_options():
+    o = binding.GemmOptions()
+    o.k_stage = 128          # MXFP8 stages are one or two 128-K slabs: 128 is allowed in validation
+    assert mx_call(opts=o) in (binding.GEMM_ERR_NO_DEVICE, binding.GEMM_ERR_UNSUPPORTED)
+    o.k_stage = 384
+    assert mx_call(opts=o) == binding.GEMM_ERR_UNSUPPORTED
+    o.k_stage = 0
+    o.stream_k = 5
+    assert mx_call(opts=o) == binding.GEMM_ERR_UNSUPPORTED
 
 
 def test_plan_requires_output_struct():
