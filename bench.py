@@ -48,6 +48,32 @@ PAGES_REFERENCE_TFLOPS = 1437.0   # MI355X, 8-wave warp-pipelined Triton, same s
 FALLBACK_BF16_TFLOPS = 1900.0
 NOMINAL_DENSE_TFLOPS = 2250.0     # GB300 dense FP16/BF16 tensor peak, nominal
 FP8_RATE = 2.0                    # nominal dense FP8 / FP16 rate on GB300 (4.5 vs 2.25 PFLOP/s)
+FP4_RATE = 6.0                    # nominal dense FP4 / FP16 rate on GB300 (13.5 vs 2.25 PFLOP/s)
+
+
+def is_mx(w) -> bool:
+    return w.dtype_in in workloads.MX_ELEMENT
+
+
+def rate_of(w) -> float:
+    """Nominal dense tensor rate of the workload's input type, relative to FP16/BF16."""
+    elem = workloads.MX_ELEMENT.get(w.dtype_in, w.dtype_in)
+    return FP4_RATE if elem == "e2m1" else FP8_RATE if elem in workloads.FP8 else 1.0
+
+
+def oracle_operands(w):
+    """The workload's operands as the oracle takes them (raw patterns, and scales for MX)."""
+    ops = workloads.workload_operands(w)
+    return tuple(workloads.as_bits(t) for t in ops)
+
+
+def oracle_rows(oracle, w, ops, rows, threads):
+    if is_mx(w):
+        A, B, SFA, SFB = ops
+        return oracle.gemm_ref_mx(A, B, SFA, SFB, w.M, w.N, w.K, workloads.MX_ELEMENT[w.dtype_in],
+                                  rows=rows, threads=threads)
+    A, B = ops
+    return oracle.gemm_ref(A, B, w.M, w.N, w.K, w.dtype_in, w.layout_b, rows=rows, threads=threads)
 
 
 def parse_args():
@@ -180,24 +206,23 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
-def oracle_sample(w, rows_total: int, threads: int):
+def oracle_sample(w, ops, rows_total: int, threads: int):
     """Time the oracle on `rows_total` output rows of workload w (FP64, host cores)."""
     import oracle
-    A, B = workloads.workload_operands(w)
-    Ab, Bb = workloads.as_bits(A), workloads.as_bits(B)
     rows = list(range(0, w.M, max(1, w.M // rows_total)))[:rows_total]
     t0 = time.perf_counter()
-    oracle.gemm_ref(Ab, Bb, w.M, w.N, w.K, w.dtype_in, w.layout_b, rows=rows, threads=threads)
+    oracle_rows(oracle, w, ops, rows, threads)
     return time.perf_counter() - t0, len(rows)
 
 
 def cpu_baseline(w, target_s: float) -> dict:
     import oracle
     threads = oracle.host_threads()
-    t1, r1 = oracle_sample(w, threads, threads)            # one row per thread: calibration
+    ops = oracle_operands(w)
+    t1, r1 = oracle_sample(w, ops, threads, threads)       # one row per thread: calibration
     rows = max(threads, min(w.M, int(r1 * target_s / max(t1, 1e-3))))
     rows = max(threads, rows // threads * threads)
-    t, r = oracle_sample(w, rows, threads)
+    t, r = oracle_sample(w, ops, rows, threads)
     flops = 2.0 * r * w.N * w.K
     return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{r} of {w.M} output rows (all {w.N} columns, K={w.K}), FP64 i-k-j loop, "
@@ -213,12 +238,10 @@ def run_reference(args):
     import oracle
     w = workloads.WORKLOADS[args.workload]
     threads = oracle.host_threads()
-    A, B = workloads.workload_operands(w)
-    Ab, Bb = workloads.as_bits(A), workloads.as_bits(B)
+    ops = oracle_operands(w)
     # calibrate: one oracle call with one row per thread
     t0 = time.perf_counter()
-    oracle.gemm_ref(Ab, Bb, w.M, w.N, w.K, w.dtype_in, w.layout_b, rows=list(range(threads)),
-                    threads=threads)
+    oracle_rows(oracle, w, ops, list(range(threads)), threads)
     t_cal = time.perf_counter() - t0
     budget = 150.0   # seconds for the whole warm-up + timed run
     per_step = budget / max(1, args.steps + args.warmup)
@@ -226,11 +249,10 @@ def run_reference(args):
     stride = max(1, w.M // rows)
     samples = [list(range((s * 7) % stride, w.M, stride))[:rows] for s in range(args.steps + args.warmup)]
     for s in range(args.warmup):
-        oracle.gemm_ref(Ab, Bb, w.M, w.N, w.K, w.dtype_in, w.layout_b, rows=samples[s], threads=threads)
+        oracle_rows(oracle, w, ops, samples[s], threads)
     t0 = time.perf_counter()
     for s in range(args.steps):
-        oracle.gemm_ref(Ab, Bb, w.M, w.N, w.K, w.dtype_in, w.layout_b,
-                        rows=samples[args.warmup + s], threads=threads)
+        oracle_rows(oracle, w, ops, samples[args.warmup + s], threads)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * w.N * w.K * args.steps
     value = flops / dt / 1e12
@@ -238,7 +260,8 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": value / PAGES_REFERENCE_TFLOPS, "dtype": "f64", "data": "synthetic",
+        "vs_baseline": value / PAGES_REFERENCE_TFLOPS if w.name == workloads.HEADLINE else None,
+        "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "dtype_in": w.dtype_in,
                    "dtype_out": w.dtype_out, "layout_b": w.layout_b,
                    "sample_rows_per_step": rows},
@@ -313,22 +336,23 @@ def run_ours(args):
 
     w = workloads.WORKLOADS[args.workload]
     out_dt = workloads.DTYPES[w.dtype_out]
-    A0, B0 = workloads.workload_operands(w)
+    ops0 = workloads.workload_operands(w)     # (A, B) or, block-scaled, (A, B, SFA, SFB)
+    A0, B0 = ops0[0], ops0[1]
     in_bytes = A0.element_size()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    set_bytes = (A0.numel() + B0.numel()) * in_bytes + w.M * w.N * torch.finfo(out_dt).bits // 8
+    set_bytes = sum(t.numel() * t.element_size() for t in ops0) + w.M * w.N * torch.finfo(out_dt).bits // 8
     n_sets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
-    bits_dt = torch.uint8 if in_bytes == 1 else torch.int16
 
     def rolled(t, i):
         # rotate rows through a same-width integer view (no roll kernel for FP8 types)
+        bits_dt = torch.uint8 if t.element_size() == 1 else torch.int16
         return t.to(dev) if i == 0 else t.to(dev).view(bits_dt).roll(i, 0).view(t.dtype)
 
-    As, Bs, Cs = [], [], []
+    sets, Cs = [], []
     for i in range(n_sets):
-        As.append(rolled(A0, i))
-        Bs.append(rolled(B0, i))
+        sets.append([rolled(t, i) for t in ops0])
         Cs.append(torch.empty((w.M, w.N), dtype=out_dt, device=dev))
+    As, Bs = [st[0] for st in sets], [st[1] for st in sets]
     torch.cuda.synchronize(dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -336,7 +360,11 @@ def run_ours(args):
 
     def step(i):
         j = i % n_sets
-        dtg.gemm(As[j], Bs[j], Cs[j], layout_b=w.layout_b, stream=stream, options=opts)
+        if is_mx(w):
+            A, B, SFA, SFB = sets[j]
+            dtg.gemm_mx(A, B, SFA, SFB, Cs[j], K=w.K, stream=stream, options=opts)
+        else:
+            dtg.gemm(As[j], Bs[j], Cs[j], layout_b=w.layout_b, stream=stream, options=opts)
 
     for i in range(args.warmup):
         step(i)
@@ -381,25 +409,27 @@ def run_ours(args):
 
     peaks, peak_src = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))  # FP16 and BF16 share the dense rate
-    fp8 = w.dtype_in in workloads.FP8
-    nominal = NOMINAL_DENSE_TFLOPS * (FP8_RATE if fp8 else 1.0)
-    if fp8:
-        peak *= FP8_RATE
-        peak_note = (f"{peak_src} bf16_tflops (burst) x {FP8_RATE:g}, the nominal dense "
-                     "FP8/BF16 ratio (4.5 / 2.25 PFLOP/s)")
+    rate = rate_of(w)
+    nominal = NOMINAL_DENSE_TFLOPS * rate
+    if rate != 1.0:
+        peak *= rate
+        peak_note = (f"{peak_src} bf16_tflops (burst) x {rate:g}, the nominal dense ratio of this "
+                     "input type to BF16 (FP8 4.5, FP4 13.5 vs 2.25 PFLOP/s)")
     else:
         peak_note = f"{peak_src} bf16_tflops (burst); FP16 dense rate = BF16"
     achieved = flops_step / (kernel_ms * 1e-3) / 1e12
-    plan = dtg.gemm_plan(w.M, w.N, w.K, dtype_in=workloads.DTYPES[w.dtype_in], dtype_out=out_dt,
+    plan = dtg.gemm_plan(w.M, w.N, w.K, dtype_in=A0.dtype, dtype_out=out_dt,
                          layout_b=w.layout_b, a_ptr=As[0].data_ptr(), b_ptr=Bs[0].data_ptr(),
-                         c_ptr=Cs[0].data_ptr(), options=opts)
+                         c_ptr=Cs[0].data_ptr(), options=opts, block_scaled=is_mx(w))
 
     cublas = None
-    if args.compare_cublas:
+    if args.compare_cublas and not is_mx(w):
         cublas = time_cublas(As, Bs, Cs, w, n_sets, args, stream, smi_id, pg, dev)
+    elif args.compare_cublas:
+        cublas = {"impl": None, "note": "no block-scaled library GEMM is timed for comparison"}
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not is_mx(w):
         Ah = A0.pin_memory()
         Bh = B0.pin_memory()
         Ch = torch.empty((w.M, w.N), dtype=out_dt).pin_memory()

@@ -166,16 +166,17 @@ def gemm_mx(A: torch.Tensor, B: torch.Tensor, SFA: torch.Tensor, SFB: torch.Tens
 
 def gemm_plan(M: int, N: int, K: int, *, dtype_in=torch.float16, dtype_out=torch.float16,
               layout_b: str = "k", a_ptr: int = 256, b_ptr: int = 256, c_ptr: int = 256,
-              options=None, device=None) -> dict:
-    """The launch gemm_ex would make (tile, grid, realign/direct-store paths), as a dict.
-    The pointers only matter for their alignment."""
+              options=None, device=None, block_scaled: bool = False) -> dict:
+    """The launch gemm_ex (or, with block_scaled, gemm_mx_ex) would make: tile, grid,
+    stream-K split, realign/direct-store paths, as a dict. The pointers only matter
+    for their alignment. For block-scaled packed FP4 pass dtype_in=torch.uint8."""
     plan = GemmPlan()
     opts = _options(options)
+    din = GEMM_E2M1 if dtype_in == torch.uint8 else _DT_IN[dtype_in]
+    fn = binding.lib.gemm_mx_plan if block_scaled else binding.lib.gemm_plan
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
-        _check(binding.lib.gemm_plan(M, N, K, _DT_IN[dtype_in], _DT_OUT[dtype_out], GEMM_K_MAJOR,
-                                     _LAYOUT[layout_b], a_ptr, b_ptr, c_ptr,
-                                     ctypes.byref(opts) if opts is not None else None,
-                                     ctypes.byref(plan)), "gemm_plan")
+        _check(fn(M, N, K, din, _DT_OUT[dtype_out], GEMM_K_MAJOR, _LAYOUT[layout_b], a_ptr, b_ptr, c_ptr,
+                  ctypes.byref(opts) if opts is not None else None, ctypes.byref(plan)), "gemm_plan")
     return plan.as_dict()
 
 

@@ -76,6 +76,8 @@ def _declare(lib):
     lib.gemm_plan.restype = c_int
     lib.gemm_plan.argtypes = [i64, i64, i64, c_int, c_int, c_int, c_int, vp, vp, vp,
                               ctypes.POINTER(GemmOptions), ctypes.POINTER(GemmPlan)]
+    lib.gemm_mx_plan.restype = c_int
+    lib.gemm_mx_plan.argtypes = lib.gemm_plan.argtypes
     lib.gemm_from_host.restype = c_int
     lib.gemm_from_host.argtypes = gemm_args + [vp]
     lib.gemm_release_workspace.restype = c_int

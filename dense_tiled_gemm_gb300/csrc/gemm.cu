@@ -722,20 +722,24 @@ gemm_status_t gemm_mx_ex(const void *A, const void *B, const uint8_t *SFA, const
                static_cast<cudaStream_t>(stream));
 }
 
-gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA,
-                        int layoutB, const void *A, const void *B, const void *C,
-                        const gemm_options_t *opts, gemm_plan_t *plan)
+}  // extern "C"
+
+namespace {
+
+gemm_status_t plan_query(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB,
+                         const void *A, const void *B, const void *C, const gemm_options_t *opts, gemm_plan_t *plan,
+                         bool scaled)
 {
     if (!plan)
         return GEMM_ERR_INVALID_ARG;
-    gemm_status_t rc = validate(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, opts);
+    gemm_status_t rc = validate(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, opts, scaled);
     if (rc != GEMM_OK)
         return rc;
     DeviceState *d = nullptr;
     if ((rc = device_state(&d)) != GEMM_OK)
         return rc;
     Plan pl;
-    if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, opts, &pl)) != GEMM_OK)
+    if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, opts, &pl, scaled)) != GEMM_OK)
         return rc;
     const Variant &var = kVariants[pl.variant];
     std::memset(plan, 0, sizeof(*plan));
@@ -756,6 +760,24 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype
     plan->sk_tiles = pl.sk_tiles;
     plan->workspace_bytes = static_cast<int32_t>(pl.ws_bytes);
     return GEMM_OK;
+}
+
+} // namespace
+
+extern "C" {
+
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA,
+                        int layoutB, const void *A, const void *B, const void *C,
+                        const gemm_options_t *opts, gemm_plan_t *plan)
+{
+    return plan_query(M, N, K, dtype_in, dtype_out, layoutA, layoutB, A, B, C, opts, plan, false);
+}
+
+gemm_status_t gemm_mx_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA,
+                           int layoutB, const void *A, const void *B, const void *C,
+                           const gemm_options_t *opts, gemm_plan_t *plan)
+{
+    return plan_query(M, N, K, dtype_in, dtype_out, layoutA, layoutB, A, B, C, opts, plan, true);
 }
 
 gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_host, int64_t M, int64_t N,

@@ -70,11 +70,13 @@ __host__ __device__ constexpr int kind_slab_k(int kind) { return kind == KIND_F1
 // all N columns of the instruction (each CTA of a pair holds all of them), in
 // the byte its descriptor's scale-ID picks. A ring stage carries SF_GROUPS
 // groups of 4 blocks: per group one atom of A and SFB_ATOMS atoms of B (the
-// whole tile width). The MMA thread copies them into one TMEM scale buffer at
-// columns SF_COL0.. before the stage's MMAs (tcgen05.cp and tcgen05.mma of
-// one thread run in issue order, so the next stage's copies cannot overtake
-// this stage's MMAs). Accumulators use columns [0, BN) and [256, 256 + BN),
-// so block-scaled tiles are at most 224 wide.
+// whole tile width). The MMA thread copies them into a TMEM scale buffer
+// before the stage's MMAs; tcgen05.cp and tcgen05.mma of one thread run in
+// issue order. Consecutive stages alternate between two buffers, at columns
+// SF_COL0 and SF_COL0 + 256 (beside each accumulator), so a stage's copies
+// never overwrite scales that the previous stage's MMAs may still read and
+// the tensor pipe does not drain between stages. Accumulators use columns
+// [0, BN) and [256, 256 + BN), so block-scaled tiles are at most 224 wide.
 constexpr int SF_ATOM_BYTES = 512;
 constexpr int SF_ATOM_ROWS = 32;
 constexpr int SF_ROW_BYTES = 16;
@@ -148,7 +150,8 @@ struct TileConfig {
     static constexpr int SFB_BYTES = SF_GROUPS * SFB_ATOMS * SF_ATOM_BYTES;
     static constexpr int STAGE_BYTES = AB_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int STAGE_TX = STAGE_BYTES;   // bytes the TMA engine delivers per stage and CTA
-    // TMEM scale buffer: A at SF_COL0 + 4g, B at SF_COL0 + 4 * SF_GROUPS + 4 * (g * SFB_ATOMS + atom)
+    // TMEM scale buffer (at SF_COL0, or SF_COL0 + 256 for odd stages): A at +4g,
+    // B at +4 * SF_GROUPS + 4 * (g * SFB_ATOMS + atom)
     static constexpr uint32_t SFB_COL = SF_COL0 + 4u * SF_GROUPS;
     static_assert(!SCALED || (SF_GROUPS >= 1 && SFB_COL + 4u * SF_GROUPS * SFB_ATOMS <= 256u),
                   "the TMEM scale buffer fits between the two accumulators");
@@ -540,7 +543,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
             // 1024 B apart (SBO); one K=16 step = 16 rows = 2048 B.
             const uint32_t b_lbo = b_mn ? 8192u : 16u;
             const uint32_t b_step = b_mn ? (2048u >> 4) : (32u >> 4);
-            uint32_t s = 0, ph = 0, acc = 0, acc_ph = 0;
+            uint32_t s = 0, ph = 0, acc = 0, acc_ph = 0, sf_sel = 0;
             for (int i = 0; i < num_jobs; ++i) {
                 const Job jb = sch.job(i);
                 wait_bounded<CG == 2>(w, tempty_bar(acc), acc_ph ^ 1u, SITE_MMA_TMEM_EMPTY);
@@ -551,7 +554,9 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     tc_fence_after_sync();
                     if (!w.aborted) {
                         const uint32_t a_addr = base + s * Cfg::STAGE_BYTES;
-                        const uint32_t sf_a = tmem_base + SF_COL0, sf_b = tmem_base + Cfg::SFB_COL;
+                        const uint32_t sf_a = tmem_base + SF_COL0 + 256u * sf_sel;
+                        const uint32_t sf_b = sf_a + (Cfg::SFB_COL - SF_COL0);
+                        sf_sel ^= 1u;
                         if constexpr (Cfg::SCALED) {
                             // this stage's scale atoms into TMEM, in smem order (A's, then B's);
                             // later MMAs of this thread see them

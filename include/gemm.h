@@ -217,6 +217,14 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K,
                         const void *A, const void *B, const void *C,
                         const gemm_options_t *opts, gemm_plan_t *plan);
 
+/* gemm_plan for the block-scaled product of gemm_mx_ex (same arguments; the
+ * scale pointers do not affect the plan). workspace_bytes counts the
+ * stream-K partial sums only, not the repacked scales. */
+gemm_status_t gemm_mx_plan(int64_t M, int64_t N, int64_t K,
+                           int dtype_in, int dtype_out, int layoutA, int layoutB,
+                           const void *A, const void *B, const void *C,
+                           const gemm_options_t *opts, gemm_plan_t *plan);
+
 /*
  * gemm_from_host: C = A·B with A, B and C in HOST memory (pinned or
  * pageable). It copies A and B to a device workspace, runs gemm on `stream`,
