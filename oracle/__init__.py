@@ -31,6 +31,8 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_oracle.c")
+_ATT_SRC = os.path.join(_HERE, "attention_oracle.c")
+SOURCES = (_SRC, _ATT_SRC)
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -45,15 +47,19 @@ _STORAGE = {"f16": np.uint16, "bf16": np.uint16, "e4m3": np.uint8, "e5m2": np.ui
 _LAYOUT = {"k": K_MAJOR, "mn": MN_MAJOR}
 
 
+def compile_cmd(out: str, sources=SOURCES) -> list[str]:
+    return ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math",
+            "-fPIC", "-shared", "-pthread", "-D_POSIX_C_SOURCE=200809L",
+            "-o", out, *sources, "-lm"]
+
+
 def build(force: bool = False) -> str:
-    """Compile gemm_oracle.c with gcc into liboracle.so (next to the source)."""
+    """Compile the oracle sources with gcc into liboracle.so (next to them)."""
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(p) for p in SOURCES)):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math",
-           "-fPIC", "-shared", "-pthread", "-D_POSIX_C_SOURCE=200809L",
-           "-o", tmp, _SRC, "-lm"]
+    cmd = compile_cmd(tmp)
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -74,6 +80,10 @@ def load_library(path: str):
                  "oracle_decode_e8m0"):
         getattr(lib, name).restype = ctypes.c_double
         getattr(lib, name).argtypes = [ctypes.c_uint8]
+    lib.oracle_attention.restype = ctypes.c_int
+    lib.oracle_attention.argtypes = [u16p, u16p, u16p, i64, i64, i64, i64, i64, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_double, ctypes.c_void_p, i64, dp, dp,
+                                     dp, ctypes.c_int]
     lib.oracle_gemm_mx.restype = ctypes.c_int
     lib.oracle_gemm_mx.argtypes = [u16p, u16p, u16p, u16p, i64, i64, i64, ctypes.c_int,
                                    ctypes.c_void_p, i64, dp, dp, ctypes.c_int]
@@ -182,3 +192,39 @@ def gemm_ref_mx(A_bits: np.ndarray, B_bits: np.ndarray, SFA: np.ndarray, SFB: np
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_mx failed with code {rc}")
     return C, C_abs
+
+
+def attention_ref(Q_bits, K_bits, V_bits, B: int, H: int, Lq: int, Lk: int, d: int, dtype: str,
+                  causal: bool = False, scale: float | None = None, rows=None,
+                  threads: int | None = None, lib=None):
+    """FP64 attention forward rows: (O, O_abs, LSE) for the flat query rows
+    r = (b*H + h)*Lq + i (None = all). Q_bits is [B][H][Lq][d], K_bits and
+    V_bits [B][H][Lk][d], uint16 FP16/BF16 patterns. scale defaults to 1/sqrt(d).
+    Follows "Two Waves, One Stage Apart", section "Beyond GEMM: FlashAttention"."""
+    lib = lib or _load()
+    Q = np.ascontiguousarray(Q_bits, dtype=np.uint16)
+    K = np.ascontiguousarray(K_bits, dtype=np.uint16)
+    V = np.ascontiguousarray(V_bits, dtype=np.uint16)
+    if Q.size != B * H * Lq * d or K.size != B * H * Lk * d or V.size != B * H * Lk * d:
+        raise ValueError("operand sizes do not match B, H, Lq, Lk, d")
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    if rows is None:
+        n_rows, rows_ptr = B * H * Lq, None
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n_rows = int(rows_arr.size)
+        rows_ptr = rows_arr.ctypes.data_as(ctypes.c_void_p)
+    O = np.empty((n_rows, d), dtype=np.float64)
+    O_abs = np.empty((n_rows, d), dtype=np.float64)
+    LSE = np.empty((n_rows,), dtype=np.float64)
+    if n_rows == 0:
+        return O, O_abs, LSE
+    dp = ctypes.POINTER(ctypes.c_double)
+    vp = ctypes.c_void_p
+    rc = lib.oracle_attention(Q.ctypes.data_as(vp), K.ctypes.data_as(vp), V.ctypes.data_as(vp),
+                              B, H, Lq, Lk, d, _DTYPE[dtype], int(bool(causal)), scale, rows_ptr,
+                              n_rows, O.ctypes.data_as(dp), O_abs.ctypes.data_as(dp),
+                              LSE.ctypes.data_as(dp), int(threads or host_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attention failed with code {rc}")
+    return O, O_abs, LSE

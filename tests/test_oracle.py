@@ -541,9 +541,7 @@ def test_planted_mistakes(name, tmp_path):
     path = tmp_path / "mutant.c"
     path.write_text(src.replace(old, new))
     so = tmp_path / "libmutant.so"
-    subprocess.run(["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
-                    "-pthread", "-D_POSIX_C_SOURCE=200809L", "-o", str(so), str(path), "-lm"],
-                   check=True)
+    subprocess.run(oracle.compile_cmd(str(so), (str(path), oracle._ATT_SRC)), check=True)
     # The battery runs in a child process: a mutant that reads out of bounds may
     # crash, and a crash counts as a caught mistake.
     here = os.path.dirname(os.path.abspath(__file__))
