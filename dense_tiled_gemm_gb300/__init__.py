@@ -18,7 +18,7 @@ from .binding import (GEMM_BF16, GEMM_E2M1, GEMM_E4M3, GEMM_E5M2, GEMM_F16, GEMM
                       GEMM_MN_MAJOR, GEMM_OK, GEMM_ERR_TIMEOUT, GEMM_JOB_FULL, GEMM_JOB_OWNER,
                       GEMM_JOB_WRITER, GemmError, GemmJob, GemmOptions, GemmPlan, STATUS_NAMES)
 
-__all__ = ["gemm", "gemm_ex", "gemm_mx", "gemm_plan", "gemm_from_host", "gemm_release_workspace",
+__all__ = ["gemm", "gemm_ex", "gemm_mx", "attention", "gemm_plan", "gemm_from_host", "gemm_release_workspace",
            "gemm_last_device_status", "gemm_selftest_wait_timeout", "gemm_status_string",
            "gemm_launch_count", "gemm_schedule_jobs", "GemmError", "GemmOptions", "GemmPlan"]
 
@@ -162,6 +162,39 @@ def gemm_mx(A: torch.Tensor, B: torch.Tensor, SFA: torch.Tensor, SFB: torch.Tens
         else:
             _check(binding.lib.gemm_mx_ex(*args, ctypes.byref(opts), _stream_ptr(stream)), "gemm_mx_ex")
     return C
+
+
+def attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool = False,
+              scale: float | None = None, O: torch.Tensor | None = None, return_lse: bool = False,
+              stream=None):
+    """O = softmax(scale * Q K^T) V per (batch, head) on Q's CUDA device (attention_fwd).
+
+    Q: (B, H, Lq, 128), K and V: (B, H, Lk, 128), float16 or bfloat16, contiguous.
+    ``causal``: key k is visible to row i iff k <= i + (Lk - Lq). ``scale`` defaults to
+    1/sqrt(128). Returns O (B, H, Lq, 128), and with ``return_lse`` also the FP32 row
+    log-sum-exp (B, H, Lq).
+    """
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        if t.device.type != "cuda" or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor")
+        if t.dtype not in (torch.float16, torch.bfloat16) or t.dtype != Q.dtype:
+            raise TypeError("Q, K and V must share one dtype, float16 or bfloat16")
+    B, H, Lq, d = Q.shape
+    if tuple(K.shape[:2]) != (B, H) or K.shape[3] != d or V.shape != K.shape:
+        raise ValueError("K and V must be (B, H, Lk, d) with Q's B, H and d")
+    Lk = K.shape[2]
+    if O is None:
+        O = torch.empty_like(Q)
+    if O.shape != Q.shape or O.dtype != Q.dtype or not O.is_contiguous():
+        raise ValueError("O must be a contiguous tensor shaped and typed like Q")
+    lse = torch.empty((B, H, Lq), dtype=torch.float32, device=Q.device) if return_lse else None
+    scale = float(d) ** -0.5 if scale is None else float(scale)
+    with torch.cuda.device(Q.device):
+        _check(binding.lib.attention_fwd(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                                         lse.data_ptr() if lse is not None else None, B, H, Lq, Lk, d,
+                                         _DT_IN[Q.dtype], int(bool(causal)), scale, _stream_ptr(stream)),
+               "attention_fwd")
+    return (O, lse) if return_lse else O
 
 
 def gemm_plan(M: int, N: int, K: int, *, dtype_in=torch.float16, dtype_out=torch.float16,

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB_PATH = os.path.join(HERE, "libdtgemm.so")
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = [os.path.join(HERE, "csrc", "gemm.cu")]
+SOURCES = [os.path.join(HERE, "csrc", "gemm.cu"), os.path.join(HERE, "csrc", "attention.cu")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -1,0 +1,405 @@
+// attention_kernel.cuh: attention forward, O = softmax(scale * Q K^T) V, for sm_103a.
+//
+// "Two Waves, One Stage Apart" (section "Beyond GEMM: FlashAttention")
+// describes the FlashAttention inner loop: QK and PV products alternate with
+// an online softmax over key/value blocks, and the QK product of block i+1
+// runs while the PV product of block i consumes its probabilities. Here the
+// same overlap comes from warp roles and two score buffers in tensor memory:
+//
+//   warp 0     producer: one thread loads the CTA's Q tile once, then K and V
+//              blocks into two-slot rings (TMA, 128-byte swizzle);
+//   warp 1     MMA issuer: S_{j+1} = Q K_{j+1}^T into score buffer (j+1) % 2,
+//              then O += P_j V_j into the output accumulator; owns TMEM;
+//   warps 2-5  softmax: one query row per thread. Read S_j, keep the running
+//              row maximum m and sum l (base-2 exponent), write P_j =
+//              exp2(s - m) in the input type to shared memory in the MMA's
+//              operand layout, rescale O by exp2(m_old - m_new) when the
+//              maximum grows, and at the end divide by l and store O and the
+//              row log-sum-exp.
+//
+// One CTA covers 128 query rows of one (batch, head); blocks are 128 keys;
+// the head dimension is 128. TMEM: score buffers at columns 0 and 128, the
+// FP32 output accumulator at 256. Masked keys (past Lk, or after the causal
+// diagonal, which is aligned to the last query row) score -inf. Every wait
+// is bounded as in the GEMM kernel: past the limit a thread records the site
+// and stops issuing work and signals.
+#pragma once
+
+#include "gemm_kernel.cuh"
+
+namespace dtg {
+
+constexpr int ATT_BM = 128;                       // query rows per CTA
+constexpr int ATT_BN = 128;                       // keys per block
+constexpr int ATT_D = 128;                        // head dimension
+constexpr int ATT_TILE = ATT_BM * ATT_D * 2;      // 32 KB: one Q, K, V or P tile
+constexpr int ATT_SLAB = ATT_TILE / 2;            // 64 columns of 16-bit data, 128-byte rows
+constexpr int ATT_STAGES = 2;                     // K and V ring slots
+constexpr uint32_t ATT_TMEM_COLS = 512;
+constexpr uint32_t ATT_O_COL = 256;
+constexpr int ATT_THREADS = 192;
+
+// shared memory: Q | K[2] | V[2] | P | barriers | TMEM address
+constexpr uint32_t ATT_Q_OFF = 0;
+constexpr uint32_t ATT_K_OFF = ATT_TILE;
+constexpr uint32_t ATT_V_OFF = ATT_K_OFF + ATT_STAGES * ATT_TILE;
+constexpr uint32_t ATT_P_OFF = ATT_V_OFF + ATT_STAGES * ATT_TILE;
+constexpr uint32_t ATT_BAR_OFF = ATT_P_OFF + ATT_TILE;
+constexpr uint32_t ATT_NUM_BARS = 16;
+constexpr uint32_t ATT_SMEM = ATT_BAR_OFF + ATT_NUM_BARS * 8 + 16;
+
+enum : uint32_t {
+    SITE_ATT_Q = 0x410,
+    SITE_ATT_K_EMPTY = 0x411,
+    SITE_ATT_V_EMPTY = 0x412,
+    SITE_ATT_K_FULL = 0x413,
+    SITE_ATT_S_EMPTY = 0x414,
+    SITE_ATT_P_FULL = 0x415,
+    SITE_ATT_V_FULL = 0x416,
+    SITE_ATT_S_FULL = 0x417,
+    SITE_ATT_O_READY = 0x418,
+    SITE_ATT_DRAIN = 0x419,
+    SITE_ATT_DONE = 0x41A,
+};
+
+struct AttParams {
+    int32_t Lq, Lk;
+    uint32_t causal;
+    uint32_t bf16;             // operand and output type: 1 BF16, 0 FP16
+    float scale_log2;          // score scale times log2(e)
+    uint32_t idesc_qk, idesc_pv;
+    void *O;                   // [B][H][Lq][128], the operand type
+    float *LSE;                // [B][H][Lq] natural-log row log-sum-exp, or null
+    uint64_t timeout_ns;
+    unsigned long long launch_id;
+    unsigned long long *status;
+};
+
+// KV blocks a query tile needs: all ceil(Lk / 128), or, when causal, those up
+// to the block holding the last key its last row may see.
+__host__ __device__ inline int att_num_blocks(int q0, int Lq, int Lk, bool causal)
+{
+    int n = (Lk + ATT_BN - 1) / ATT_BN;
+    if (causal) {
+        const int last_row = min(q0 + ATT_BM, Lq) - 1;
+        const int last_key = last_row + (Lk - Lq);
+        n = last_key < 0 ? 0 : min(n, last_key / ATT_BN + 1);
+    }
+    return n;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b, bool bf16, float &ra, float &rb)
+{
+    if (bf16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        ra = __bfloat162float(v.x);
+        rb = __bfloat162float(v.y);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+    __half2 v = __floats2half2_rn(a, b);
+    ra = __half2float(v.x);
+    rb = __half2float(v.y);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__global__ void __launch_bounds__(ATT_THREADS, 1)
+attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const AttParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = smem_u32(smem_raw);
+    if (base & 1023u) {
+        if (threadIdx.x == 0)
+            record_timeout(p.status, p.launch_id, SITE_SMEM_ALIGN);
+        return;
+    }
+    const uint32_t warp = threadIdx.x / 32u, lane = threadIdx.x % 32u;
+    const int q_tile = static_cast<int>(blockIdx.x), bh = static_cast<int>(blockIdx.y);
+    const int q0 = q_tile * ATT_BM;
+    const int nkv = att_num_blocks(q0, p.Lq, p.Lk, p.causal != 0);
+
+    const uint32_t bar0 = base + ATT_BAR_OFF;
+    const uint32_t q_full = bar0;
+    auto k_full = [&](uint32_t s) { return bar0 + 8u * (1 + s); };
+    auto k_empty = [&](uint32_t s) { return bar0 + 8u * (3 + s); };
+    auto v_full = [&](uint32_t s) { return bar0 + 8u * (5 + s); };
+    auto v_empty = [&](uint32_t s) { return bar0 + 8u * (7 + s); };
+    auto s_full = [&](uint32_t b) { return bar0 + 8u * (9 + b); };
+    auto s_empty = [&](uint32_t b) { return bar0 + 8u * (11 + b); };
+    const uint32_t p_full = bar0 + 8u * 13, o_ready = bar0 + 8u * 14, done_bar = bar0 + 8u * 15;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem_raw + ATT_BAR_OFF + ATT_NUM_BARS * 8);
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (uint32_t s = 0; s < ATT_STAGES; ++s) {
+            mbar_init(k_full(s), 1);
+            mbar_init(k_empty(s), 1);
+            mbar_init(v_full(s), 1);
+            mbar_init(v_empty(s), 1);
+        }
+        for (uint32_t b = 0; b < 2; ++b) {
+            mbar_init(s_full(b), 1);    // one tcgen05.commit
+            mbar_init(s_empty(b), 4);   // every softmax warp
+        }
+        mbar_init(p_full, 4);
+        mbar_init(o_ready, 1);
+        mbar_init(done_bar, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(smem_u32(tmem_holder), ATT_TMEM_COLS);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_holder);
+    grid_dependency_wait();
+    grid_launch_dependents();
+
+    WaitCtx w{p.timeout_ns, p.launch_id, p.status, false};
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && nkv > 0) {
+            prefetch_tensor_map(&tmap_q);
+            prefetch_tensor_map(&tmap_k);
+            prefetch_tensor_map(&tmap_v);
+            mbar_arrive_expect_tx(q_full, ATT_TILE);
+            tma_load_3d(base + ATT_Q_OFF, &tmap_q, q_full, 0, q0, bh);
+            tma_load_3d(base + ATT_Q_OFF + ATT_SLAB, &tmap_q, q_full, 64, q0, bh);
+            uint32_t k_pend = 0, v_pend = 0, k_par = 0, v_par = 0;
+            for (int j = 0; j < nkv; ++j) {
+                const uint32_t s = j % ATT_STAGES, ph = (j / ATT_STAGES) & 1;
+                const int key0 = j * ATT_BN;
+                wait_bounded<false>(w, k_empty(s), ph ^ 1u, SITE_ATT_K_EMPTY);
+                if (!w.aborted) {
+                    const uint32_t dst = base + ATT_K_OFF + s * ATT_TILE;
+                    mbar_arrive_expect_tx(k_full(s), ATT_TILE);
+                    tma_load_3d(dst, &tmap_k, k_full(s), 0, key0, bh);
+                    tma_load_3d(dst + ATT_SLAB, &tmap_k, k_full(s), 64, key0, bh);
+                    k_pend |= 1u << s;
+                    k_par = (k_par & ~(1u << s)) | (ph << s);
+                }
+                wait_bounded<false>(w, v_empty(s), ph ^ 1u, SITE_ATT_V_EMPTY);
+                if (!w.aborted) {
+                    // V serves as an N-contiguous B operand: per 64-key slab, two 64-wide d atoms
+                    const uint32_t dst = base + ATT_V_OFF + s * ATT_TILE;
+                    mbar_arrive_expect_tx(v_full(s), ATT_TILE);
+                    for (int ks = 0; ks < 2; ++ks)
+                        for (int na = 0; na < 2; ++na)
+                            tma_load_3d(dst + ks * ATT_SLAB + na * 8192u, &tmap_v, v_full(s), 64 * na,
+                                        key0 + 64 * ks, bh);
+                    v_pend |= 1u << s;
+                    v_par = (v_par & ~(1u << s)) | (ph << s);
+                }
+            }
+            // leave no bulk copy in flight
+            wait_drain<false>(q_full, 0, w.limit_ns, w.id, w.status, SITE_ATT_DRAIN);
+            for (uint32_t s = 0; s < ATT_STAGES; ++s) {
+                if ((k_pend >> s) & 1u)
+                    wait_drain<false>(k_full(s), (k_par >> s) & 1u, w.limit_ns, w.id, w.status, SITE_ATT_DRAIN);
+                if ((v_pend >> s) & 1u)
+                    wait_drain<false>(v_full(s), (v_par >> s) & 1u, w.limit_ns, w.id, w.status, SITE_ATT_DRAIN);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && nkv > 0) {
+            wait_bounded<false>(w, q_full, 0, SITE_ATT_Q);
+            tc_fence_after_sync();
+            auto issue_qk = [&](int j) {
+                const uint32_t s = j % ATT_STAGES, ph = (j / ATT_STAGES) & 1;
+                const uint32_t b = j & 1, bph = (j >> 1) & 1;
+                wait_bounded<false>(w, k_full(s), ph, SITE_ATT_K_FULL);
+                wait_bounded<false>(w, s_empty(b), bph ^ 1u, SITE_ATT_S_EMPTY);
+                tc_fence_after_sync();
+                if (w.aborted)
+                    return;
+                const uint32_t d_tmem = tmem_base + b * ATT_BN;
+                const uint32_t k_addr = base + ATT_K_OFF + s * ATT_TILE;
+#pragma unroll
+                for (int slab = 0; slab < 2; ++slab) {
+                    const uint64_t a_desc = smem_desc_sw128(base + ATT_Q_OFF + slab * ATT_SLAB, 16u, 1024u);
+                    const uint64_t b_desc = smem_desc_sw128(k_addr + slab * ATT_SLAB, 16u, 1024u);
+#pragma unroll
+                    for (uint32_t k = 0; k < 4; ++k)
+                        mma<1, KIND_F16>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc_qk,
+                                         (slab > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(s_full(b));
+                mma_commit(k_empty(s));
+            };
+            issue_qk(0);
+            for (int j = 0; j < nkv; ++j) {
+                if (j + 1 < nkv)
+                    issue_qk(j + 1);   // the tensor core computes S_{j+1} while softmax works on S_j
+                const uint32_t s = j % ATT_STAGES, ph = (j / ATT_STAGES) & 1;
+                wait_bounded<false>(w, p_full, j & 1, SITE_ATT_P_FULL);
+                wait_bounded<false>(w, v_full(s), ph, SITE_ATT_V_FULL);
+                tc_fence_after_sync();
+                if (w.aborted)
+                    continue;
+                const uint32_t v_addr = base + ATT_V_OFF + s * ATT_TILE;
+#pragma unroll
+                for (int slab = 0; slab < 2; ++slab) {
+                    const uint64_t a_desc = smem_desc_sw128(base + ATT_P_OFF + slab * ATT_SLAB, 16u, 1024u);
+                    // N-contiguous V: 64-wide d atoms 8192 B apart, 16 keys = 2048 B per MMA
+                    const uint64_t b_desc = smem_desc_sw128(v_addr + slab * ATT_SLAB, 8192u, 1024u);
+#pragma unroll
+                    for (uint32_t k = 0; k < 4; ++k)
+                        mma<1, KIND_F16>(tmem_base + ATT_O_COL, a_desc + 2u * k, b_desc + (2048u >> 4) * k,
+                                         p.idesc_pv, (j > 0 || slab > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(o_ready);
+                mma_commit(v_empty(s));
+            }
+            mma_commit(done_bar);
+            wait_drain<false>(done_bar, 0, w.limit_ns, w.id, w.status, SITE_ATT_DONE);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax and output
+        const uint32_t quarter = warp & 3u;
+        const int r = static_cast<int>(quarter * 32u + lane);   // row within the tile (TMEM lane)
+        const int qrow = q0 + r;
+        const uint32_t t_lane = (quarter * 32u) << 16;
+        const bool bf16 = p.bf16 != 0;
+        float m = -INFINITY, l = 0.0f;
+        for (int j = 0; j < nkv; ++j) {
+            const uint32_t b = j & 1;
+            wait_bounded<false>(w, s_full(b), (j >> 1) & 1, SITE_ATT_S_FULL);
+            bool skip = __any_sync(0xffffffffu, w.aborted);
+            w.aborted = skip;
+            tc_fence_after_sync();
+            float sv[ATT_BN];
+            if (!skip) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tmem_base + t_lane + b * ATT_BN + c * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        sv[c * 32 + i] = __uint_as_float(v[i]);
+                }
+            }
+            // the score buffer is free for S_{j+2}
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0 && !skip)
+                mbar_arrive_local(s_empty(b));
+            // mask, scale (base 2), running maximum
+            const int key0 = j * ATT_BN;
+            const int key_end = p.causal ? min(p.Lk, qrow + (p.Lk - p.Lq) + 1) : p.Lk;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < ATT_BN; ++c) {
+                const float x = (key0 + c < key_end) ? sv[c] * p.scale_log2 : -INFINITY;
+                sv[c] = x;
+                mx = fmaxf(mx, x);
+            }
+            const float m_new = fmaxf(m, mx);
+            const float m_use = m_new == -INFINITY ? 0.0f : m_new;
+            const float alpha = exp2f(m - m_use);   // 0 while no key has been seen
+            // probabilities, rounded to the operand type; l sums the rounded values
+            uint32_t pk[ATT_BN / 2];
+            float rowsum = 0.0f;
+#pragma unroll
+            for (int c = 0; c < ATT_BN / 2; ++c) {
+                float ra, rb;
+                pk[c] = pack_half2(exp2f(sv[2 * c] - m_use), exp2f(sv[2 * c + 1] - m_use), bf16, ra, rb);
+                rowsum += ra + rb;
+            }
+            l = l * alpha + rowsum;
+            m = m_new;
+            // O and the P buffer are free once PV_{j-1} has completed
+            if (j > 0)
+                wait_bounded<false>(w, o_ready, (j - 1) & 1, SITE_ATT_O_READY);
+            skip = __any_sync(0xffffffffu, w.aborted);
+            w.aborted = skip;
+            tc_fence_after_sync();
+            if (!skip) {
+                // P row r, 128-byte swizzle: 16-byte unit u of a 128-byte row at u ^ (r % 8)
+#pragma unroll
+                for (int slab = 0; slab < 2; ++slab) {
+                    const uint32_t row = base + ATT_P_OFF + slab * ATT_SLAB + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int e = slab * 32 + u * 4;   // index into pk (two values per word)
+                        st_shared_v4(row + ((static_cast<uint32_t>(u) ^ (static_cast<uint32_t>(r) & 7u)) << 4),
+                                     pk[e], pk[e + 1], pk[e + 2], pk[e + 3]);
+                    }
+                }
+                // rescale the accumulator when any row of the warp raised its maximum
+                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t v[32];
+                        const uint32_t ta = tmem_base + t_lane + ATT_O_COL + c * 32;
+                        tmem_ld_32x32b_x32(ta, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        tmem_st_32x32b_x32(ta, v);
+                    }
+                    tmem_st_wait();
+                }
+            }
+            fence_proxy_async_smem();   // P is read by the tensor core (async proxy)
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0 && !skip)
+                mbar_arrive_local(p_full);
+        }
+        // ---------------------------------------------------------- output
+        bool skip = false;
+        if (nkv > 0) {
+            wait_bounded<false>(w, o_ready, (nkv - 1) & 1, SITE_ATT_O_READY);
+            skip = __any_sync(0xffffffffu, w.aborted);
+            tc_fence_after_sync();
+        }
+        if (!skip) {
+            const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+            uint8_t *orow = static_cast<uint8_t *>(p.O) + (static_cast<size_t>(bh) * p.Lq + qrow) * ATT_D * 2;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                if (nkv > 0) {
+                    tmem_ld_32x32b_x32(tmem_base + t_lane + ATT_O_COL + c * 32, v);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = 0u;
+                }
+                if (qrow < p.Lq) {
+                    uint32_t o[16];
+                    float ra, rb;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        o[i] = pack_half2(__uint_as_float(v[2 * i]) * inv_l, __uint_as_float(v[2 * i + 1]) * inv_l,
+                                          bf16, ra, rb);
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 64);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                }
+            }
+            if (p.LSE && qrow < p.Lq)
+                p.LSE[static_cast<size_t>(bh) * p.Lq + qrow] =
+                    l > 0.0f ? m * 0.69314718055994531f + logf(l) : -INFINITY;
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc<1>(tmem_base, ATT_TMEM_COLS);
+    }
+}
+
+} // namespace dtg

@@ -19,6 +19,7 @@
 
 #include "gemm.h"
 #include "gemm_kernel.cuh"
+#include "runtime.h"
 
 using namespace dtg;
 
@@ -1027,6 +1028,46 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
 }
 
 } // namespace
+
+// ---------------------------------------------------------------------------
+// Services for the library's other translation units (runtime.h).
+namespace dtg {
+
+gemm_status_t runtime_info(RuntimeInfo *out)
+{
+    DeviceState *d = nullptr;
+    const gemm_status_t rc = device_state(&d);
+    if (rc != GEMM_OK)
+        return rc;
+    out->status = d->status;
+    out->sms = d->sms;
+    return GEMM_OK;
+}
+
+unsigned long long runtime_next_launch_id() { return next_launch_id(); }
+
+void runtime_count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+bool runtime_encode(CUtensorMap *map, CUtensorMapDataType dt, uint32_t rank, const void *base,
+                    const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                    CUtensorMapSwizzle swizzle)
+{
+    if (!g_encode || rank < 1 || rank > 5)
+        return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (uint32_t i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank)
+            st[i] = strides_bytes[i];
+    }
+    return g_encode(map, dt, rank, const_cast<void *>(base), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+} // namespace dtg
 
 extern "C" gemm_status_t gemm_no_alloc(const void *A, const void *B, void *C, int64_t M, int64_t N,
                                        int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB,

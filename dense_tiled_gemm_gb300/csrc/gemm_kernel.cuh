@@ -256,7 +256,7 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t 
 // Wait until *flag == id (another CTA of this launch has published its
 // partial sum). Returns false after a timeout of this or another thread of
 // the launch, recording the site in the first case.
-__device__ __noinline__ bool wait_flag_slow(const unsigned long long *flag, uint64_t limit_ns,
+static __device__ __noinline__ bool wait_flag_slow(const unsigned long long *flag, uint64_t limit_ns,
                                             unsigned long long id, unsigned long long *status, uint32_t site)
 {
     const uint64_t t0 = global_timer_ns();
@@ -749,7 +749,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
 // One CTA waits, through the same bounded wait, on a barrier that nothing
 // arrives at; it must record SITE_SELFTEST and return.
-__global__ void wait_selftest_kernel(uint64_t timeout_ns, unsigned long long launch_id,
+static __global__ void wait_selftest_kernel(uint64_t timeout_ns, unsigned long long launch_id,
                                      unsigned long long *status)
 {
     __shared__ __align__(8) uint64_t bar;
@@ -769,7 +769,7 @@ __global__ void wait_selftest_kernel(uint64_t timeout_ns, unsigned long long lau
 // stage `groups` groups of 4 blocks, each group `atoms` atoms of 128 rows
 // (see SF_ATOM_BYTES). Missing rows and blocks are zero. out has row_blocks x
 // stages x groups x atoms x 32 rows of 16 bytes; each thread writes one row.
-__global__ void pack_scales_kernel(const uint8_t *__restrict__ sf, uint8_t *__restrict__ out, int64_t rows,
+static __global__ void pack_scales_kernel(const uint8_t *__restrict__ sf, uint8_t *__restrict__ out, int64_t rows,
                                    int64_t n_blocks, int R, int64_t row_blocks, int64_t stages, int groups,
                                    int atoms)
 {

@@ -48,3 +48,29 @@ def check(C_gpu, C_ref, C_abs, dtype_out: str):
     ratio = float(np.nanmax(err / lim)) if err.size else 0.0
     first = tuple(int(v) for v in np.argwhere(bad)[0]) if n_bad else None
     return n_bad == 0, ratio, n_bad, first
+
+
+# Attention forward ("Two Waves, One Stage Apart", section "Beyond GEMM:
+# FlashAttention"). The probabilities enter the PV product rounded to the
+# operand type (relative error <= 2^-9 for BF16, 2^-12 for FP16), and the row
+# sum is taken over the rounded values, so the output error is at most about
+# 2^-9 * (O_abs + |O|) <= 2^-8 * O_abs, with O_abs = sum_k p_k |v_k| / l; the
+# FP32 score and output sums add far less. The bound below doubles that. The
+# row log-sum-exp inherits the relative error of l: |dLSE| <= log(1 + 2^-9).
+ATT_REL = 2.0 ** -7
+ATT_LSE_ABS = 2.0 ** -7
+
+
+def attention_bound(O_ref, O_abs, dtype_out: str):
+    return ATT_REL * O_abs + 1e-6 + ulp_out(O_ref, dtype_out)
+
+
+def check_attention(O_gpu, O_ref, O_abs, dtype_out: str):
+    """Elementwise |O_gpu - O_ref| <= attention_bound. Returns (ok, worst ratio, n_bad, first bad)."""
+    O_gpu = np.asarray(O_gpu, dtype=np.float64)
+    err = np.abs(O_gpu - O_ref)
+    lim = attention_bound(O_ref, O_abs, dtype_out)
+    bad = ~(err <= lim)
+    ratio = float(np.max(err / lim)) if err.size else 0.0
+    idx = np.argwhere(bad)
+    return (not bad.any(), ratio, int(bad.sum()), tuple(int(i) for i in idx[0]) if idx.size else None)

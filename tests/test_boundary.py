@@ -12,7 +12,8 @@ import pytest
 from dense_tiled_gemm_gb300 import binding
 import dense_tiled_gemm_gb300 as dtg
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gemm.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADER = os.path.join(INCLUDE, "gemm.h")
 FAKE = 0x10000   # never dereferenced: every call below fails validation first
 
 
@@ -22,15 +23,22 @@ def header_text() -> str:
 
 
 def declared_functions() -> list[str]:
-    text = re.sub(r"/\*.*?\*/", "", header_text(), flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(gemm\w*)\s*\(", text, flags=re.M)))
+    names = set()
+    for name in sorted(os.listdir(INCLUDE)):
+        if name.endswith(".h"):
+            with open(os.path.join(INCLUDE, name)) as fh:
+                text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+            names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*((?:gemm|attention)\w*)\s*\(", text,
+                                    flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for required in ("gemm", "gemm_ex", "gemm_plan", "gemm_from_host", "gemm_last_device_status",
                      "gemm_status_string", "gemm_selftest_wait_timeout", "gemm_launch_count",
-                     "gemm_release_workspace"):
+                     "gemm_release_workspace", "gemm_mx", "gemm_mx_ex", "gemm_mx_plan",
+                     "gemm_schedule_jobs", "gemm_no_alloc", "attention_fwd"):
         assert required in names
 
 
@@ -133,6 +141,27 @@ def test_gemm_mx_options():
     o.k_stage = 0
     o.stream_k = 5
     assert mx_call(opts=o) == binding.GEMM_ERR_UNSUPPORTED
+
+
+def att_call(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, lse=None, B=1, H=1, Lq=128, Lk=128, d=128, dt=1, causal=0,
+             scale=0.088):
+    return binding.lib.attention_fwd(Q, K, V, O, lse, B, H, Lq, Lk, d, dt, causal, scale, None)
+
+
+@pytest.mark.parametrize("kwargs,expect", [
+    (dict(Q=None), 1), (dict(O=None), 1), (dict(B=0), 1), (dict(Lk=0), 1), (dict(dt=7), 1),
+    (dict(dt=2), 2), (dict(d=64), 2), (dict(causal=2), 1), (dict(scale=float("inf")), 1),
+    (dict(B=300, H=300), 2), (dict(Q=FAKE + 8), 2), (dict(lse=FAKE + 2), 1),
+])
+def test_attention_rejects_on_host(kwargs, expect):
+    assert att_call(**kwargs) == expect
+
+
+def test_attention_no_device():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert att_call() == binding.GEMM_ERR_NO_DEVICE
 
 
 def test_plan_requires_output_struct():

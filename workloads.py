@@ -130,21 +130,19 @@ def workload_operands(w: Workload):
     return make_operands(w.M, w.N, w.K, w.dtype_in, w.layout_b, w.dist, w.seed)
 
 
-_E2M1_GRID = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)   # magnitudes of codes 0..7
+# E2M1 codes 0..7 have magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6. Between codes c and
+# c + 1 the midpoint rounds to the even code: up when c is odd, down when c is even.
+_E2M1_MIDPOINTS = ((0.25, False), (0.75, True), (1.25, False), (1.75, True), (2.5, False),
+                   (3.5, True), (5.0, False))   # (midpoint, a tie rounds up)
 
 
 def round_e2m1(x: torch.Tensor) -> torch.Tensor:
-    """FP32 values -> E2M1 codes (uint8, 0..15): nearest grid magnitude, ties to the
-    code with a zero fraction bit (even), saturating at 6; sign in bit 3."""
-    mag = x.abs().clamp(max=6.0)
-    grid = torch.tensor(_E2M1_GRID)
-    dist = (mag[..., None] - grid).abs()
-    best = dist.min(dim=-1, keepdim=True).values
-    tie_ok = dist == best
-    # prefer even codes (fraction bit 0) among the nearest: codes 0, 2, 4, 6
-    even = torch.tensor([c % 2 == 0 for c in range(8)])
-    score = tie_ok.to(torch.int8) * 2 + (tie_ok & even).to(torch.int8)
-    code = score.argmax(dim=-1).to(torch.uint8)
+    """FP32 values -> E2M1 codes (uint8, 0..15): nearest magnitude, ties to the
+    even code, saturating at 6; sign in bit 3 (never on zero)."""
+    mag = x.abs()
+    code = torch.zeros(x.shape, dtype=torch.uint8)
+    for mid, tie_up in _E2M1_MIDPOINTS:
+        code += (mag >= mid if tie_up else mag > mid).to(torch.uint8)
     return code | ((x < 0) & (code != 0)).to(torch.uint8) << 3
 
 
@@ -205,3 +203,50 @@ def sample_rows(M: int, count: int, seed: int, tile: int = 128) -> list[int]:
             break
         rows.add(int(r))
     return sorted(rows)
+
+
+# ---------------------------------------------------------------------------- attention
+@dataclass(frozen=True)
+class AttentionWorkload:
+    """Attention forward O = softmax(scale Q K^T) V over B x H heads."""
+    name: str
+    B: int
+    H: int
+    Lq: int
+    Lk: int
+    d: int
+    dtype: str          # "f16" | "bf16"
+    causal: bool
+    dist: tuple
+    seed: int
+    note: str = field(default="", compare=False)
+
+    @property
+    def flops(self) -> int:
+        """Two products of 2 * Lq * Lk * d per head; a causal mask keeps the visible half."""
+        full = 4 * self.B * self.H * self.Lq * self.Lk * self.d
+        if not self.causal:
+            return full
+        # visible (query, key) pairs: row i sees min(Lk, i + Lk - Lq + 1) keys
+        off = self.Lk - self.Lq
+        seen = sum(max(0, min(self.Lk, i + off + 1)) for i in range(self.Lq))
+        return 4 * self.B * self.H * seen * self.d
+
+
+ATTENTION_WORKLOADS = {w.name: w for w in [
+    AttentionWorkload("attention_4x16x4096x128_bf16", 4, 16, 4096, 4096, 128, "bf16", False,
+                      ("normal", 1.0), 20, "attention forward, long sequence"),
+    AttentionWorkload("attention_4x16x4096x128_bf16_causal", 4, 16, 4096, 4096, 128, "bf16", True,
+                      ("normal", 1.0), 21, "attention forward, causal"),
+]}
+
+
+def make_attention_operands(B: int, H: int, Lq: int, Lk: int, d: int, dtype: str, dist: tuple,
+                            seed: int):
+    """CPU tensors Q (B, H, Lq, d), K and V (B, H, Lk, d), drawn Q, K, V in that order."""
+    gen = torch.Generator().manual_seed(int(seed))
+    dt = DTYPES[dtype]
+    Q = _draw(gen, B * H * Lq * d, dist).to(dt).reshape(B, H, Lq, d)
+    K = _draw(gen, B * H * Lk * d, dist).to(dt).reshape(B, H, Lk, d)
+    V = _draw(gen, B * H * Lk * d, dist).to(dt).reshape(B, H, Lk, d)
+    return Q, K, V
