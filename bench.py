@@ -82,7 +82,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=workloads.HEADLINE,
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.ATTENTION_WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--compare-cublas", action="store_true",
@@ -485,8 +486,138 @@ def run_ours(args):
     return 0
 
 
+# ---------------------------------------------------------------------------- attention
+def run_attention(args):
+    """The attention forward workloads: one step = one attention_fwd call over all
+    B x H heads, rotating (Q, K, V, O) sets larger than 2 x L2; FLOPs = 4 * B * H *
+    (visible query-key pairs) * d, as in the two products of the forward pass."""
+    world, rank, local = dist_env()
+    import dense_tiled_gemm_gb300 as dtg
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    w = workloads.ATTENTION_WORKLOADS[args.workload]
+    Q0, K0, V0 = workloads.make_attention_operands(w.B, w.H, w.Lq, w.Lk, w.d, w.dtype, w.dist, w.seed)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = 2 * (2 * Q0.numel() + K0.numel() + V0.numel())
+    n_sets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+    sets = []
+    for i in range(n_sets):
+        sets.append([t.to(dev).view(torch.int16).roll(i, 2).view(t.dtype) if i else t.to(dev)
+                     for t in (Q0, K0, V0)] + [torch.empty_like(Q0, device=dev)])
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    def step(i):
+        Q, K, V, O = sets[i % n_sets]
+        dtg.attention(Q, K, V, causal=w.causal, O=O, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    status, detail = dtg.gemm_last_device_status(stream)
+    if status != dtg.GEMM_OK:
+        raise RuntimeError(f"device status {dtg.gemm_status_string(status)} site {detail:#x}")
+    try:
+        smi_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:  # noqa: BLE001
+        smi_id = str(local)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(smi_id)
+    sampler.start()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = dtg.gemm_launch_count()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    launches = dtg.gemm_launch_count() - launches0
+    clocks = sampler.stop()
+    status, detail = dtg.gemm_last_device_status(stream)
+    if status != dtg.GEMM_OK:
+        raise RuntimeError(f"device status {dtg.gemm_status_string(status)} site {detail:#x}")
+    region_ms = ev0.elapsed_time(ev1)
+    kernel_ms = region_ms / args.steps
+    region_ms = max_over_ranks(region_ms, pg, dev)
+    value = whole_job_tflops(world, float(w.flops), args.steps, region_ms * 1e-3)
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+
+    comparison = None
+    if args.compare_cublas:
+        # torch's fused attention (its flash / cuDNN kernels), timed the same way; a comparison only
+        import torch.nn.functional as F
+
+        def tstep(i):
+            Q, K, V, _ = sets[i % n_sets]
+            F.scaled_dot_product_attention(Q, K, V, is_causal=w.causal and w.Lq == w.Lk)
+        for i in range(args.warmup):
+            tstep(i)
+        sampler = ClockSampler(smi_id)
+        sampler.start()
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for i in range(args.steps):
+            tstep(i)
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        tclk = sampler.stop()
+        t_ms = ev0.elapsed_time(ev1) / args.steps
+        comparison = {"impl": "torch.nn.functional.scaled_dot_product_attention", "kernel_ms": t_ms,
+                      "value": w.flops / (t_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "clocks": tclk}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.host_threads()
+        bits = [t.contiguous().view(torch.int16).numpy() for t in (Q0, K0, V0)]
+        total = w.B * w.H * w.Lq
+        n = threads * 4
+        t0 = time.perf_counter()
+        oracle.attention_ref(*bits, w.B, w.H, w.Lq, w.Lk, w.d, w.dtype, w.causal,
+                             rows=list(range(0, total, max(1, total // n)))[:n], threads=threads)
+        dt = time.perf_counter() - t0
+        per_row = w.flops / total
+        cpu = {"value": n * per_row / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{n} of {total} query rows, FP64 plain softmax(QK^T)V", "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "accumulate": "f32",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d,
+                       "causal": w.causal, "flops_per_step": w.flops,
+                       "l2": f"rotating {n_sets} (Q, K, V, O) sets", "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16_tflops (burst)", "kernel_ms": kernel_ms,
+                         "frac_of_nominal": achieved / NOMINAL_DENSE_TFLOPS},
+            "clocks": clocks, "gpu_launches": launches, "e2e": None, "cpu_baseline": cpu,
+            "library_comparison": comparison,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.workload in workloads.ATTENTION_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the GEMM workloads"}))
+            return 0
+        return run_attention(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

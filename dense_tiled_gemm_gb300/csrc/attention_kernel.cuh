@@ -13,9 +13,11 @@
 //   warps 2-5  softmax: one query row per thread. Read S_j, keep the running
 //              row maximum m and sum l (base-2 exponent), write P_j =
 //              exp2(s - m) in the input type to shared memory in the MMA's
-//              operand layout, rescale O by exp2(m_old - m_new) when the
-//              maximum grows, and at the end divide by l and store O and the
-//              row log-sum-exp.
+//              operand layout, and at the end divide by l and store O and the
+//              row log-sum-exp. The maximum used for P is raised (and O and l
+//              rescaled by exp2(m_old - m_new)) only when a row's maximum
+//              grows by more than RESCALE_LOG2 = 8: until then P <= 2^8, which
+//              the operand types hold, and O, l stay consistently scaled.
 //
 // One CTA covers 128 query rows of one (batch, head); blocks are 128 keys;
 // the head dimension is 128. TMEM: score buffers at columns 0 and 128, the
@@ -38,6 +40,7 @@ constexpr int ATT_STAGES = 2;                     // K and V ring slots
 constexpr uint32_t ATT_TMEM_COLS = 512;
 constexpr uint32_t ATT_O_COL = 256;
 constexpr int ATT_THREADS = 192;
+constexpr float RESCALE_LOG2 = 8.0f;              // lazy rescaling threshold (base-2 exponent)
 
 // shared memory: Q | K[2] | V[2] | P | barriers | TMEM address
 constexpr uint32_t ATT_Q_OFF = 0;
@@ -86,6 +89,14 @@ __host__ __device__ inline int att_num_blocks(int q0, int Lq, int Lk, bool causa
         n = last_key < 0 ? 0 : min(n, last_key / ATT_BN + 1);
     }
     return n;
+}
+
+// 2^x by the PTX ex2 instruction (approximate, flushes subnormals; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b, bool bf16, float &ra, float &rb)
@@ -273,15 +284,16 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             tc_fence_after_sync();
             float sv[ATT_BN];
             if (!skip) {
+                uint32_t v[4][32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(tmem_base + t_lane + b * ATT_BN + c * 32, v);
-                    tmem_ld_wait();
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld_32x32b_x32(tmem_base + t_lane + b * ATT_BN + c * 32, v[c]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        sv[c * 32 + i] = __uint_as_float(v[i]);
-                }
+                        sv[c * 32 + i] = __uint_as_float(v[c][i]);
             }
             // the score buffer is free for S_{j+2}
             tc_fence_before_sync();
@@ -298,16 +310,19 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 sv[c] = x;
                 mx = fmaxf(mx, x);
             }
-            const float m_new = fmaxf(m, mx);
+            // raise the maximum only when some row of the warp outgrew it by more
+            // than the threshold (always on the first block with a visible key)
+            const bool raise = __any_sync(0xffffffffu, mx > m + RESCALE_LOG2);
+            const float m_new = raise ? fmaxf(m, mx) : m;
             const float m_use = m_new == -INFINITY ? 0.0f : m_new;
-            const float alpha = exp2f(m - m_use);   // 0 while no key has been seen
+            const float alpha = raise ? ex2(m - m_use) : 1.0f;   // 0 while no key has been seen
             // probabilities, rounded to the operand type; l sums the rounded values
             uint32_t pk[ATT_BN / 2];
             float rowsum = 0.0f;
 #pragma unroll
             for (int c = 0; c < ATT_BN / 2; ++c) {
                 float ra, rb;
-                pk[c] = pack_half2(exp2f(sv[2 * c] - m_use), exp2f(sv[2 * c + 1] - m_use), bf16, ra, rb);
+                pk[c] = pack_half2(ex2(sv[2 * c] - m_use), ex2(sv[2 * c + 1] - m_use), bf16, ra, rb);
                 rowsum += ra + rb;
             }
             l = l * alpha + rowsum;
@@ -330,18 +345,22 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                                      pk[e], pk[e + 1], pk[e + 2], pk[e + 3]);
                     }
                 }
-                // rescale the accumulator when any row of the warp raised its maximum
-                if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+                // rescale the accumulator when the warp raised its maximum
+                if (j > 0 && raise) {
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t v[32];
-                        const uint32_t ta = tmem_base + t_lane + ATT_O_COL + c * 32;
-                        tmem_ld_32x32b_x32(ta, v);
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t v[2][32];
+                        const uint32_t ta = tmem_base + t_lane + ATT_O_COL + h * 64;
+                        tmem_ld_32x32b_x32(ta, v[0]);
+                        tmem_ld_32x32b_x32(ta + 32, v[1]);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                        tmem_st_32x32b_x32(ta, v);
+                        for (int c = 0; c < 2; ++c)
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                v[c][i] = __float_as_uint(__uint_as_float(v[c][i]) * alpha);
+                        tmem_st_32x32b_x32(ta, v[0]);
+                        tmem_st_32x32b_x32(ta + 32, v[1]);
                     }
                     tmem_st_wait();
                 }
