@@ -65,7 +65,7 @@ extern "C" gemm_status_t attention_fwd(const void *Q, const void *K, const void 
         return dtype == GEMM_F32 ? GEMM_ERR_UNSUPPORTED : GEMM_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1)
         return GEMM_ERR_INVALID_ARG;
-    if (!std::isfinite(scale))
+    if (!std::isfinite(scale) || !(scale > 0.0f))
         return GEMM_ERR_INVALID_ARG;
     if (d != ATT_D || B * H > 65535)
         return GEMM_ERR_UNSUPPORTED;

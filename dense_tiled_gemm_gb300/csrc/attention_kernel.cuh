@@ -14,7 +14,8 @@
 //              row maximum m and sum l (base-2 exponent), write P_j =
 //              exp2(s - m) in the input type to shared memory in the MMA's
 //              operand layout, and at the end divide by l and store O and the
-//              row log-sum-exp. The maximum used for P is raised (and O and l
+//              row log-sum-exp (l sums the probabilities in FP32, before
+//              their rounding). The maximum used for P is raised (and O and l
 //              rescaled by exp2(m_old - m_new)) only when a row's maximum
 //              grows by more than RESCALE_LOG2 = 8: until then P <= 2^8, which
 //              the operand types hold, and O, l stay consistently scaled.
@@ -97,6 +98,16 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+__device__ __forceinline__ uint32_t pack2_rn(float a, float b, bool bf16)
+{
+    if (bf16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+    __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b, bool bf16, float &ra, float &rb)
@@ -300,31 +311,38 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             __syncwarp();
             if (lane == 0 && !skip)
                 mbar_arrive_local(s_empty(b));
-            // mask, scale (base 2), running maximum
+            // mask (only blocks that reach past some row's last visible key),
+            // then the running maximum over raw scores, scaled once (scale > 0)
             const int key0 = j * ATT_BN;
             const int key_end = p.causal ? min(p.Lk, qrow + (p.Lk - p.Lq) + 1) : p.Lk;
-            float mx = -INFINITY;
+            if (__any_sync(0xffffffffu, key0 + ATT_BN > key_end)) {
 #pragma unroll
-            for (int c = 0; c < ATT_BN; ++c) {
-                const float x = (key0 + c < key_end) ? sv[c] * p.scale_log2 : -INFINITY;
-                sv[c] = x;
-                mx = fmaxf(mx, x);
+                for (int c = 0; c < ATT_BN; ++c)
+                    sv[c] = (key0 + c < key_end) ? sv[c] : -INFINITY;
             }
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < ATT_BN; ++c)
+                mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
             // raise the maximum only when some row of the warp outgrew it by more
             // than the threshold (always on the first block with a visible key)
             const bool raise = __any_sync(0xffffffffu, mx > m + RESCALE_LOG2);
             const float m_new = raise ? fmaxf(m, mx) : m;
             const float m_use = m_new == -INFINITY ? 0.0f : m_new;
             const float alpha = raise ? ex2(m - m_use) : 1.0f;   // 0 while no key has been seen
-            // probabilities, rounded to the operand type; l sums the rounded values
+            // probabilities p = 2^(s * scale_log2 - m): one FFMA and one ex2 each,
+            // rounded to the operand type for the PV product; l sums them in FP32
             uint32_t pk[ATT_BN / 2];
-            float rowsum = 0.0f;
+            float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int c = 0; c < ATT_BN / 2; ++c) {
-                float ra, rb;
-                pk[c] = pack_half2(ex2(sv[2 * c] - m_use), ex2(sv[2 * c + 1] - m_use), bf16, ra, rb);
-                rowsum += ra + rb;
+                const float pa = ex2(fmaf(sv[2 * c], p.scale_log2, -m_use));
+                const float pb = ex2(fmaf(sv[2 * c + 1], p.scale_log2, -m_use));
+                pk[c] = pack2_rn(pa, pb, bf16);
+                sum4[c & 3] += pa + pb;
             }
+            const float rowsum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
             l = l * alpha + rowsum;
             m = m_new;
             // O and the P buffer are free once PV_{j-1} has completed

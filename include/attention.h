@@ -12,7 +12,8 @@
  *
  * per (batch, head), with FP32 accumulation (scores, probabilities' sum and
  * output) and the output cast to the operand type, rounding to nearest even.
- * The probabilities enter the PV product rounded to the operand type.
+ * The probabilities enter the PV product rounded to the operand type; their
+ * FP32 row sum is taken before that rounding.
  * Status codes are gemm.h's gemm_status_t.
  */
 #ifndef DENSE_TILED_GEMM_ATTENTION_H
@@ -41,7 +42,7 @@ extern "C" {
  *   dtype   GEMM_F16 or GEMM_BF16 for Q, K, V and O.
  *   causal  0: every key is visible; 1: key k is visible to query row i iff
  *           k <= i + (Lk - Lq) (the diagonal ends at the last query row).
- *   scale   the score scale, usually 1/sqrt(d); must be finite.
+ *   scale   the score scale, usually 1/sqrt(d); must be finite and > 0.
  *   stream  cudaStream_t as void*.
  *
  * Base addresses must be 16-byte aligned (GEMM_ERR_UNSUPPORTED otherwise).

@@ -52,11 +52,12 @@ def check(C_gpu, C_ref, C_abs, dtype_out: str):
 
 # Attention forward ("Two Waves, One Stage Apart", section "Beyond GEMM:
 # FlashAttention"). The probabilities enter the PV product rounded to the
-# operand type (relative error <= 2^-9 for BF16, 2^-12 for FP16), and the row
-# sum is taken over the rounded values, so the output error is at most about
-# 2^-9 * (O_abs + |O|) <= 2^-8 * O_abs, with O_abs = sum_k p_k |v_k| / l; the
-# FP32 score and output sums add far less. The bound below doubles that. The
-# row log-sum-exp inherits the relative error of l: |dLSE| <= log(1 + 2^-9).
+# operand type (relative error <= 2^-9 for BF16, 2^-12 for FP16) while the
+# row sum l is taken before the rounding, so the output error is at most about
+# 2^-9 * O_abs from the numerator plus 2^-9 * |O| from the normalisation,
+# <= 2^-8 * O_abs with O_abs = sum_k p_k |v_k| / l; the FP32 score and output
+# sums add far less. The bound below doubles that. The row log-sum-exp only
+# sees FP32 rounding of l; 2^-7 leaves ample room.
 ATT_REL = 2.0 ** -7
 ATT_LSE_ABS = 2.0 ** -7
 
