@@ -607,8 +607,10 @@ gemm_status_t pack_scales(const uint8_t *sf, int64_t rows, int64_t K, const SfGe
     const int64_t total = g.atom_rows;
     const unsigned blocks = static_cast<unsigned>(
         std::max<int64_t>(std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(sms) * 8), 1));
-    pack_scales_kernel<<<blocks, 256, 0, st>>>(sf, static_cast<uint8_t *>(dst), rows, (K + 31) / 32, g.R,
-                                               g.row_blocks, g.stages, g.groups, g.atoms);
+    const int64_t nb = (K + 31) / 32;
+    const int words = (nb % 4 == 0 && reinterpret_cast<uintptr_t>(sf) % 4 == 0) ? 1 : 0;
+    pack_scales_kernel<<<blocks, 256, 0, st>>>(sf, static_cast<uint8_t *>(dst), rows, nb, g.R, g.row_blocks,
+                                               g.stages, g.groups, g.atoms, words);
     if (cudaGetLastError() != cudaSuccess)
         return GEMM_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);

@@ -768,34 +768,43 @@ static __global__ void wait_selftest_kernel(uint64_t timeout_ns, unsigned long l
 // into the kernel's atoms: row blocks of R rows, and per row block and ring
 // stage `groups` groups of 4 blocks, each group `atoms` atoms of 128 rows
 // (see SF_ATOM_BYTES). Missing rows and blocks are zero. out has row_blocks x
-// stages x groups x atoms x 32 rows of 16 bytes; each thread writes one row.
+// stages x groups x atoms x 32 rows of 16 bytes; each thread writes one such
+// row. Consecutive threads take consecutive groups of 4 blocks of the same
+// scale rows, so the reads (4-byte words when `words` is set: the scale
+// rows and base are 4-byte aligned) are coalesced.
 static __global__ void pack_scales_kernel(const uint8_t *__restrict__ sf, uint8_t *__restrict__ out, int64_t rows,
-                                   int64_t n_blocks, int R, int64_t row_blocks, int64_t stages, int groups,
-                                   int atoms)
+                                          int64_t n_blocks, int R, int64_t row_blocks, int64_t stages, int groups,
+                                          int atoms, int words)
 {
-    const int64_t total = row_blocks * stages * groups * atoms * SF_ATOM_ROWS;
+    const int64_t sg_count = stages * groups;   // groups of 4 blocks along K
+    const int64_t total = row_blocks * atoms * SF_ATOM_ROWS * sg_count;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int m32 = static_cast<int>(i % SF_ATOM_ROWS);
-        int64_t t = i / SF_ATOM_ROWS;
+        const int64_t sg = i % sg_count;
+        int64_t t = i / sg_count;
+        const int m32 = static_cast<int>(t % SF_ATOM_ROWS);
+        t /= SF_ATOM_ROWS;
         const int a = static_cast<int>(t % atoms);
-        t /= atoms;
-        const int g = static_cast<int>(t % groups);
-        t /= groups;
-        const int64_t st = t % stages, rb = t / stages;
+        const int64_t rb = t / atoms;
+        const int64_t blk0 = sg * 4;
         uint32_t w[4] = {0, 0, 0, 0};
         for (int m4 = 0; m4 < 4; ++m4) {
             const int m = a * 128 + m4 * SF_ATOM_ROWS + m32;
             const int64_t row = rb * R + m;
             if (m >= R || row >= rows)
                 continue;
-            for (int k4 = 0; k4 < 4; ++k4) {
-                const int64_t blk = (st * groups + g) * 4 + k4;
-                if (blk < n_blocks)
-                    w[m4] |= static_cast<uint32_t>(sf[row * n_blocks + blk]) << (8 * k4);
+            const uint8_t *src = sf + row * n_blocks + blk0;
+            if (words && blk0 + 4 <= n_blocks) {
+                w[m4] = *reinterpret_cast<const uint32_t *>(src);
+            } else {
+                for (int k4 = 0; k4 < 4; ++k4)
+                    if (blk0 + k4 < n_blocks)
+                        w[m4] |= static_cast<uint32_t>(src[k4]) << (8 * k4);
             }
         }
-        reinterpret_cast<uint4 *>(out)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        const int64_t st = sg / groups, g = sg % groups;
+        const int64_t o = (((rb * stages + st) * groups + g) * atoms + a) * SF_ATOM_ROWS + m32;
+        reinterpret_cast<uint4 *>(out)[o] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
