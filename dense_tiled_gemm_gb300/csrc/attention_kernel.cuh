@@ -100,6 +100,30 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+// Packed FP32 pairs (Blackwell f32x2 arithmetic): one instruction for two lanes of work.
+__device__ __forceinline__ void ffma2(float &x0, float &x1, float a0, float a1, float b, float c)
+{
+    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %4};\n\t"
+        "mov.b64 pc, {%5, %5};\n\t"
+        "fma.rn.f32x2 pd, pa, pb, pc;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(x0), "=f"(x1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+__device__ __forceinline__ void fadd2(float &s0, float &s1, float a0, float a1)
+{
+    asm("{\n\t.reg .b64 ps, pa;\n\t"
+        "mov.b64 ps, {%0, %1};\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "add.rn.f32x2 ps, ps, pa;\n\t"
+        "mov.b64 {%0, %1}, ps;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "f"(a0), "f"(a1));
+}
+
 __device__ __forceinline__ uint32_t pack2_rn(float a, float b, bool bf16)
 {
     if (bf16) {
@@ -331,16 +355,21 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             const float m_new = raise ? fmaxf(m, mx) : m;
             const float m_use = m_new == -INFINITY ? 0.0f : m_new;
             const float alpha = raise ? ex2(m - m_use) : 1.0f;   // 0 while no key has been seen
-            // probabilities p = 2^(s * scale_log2 - m): one FFMA and one ex2 each,
-            // rounded to the operand type for the PV product; l sums them in FP32
+            // probabilities p = 2^(s * scale_log2 - m): a packed FFMA per pair and
+            // one ex2 each, rounded to the operand type for the PV product; l sums
+            // them in FP32 (packed adds, two pairs of accumulators)
             uint32_t pk[ATT_BN / 2];
             float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int c = 0; c < ATT_BN / 2; ++c) {
-                const float pa = ex2(fmaf(sv[2 * c], p.scale_log2, -m_use));
-                const float pb = ex2(fmaf(sv[2 * c + 1], p.scale_log2, -m_use));
+                float xa, xb;
+                ffma2(xa, xb, sv[2 * c], sv[2 * c + 1], p.scale_log2, -m_use);
+                const float pa = ex2(xa), pb = ex2(xb);
                 pk[c] = pack2_rn(pa, pb, bf16);
-                sum4[c & 3] += pa + pb;
+                if (c & 1)
+                    fadd2(sum4[2], sum4[3], pa, pb);
+                else
+                    fadd2(sum4[0], sum4[1], pa, pb);
             }
             const float rowsum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
             l = l * alpha + rowsum;

@@ -54,6 +54,12 @@ __device__ __forceinline__ uint32_t cluster_cta_rank()
     return r;
 }
 
+// Named barrier `id` (1-15) over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
