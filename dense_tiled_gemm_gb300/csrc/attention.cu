@@ -1,8 +1,8 @@
 // attention.cu: host side of attention_fwd (include/attention.h).
 //
-// One launch of attention_fwd_kernel per call: a grid of ceil(Lq / 128)
-// query tiles by B * H heads, 192 threads and ~193 KB of shared memory per
-// CTA, with programmatic stream serialisation like the GEMM. The tensor maps
+// One launch of attention_fwd_kernel per call: a grid of ceil(Lq / 256)
+// query row blocks (two 128-row tiles each) by B * H heads, 320 threads and
+// ~192 KB of shared memory per CTA, with programmatic stream serialisation like the GEMM. The tensor maps
 // view Q, K and V as 3-D (d, rows, B * H) so that a tile never reads into
 // the next head: rows past Lq or Lk come back as zeros.
 #include <cuda_runtime.h>
@@ -104,7 +104,7 @@ extern "C" gemm_status_t attention_fwd(const void *Q, const void *K, const void 
     p.status = rt.status;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((Lq + ATT_BM - 1) / ATT_BM), static_cast<unsigned>(bh));
+    cfg.gridDim = dim3(static_cast<unsigned>((Lq + ATT_ROWS - 1) / ATT_ROWS), static_cast<unsigned>(bh));
     cfg.blockDim = dim3(ATT_THREADS);
     cfg.dynamicSmemBytes = ATT_SMEM;
     cfg.stream = static_cast<cudaStream_t>(stream);

@@ -2,54 +2,63 @@
 //
 // "Two Waves, One Stage Apart" (section "Beyond GEMM: FlashAttention")
 // describes the FlashAttention inner loop: QK and PV products alternate with
-// an online softmax over key/value blocks, and the QK product of block i+1
-// runs while the PV product of block i consumes its probabilities. Here the
-// same overlap comes from warp roles and two score buffers in tensor memory:
+// an online softmax over key/value blocks, and the matrix work of one wave
+// group overlaps the softmax of the other. Here one CTA holds two query tiles
+// (A: rows 0-127, B: rows 128-255 of its 256) with a softmax warp group each,
+// so that while one group turns its scores into probabilities, the tensor
+// core runs the other group's products:
 //
-//   warp 0     producer: one thread loads the CTA's Q tile once, then K and V
+//   warp 0     producer: one thread loads both Q tiles once, then K and V
 //              blocks into two-slot rings (TMA, 128-byte swizzle);
-//   warp 1     MMA issuer: S_{j+1} = Q K_{j+1}^T into score buffer (j+1) % 2,
-//              then O += P_j V_j into the output accumulator; owns TMEM;
-//   warps 2-5  softmax: one query row per thread. Read S_j, keep the running
-//              row maximum m and sum l (base-2 exponent), write P_j =
-//              exp2(s - m) in the input type to shared memory in the MMA's
-//              operand layout, and at the end divide by l and store O and the
-//              row log-sum-exp (l sums the probabilities in FP32, before
-//              their rounding). The maximum used for P is raised (and O and l
-//              rescaled by exp2(m_old - m_new)) only when a row's maximum
-//              grows by more than RESCALE_LOG2 = 8: until then P <= 2^8, which
-//              the operand types hold, and O, l stay consistently scaled.
+//   warp 1     MMA issuer, per key block j:
+//                PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1)
+//              (S_g = Q_g K^T into tile g's TMEM score buffer, O_g += P_g V
+//              into tile g's FP32 accumulator, P_g read from TMEM); owns TMEM;
+//   warps 2-5  softmax group A, warps 6-9 group B: one query row per thread.
+//              Read S_g(j), keep the running row maximum m and sum l (base-2
+//              exponent), and write P_g = exp2(s - m), rounded to the operand
+//              type, over the first half of the score buffer it came from; at
+//              the end divide by l and store O and the row log-sum-exp. The
+//              maximum used for P is raised (and O and l rescaled by
+//              exp2(m_old - m_new)) only when a row's maximum grows by more
+//              than RESCALE_LOG2 = 8: until then P <= 2^8, which the operand
+//              types hold, and O and l stay consistently scaled; l sums the
+//              probabilities in FP32 before their rounding.
 //
-// One CTA covers 128 query rows of one (batch, head); blocks are 128 keys;
-// the head dimension is 128. TMEM: score buffers at columns 0 and 128, the
-// FP32 output accumulator at 256. Masked keys (past Lk, or after the causal
-// diagonal, which is aligned to the last query row) score -inf. Every wait
-// is bounded as in the GEMM kernel: past the limit a thread records the site
-// and stops issuing work and signals.
+// The tensor core runs a CTA's products in issue order, so QK_g(j+1), issued
+// after PV_g(j), overwrites P_g(j) only after PV_g(j) has read it, and the
+// commit that signals S_g(j+1) also covers PV_g(j): a softmax group that holds
+// S_g(j+1) may rescale O_g. Blocks are 128 keys; the head dimension is 128.
+// TMEM: score buffers at columns 0 (A) and 128 (B), accumulators at 256 (A)
+// and 384 (B). Masked keys (past Lk, or after the causal diagonal, which is
+// aligned to the last query row) score -inf. Every wait is bounded as in the
+// GEMM kernel: past the limit a thread records the site and stops issuing
+// work and signals.
 #pragma once
 
 #include "gemm_kernel.cuh"
 
 namespace dtg {
 
-constexpr int ATT_BM = 128;                       // query rows per CTA
+constexpr int ATT_BM = 128;                       // query rows per tile
+constexpr int ATT_TILES = 2;                      // query tiles per CTA
+constexpr int ATT_ROWS = ATT_BM * ATT_TILES;      // query rows per CTA
 constexpr int ATT_BN = 128;                       // keys per block
 constexpr int ATT_D = 128;                        // head dimension
-constexpr int ATT_TILE = ATT_BM * ATT_D * 2;      // 32 KB: one Q, K, V or P tile
+constexpr int ATT_TILE = ATT_BM * ATT_D * 2;      // 32 KB: one Q, K or V tile
 constexpr int ATT_SLAB = ATT_TILE / 2;            // 64 columns of 16-bit data, 128-byte rows
 constexpr int ATT_STAGES = 2;                     // K and V ring slots
 constexpr uint32_t ATT_TMEM_COLS = 512;
-constexpr uint32_t ATT_O_COL = 256;
-constexpr int ATT_THREADS = 192;
+constexpr uint32_t ATT_O_COL = 256;               // accumulator of tile g at 256 + 128 g
+constexpr int ATT_THREADS = 64 + 32 * 4 * ATT_TILES;   // producer, MMA, 4 softmax warps per tile
 constexpr float RESCALE_LOG2 = 8.0f;              // lazy rescaling threshold (base-2 exponent)
 
-// shared memory: Q | K[2] | V[2] | P | barriers | TMEM address
+// shared memory: Q[2] | K[2] | V[2] | barriers | TMEM address
 constexpr uint32_t ATT_Q_OFF = 0;
-constexpr uint32_t ATT_K_OFF = ATT_TILE;
+constexpr uint32_t ATT_K_OFF = ATT_TILES * ATT_TILE;
 constexpr uint32_t ATT_V_OFF = ATT_K_OFF + ATT_STAGES * ATT_TILE;
-constexpr uint32_t ATT_P_OFF = ATT_V_OFF + ATT_STAGES * ATT_TILE;
-constexpr uint32_t ATT_BAR_OFF = ATT_P_OFF + ATT_TILE;
-constexpr uint32_t ATT_NUM_BARS = 16;
+constexpr uint32_t ATT_BAR_OFF = ATT_V_OFF + ATT_STAGES * ATT_TILE;
+constexpr uint32_t ATT_NUM_BARS = 14;
 constexpr uint32_t ATT_SMEM = ATT_BAR_OFF + ATT_NUM_BARS * 8 + 16;
 
 enum : uint32_t {
@@ -57,11 +66,9 @@ enum : uint32_t {
     SITE_ATT_K_EMPTY = 0x411,
     SITE_ATT_V_EMPTY = 0x412,
     SITE_ATT_K_FULL = 0x413,
-    SITE_ATT_S_EMPTY = 0x414,
     SITE_ATT_P_FULL = 0x415,
     SITE_ATT_V_FULL = 0x416,
     SITE_ATT_S_FULL = 0x417,
-    SITE_ATT_O_READY = 0x418,
     SITE_ATT_DRAIN = 0x419,
     SITE_ATT_DONE = 0x41A,
 };
@@ -79,13 +86,13 @@ struct AttParams {
     unsigned long long *status;
 };
 
-// KV blocks a query tile needs: all ceil(Lk / 128), or, when causal, those up
-// to the block holding the last key its last row may see.
-__host__ __device__ inline int att_num_blocks(int q0, int Lq, int Lk, bool causal)
+// KV blocks the rows [q0, q0 + rows) need: all ceil(Lk / 128), or, when
+// causal, those up to the block holding the last key their last row may see.
+__host__ __device__ inline int att_num_blocks(int q0, int rows, int Lq, int Lk, bool causal)
 {
     int n = (Lk + ATT_BN - 1) / ATT_BN;
     if (causal) {
-        const int last_row = min(q0 + ATT_BM, Lq) - 1;
+        const int last_row = min(q0 + rows, Lq) - 1;
         const int last_key = last_row + (Lk - Lq);
         n = last_key < 0 ? 0 : min(n, last_key / ATT_BN + 1);
     }
@@ -134,20 +141,6 @@ __device__ __forceinline__ uint32_t pack2_rn(float a, float b, bool bf16)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ uint32_t pack_half2(float a, float b, bool bf16, float &ra, float &rb)
-{
-    if (bf16) {
-        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-        ra = __bfloat162float(v.x);
-        rb = __bfloat162float(v.y);
-        return *reinterpret_cast<uint32_t *>(&v);
-    }
-    __half2 v = __floats2half2_rn(a, b);
-    ra = __half2float(v.x);
-    rb = __half2float(v.y);
-    return *reinterpret_cast<uint32_t *>(&v);
-}
-
 __global__ void __launch_bounds__(ATT_THREADS, 1)
 attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const AttParams p)
@@ -160,9 +153,11 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         return;
     }
     const uint32_t warp = threadIdx.x / 32u, lane = threadIdx.x % 32u;
-    const int q_tile = static_cast<int>(blockIdx.x), bh = static_cast<int>(blockIdx.y);
-    const int q0 = q_tile * ATT_BM;
-    const int nkv = att_num_blocks(q0, p.Lq, p.Lk, p.causal != 0);
+    const int bh = static_cast<int>(blockIdx.y);
+    const int q0 = static_cast<int>(blockIdx.x) * ATT_ROWS;
+    // key blocks of each tile; tile B's (the later rows) are the CTA's
+    const int nkv_a = att_num_blocks(q0, ATT_BM, p.Lq, p.Lk, p.causal != 0);
+    const int nkv = att_num_blocks(q0, ATT_ROWS, p.Lq, p.Lk, p.causal != 0);
 
     const uint32_t bar0 = base + ATT_BAR_OFF;
     const uint32_t q_full = bar0;
@@ -170,9 +165,9 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     auto k_empty = [&](uint32_t s) { return bar0 + 8u * (3 + s); };
     auto v_full = [&](uint32_t s) { return bar0 + 8u * (5 + s); };
     auto v_empty = [&](uint32_t s) { return bar0 + 8u * (7 + s); };
-    auto s_full = [&](uint32_t b) { return bar0 + 8u * (9 + b); };
-    auto s_empty = [&](uint32_t b) { return bar0 + 8u * (11 + b); };
-    const uint32_t p_full = bar0 + 8u * 13, o_ready = bar0 + 8u * 14, done_bar = bar0 + 8u * 15;
+    auto s_full = [&](uint32_t g) { return bar0 + 8u * (9 + g); };
+    auto p_full = [&](uint32_t g) { return bar0 + 8u * (11 + g); };
+    const uint32_t done_bar = bar0 + 8u * 13;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem_raw + ATT_BAR_OFF + ATT_NUM_BARS * 8);
 
     if (threadIdx.x == 0) {
@@ -183,12 +178,10 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             mbar_init(v_full(s), 1);
             mbar_init(v_empty(s), 1);
         }
-        for (uint32_t b = 0; b < 2; ++b) {
-            mbar_init(s_full(b), 1);    // one tcgen05.commit
-            mbar_init(s_empty(b), 4);   // every softmax warp
+        for (uint32_t g = 0; g < ATT_TILES; ++g) {
+            mbar_init(s_full(g), 1);    // one tcgen05.commit
+            mbar_init(p_full(g), 4);    // the group's four warps
         }
-        mbar_init(p_full, 4);
-        mbar_init(o_ready, 1);
         mbar_init(done_bar, 1);
         fence_barrier_init();
     }
@@ -211,9 +204,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             prefetch_tensor_map(&tmap_q);
             prefetch_tensor_map(&tmap_k);
             prefetch_tensor_map(&tmap_v);
-            mbar_arrive_expect_tx(q_full, ATT_TILE);
-            tma_load_3d(base + ATT_Q_OFF, &tmap_q, q_full, 0, q0, bh);
-            tma_load_3d(base + ATT_Q_OFF + ATT_SLAB, &tmap_q, q_full, 64, q0, bh);
+            mbar_arrive_expect_tx(q_full, ATT_TILES * ATT_TILE);
+            for (int g = 0; g < ATT_TILES; ++g) {
+                const uint32_t dst = base + ATT_Q_OFF + g * ATT_TILE;
+                tma_load_3d(dst, &tmap_q, q_full, 0, q0 + g * ATT_BM, bh);
+                tma_load_3d(dst + ATT_SLAB, &tmap_q, q_full, 64, q0 + g * ATT_BM, bh);
+            }
             uint32_t k_pend = 0, v_pend = 0, k_par = 0, v_par = 0;
             for (int j = 0; j < nkv; ++j) {
                 const uint32_t s = j % ATT_STAGES, ph = (j / ATT_STAGES) & 1;
@@ -254,75 +250,93 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         if (lane == 0 && nkv > 0) {
             wait_bounded<false>(w, q_full, 0, SITE_ATT_Q);
             tc_fence_after_sync();
-            auto issue_qk = [&](int j) {
+            // S_g(j) = Q_g K_j^T into tile g's score buffer; after tile B, K_j's slot is free
+            auto issue_qk = [&](int j, uint32_t g) {
                 const uint32_t s = j % ATT_STAGES, ph = (j / ATT_STAGES) & 1;
-                const uint32_t b = j & 1, bph = (j >> 1) & 1;
-                wait_bounded<false>(w, k_full(s), ph, SITE_ATT_K_FULL);
-                wait_bounded<false>(w, s_empty(b), bph ^ 1u, SITE_ATT_S_EMPTY);
+                if (g == 0 || j >= nkv_a)
+                    wait_bounded<false>(w, k_full(s), ph, SITE_ATT_K_FULL);
                 tc_fence_after_sync();
                 if (w.aborted)
                     return;
-                const uint32_t d_tmem = tmem_base + b * ATT_BN;
                 const uint32_t k_addr = base + ATT_K_OFF + s * ATT_TILE;
+                const uint32_t q_addr = base + ATT_Q_OFF + g * ATT_TILE;
 #pragma unroll
                 for (int slab = 0; slab < 2; ++slab) {
-                    const uint64_t a_desc = smem_desc_sw128(base + ATT_Q_OFF + slab * ATT_SLAB, 16u, 1024u);
+                    const uint64_t a_desc = smem_desc_sw128(q_addr + slab * ATT_SLAB, 16u, 1024u);
                     const uint64_t b_desc = smem_desc_sw128(k_addr + slab * ATT_SLAB, 16u, 1024u);
 #pragma unroll
                     for (uint32_t k = 0; k < 4; ++k)
-                        mma<1, KIND_F16>(d_tmem, a_desc + 2u * k, b_desc + 2u * k, p.idesc_qk,
+                        mma<1, KIND_F16>(tmem_base + g * ATT_BN, a_desc + 2u * k, b_desc + 2u * k, p.idesc_qk,
                                          (slab > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit(s_full(b));
-                mma_commit(k_empty(s));
+                mma_commit(s_full(g));
+                if (g == 1)
+                    mma_commit(k_empty(s));
             };
-            issue_qk(0);
-            for (int j = 0; j < nkv; ++j) {
-                if (j + 1 < nkv)
-                    issue_qk(j + 1);   // the tensor core computes S_{j+1} while softmax works on S_j
+            // O_g += P_g V_j, P_g from TMEM (16 products of 16 keys, 8 columns each);
+            // after tile B, V_j's slot is free
+            auto issue_pv = [&](int j, uint32_t g) {
                 const uint32_t s = j % ATT_STAGES, ph = (j / ATT_STAGES) & 1;
-                wait_bounded<false>(w, p_full, j & 1, SITE_ATT_P_FULL);
-                wait_bounded<false>(w, v_full(s), ph, SITE_ATT_V_FULL);
+                wait_bounded<false>(w, p_full(g), j & 1, SITE_ATT_P_FULL);
+                if (g == 0 || j >= nkv_a)
+                    wait_bounded<false>(w, v_full(s), ph, SITE_ATT_V_FULL);
                 tc_fence_after_sync();
                 if (w.aborted)
-                    continue;
+                    return;
                 const uint32_t v_addr = base + ATT_V_OFF + s * ATT_TILE;
 #pragma unroll
                 for (int slab = 0; slab < 2; ++slab) {
-                    const uint64_t a_desc = smem_desc_sw128(base + ATT_P_OFF + slab * ATT_SLAB, 16u, 1024u);
                     // N-contiguous V: 64-wide d atoms 8192 B apart, 16 keys = 2048 B per MMA
                     const uint64_t b_desc = smem_desc_sw128(v_addr + slab * ATT_SLAB, 8192u, 1024u);
 #pragma unroll
                     for (uint32_t k = 0; k < 4; ++k)
-                        mma<1, KIND_F16>(tmem_base + ATT_O_COL, a_desc + 2u * k, b_desc + (2048u >> 4) * k,
-                                         p.idesc_pv, (j > 0 || slab > 0 || k > 0) ? 1u : 0u);
+                        mma_f16_tmem_a(tmem_base + ATT_O_COL + g * ATT_BN, tmem_base + g * ATT_BN + slab * 32 + k * 8,
+                                       b_desc + (2048u >> 4) * k, p.idesc_pv, (j > 0 || slab > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit(o_ready);
-                mma_commit(v_empty(s));
+                if (g == 1)
+                    mma_commit(v_empty(s));
+            };
+            if (nkv_a > 0)
+                issue_qk(0, 0);
+            issue_qk(0, 1);
+            for (int j = 0; j < nkv; ++j) {
+                if (j < nkv_a) {
+                    issue_pv(j, 0);
+                    if (j + 1 < nkv_a)
+                        issue_qk(j + 1, 0);   // tile A's next scores while group B finishes block j
+                }
+                issue_pv(j, 1);
+                if (j + 1 < nkv)
+                    issue_qk(j + 1, 1);
             }
             mma_commit(done_bar);
             wait_drain<false>(done_bar, 0, w.limit_ns, w.id, w.status, SITE_ATT_DONE);
         }
     } else {
         // ------------------------------------------------------------ softmax and output
-        const uint32_t quarter = warp & 3u;
-        const int r = static_cast<int>(quarter * 32u + lane);   // row within the tile (TMEM lane)
-        const int qrow = q0 + r;
+        const uint32_t g = (warp - EPI_WARP0) / 4u;            // the query tile of this warp group
+        const uint32_t quarter = warp & 3u;                    // the TMEM lane quarter this warp may access
+        const int r = static_cast<int>(quarter * 32u + lane);  // row within the tile (TMEM lane)
+        const int qrow = q0 + static_cast<int>(g) * ATT_BM + r;
         const uint32_t t_lane = (quarter * 32u) << 16;
+        const uint32_t s_col = g * ATT_BN, o_col = ATT_O_COL + g * ATT_BN;
+        const int nkv_g = g == 0 ? nkv_a : nkv;
         const bool bf16 = p.bf16 != 0;
+        const int key_end = p.causal ? min(p.Lk, qrow + (p.Lk - p.Lq) + 1) : p.Lk;
         float m = -INFINITY, l = 0.0f;
-        for (int j = 0; j < nkv; ++j) {
-            const uint32_t b = j & 1;
-            wait_bounded<false>(w, s_full(b), (j >> 1) & 1, SITE_ATT_S_FULL);
-            bool skip = __any_sync(0xffffffffu, w.aborted);
+        for (int j = 0; j < nkv_g; ++j) {
+            wait_bounded<false>(w, s_full(g), j & 1, SITE_ATT_S_FULL);
+            const bool skip = __any_sync(0xffffffffu, w.aborted);
             w.aborted = skip;
+            if (skip)
+                break;
             tc_fence_after_sync();
             float sv[ATT_BN];
-            if (!skip) {
+            {
                 uint32_t v[4][32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    tmem_ld_32x32b_x32(tmem_base + t_lane + b * ATT_BN + c * 32, v[c]);
+                    tmem_ld_32x32b_x32(tmem_base + t_lane + s_col + c * 32, v[c]);
                 tmem_ld_wait();
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
@@ -330,15 +344,9 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     for (int i = 0; i < 32; ++i)
                         sv[c * 32 + i] = __uint_as_float(v[c][i]);
             }
-            // the score buffer is free for S_{j+2}
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0 && !skip)
-                mbar_arrive_local(s_empty(b));
             // mask (only blocks that reach past some row's last visible key),
             // then the running maximum over raw scores, scaled once (scale > 0)
             const int key0 = j * ATT_BN;
-            const int key_end = p.causal ? min(p.Lk, qrow + (p.Lk - p.Lq) + 1) : p.Lk;
             if (__any_sync(0xffffffffu, key0 + ATT_BN > key_end)) {
 #pragma unroll
                 for (int c = 0; c < ATT_BN; ++c)
@@ -355,73 +363,59 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             const float m_new = raise ? fmaxf(m, mx) : m;
             const float m_use = m_new == -INFINITY ? 0.0f : m_new;
             const float alpha = raise ? ex2(m - m_use) : 1.0f;   // 0 while no key has been seen
-            // probabilities p = 2^(s * scale_log2 - m): a packed FFMA per pair and
-            // one ex2 each, rounded to the operand type for the PV product; l sums
-            // them in FP32 (packed adds, two pairs of accumulators)
-            uint32_t pk[ATT_BN / 2];
+            // probabilities p = 2^(s * scale_log2 - m): a packed FFMA per pair and one
+            // ex2 each, rounded to the operand type, two per TMEM column over the
+            // first 64 columns of the score buffer; l sums them in FP32 (packed
+            // adds, two pairs of accumulators)
             float sum4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int c = 0; c < ATT_BN / 2; ++c) {
-                float xa, xb;
-                ffma2(xa, xb, sv[2 * c], sv[2 * c + 1], p.scale_log2, -m_use);
-                const float pa = ex2(xa), pb = ex2(xb);
-                pk[c] = pack2_rn(pa, pb, bf16);
-                if (c & 1)
-                    fadd2(sum4[2], sum4[3], pa, pb);
-                else
-                    fadd2(sum4[0], sum4[1], pa, pb);
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int e = 64 * h + 2 * c;
+                    float xa, xb;
+                    ffma2(xa, xb, sv[e], sv[e + 1], p.scale_log2, -m_use);
+                    const float pa = ex2(xa), pb = ex2(xb);
+                    pk[c] = pack2_rn(pa, pb, bf16);
+                    if (c & 1)
+                        fadd2(sum4[2], sum4[3], pa, pb);
+                    else
+                        fadd2(sum4[0], sum4[1], pa, pb);
+                }
+                tmem_st_32x32b_x32(tmem_base + t_lane + s_col + h * 32, pk);
             }
-            const float rowsum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-            l = l * alpha + rowsum;
+            l = l * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
             m = m_new;
-            // O and the P buffer are free once PV_{j-1} has completed
-            if (j > 0)
-                wait_bounded<false>(w, o_ready, (j - 1) & 1, SITE_ATT_O_READY);
-            skip = __any_sync(0xffffffffu, w.aborted);
-            w.aborted = skip;
-            tc_fence_after_sync();
-            if (!skip) {
-                // P row r, 128-byte swizzle: 16-byte unit u of a 128-byte row at u ^ (r % 8)
-#pragma unroll
-                for (int slab = 0; slab < 2; ++slab) {
-                    const uint32_t row = base + ATT_P_OFF + slab * ATT_SLAB + static_cast<uint32_t>(r) * 128u;
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int e = slab * 32 + u * 4;   // index into pk (two values per word)
-                        st_shared_v4(row + ((static_cast<uint32_t>(u) ^ (static_cast<uint32_t>(r) & 7u)) << 4),
-                                     pk[e], pk[e + 1], pk[e + 2], pk[e + 3]);
-                    }
-                }
-                // rescale the accumulator when the warp raised its maximum
-                if (j > 0 && raise) {
+            // rescale this tile's accumulator row when the warp raised its maximum
+            // (PV_g(j-1) has completed: S_g(j)'s commit covers it)
+            if (j > 0 && raise) {
 #pragma unroll 1
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t v[2][32];
-                        const uint32_t ta = tmem_base + t_lane + ATT_O_COL + h * 64;
-                        tmem_ld_32x32b_x32(ta, v[0]);
-                        tmem_ld_32x32b_x32(ta + 32, v[1]);
-                        tmem_ld_wait();
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[2][32];
+                    const uint32_t ta = tmem_base + t_lane + o_col + h * 64;
+                    tmem_ld_32x32b_x32(ta, v[0]);
+                    tmem_ld_32x32b_x32(ta + 32, v[1]);
+                    tmem_ld_wait();
 #pragma unroll
-                        for (int c = 0; c < 2; ++c)
+                    for (int c = 0; c < 2; ++c)
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                v[c][i] = __float_as_uint(__uint_as_float(v[c][i]) * alpha);
-                        tmem_st_32x32b_x32(ta, v[0]);
-                        tmem_st_32x32b_x32(ta + 32, v[1]);
-                    }
-                    tmem_st_wait();
+                        for (int i = 0; i < 32; ++i)
+                            v[c][i] = __float_as_uint(__uint_as_float(v[c][i]) * alpha);
+                    tmem_st_32x32b_x32(ta, v[0]);
+                    tmem_st_32x32b_x32(ta + 32, v[1]);
                 }
             }
-            fence_proxy_async_smem();   // P is read by the tensor core (async proxy)
+            tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0 && !skip)
-                mbar_arrive_local(p_full);
+            if (lane == 0)
+                mbar_arrive_local(p_full(g));
         }
         // ---------------------------------------------------------- output
-        bool skip = false;
-        if (nkv > 0) {
-            wait_bounded<false>(w, o_ready, (nkv - 1) & 1, SITE_ATT_O_READY);
+        bool skip = w.aborted;
+        if (nkv > 0 && !skip) {
+            wait_bounded<false>(w, done_bar, 0, SITE_ATT_DONE);
             skip = __any_sync(0xffffffffu, w.aborted);
             tc_fence_after_sync();
         }
@@ -431,8 +425,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
-                if (nkv > 0) {
-                    tmem_ld_32x32b_x32(tmem_base + t_lane + ATT_O_COL + c * 32, v);
+                if (nkv_g > 0) {
+                    tmem_ld_32x32b_x32(tmem_base + t_lane + o_col + c * 32, v);
                     tmem_ld_wait();
                 } else {
 #pragma unroll
@@ -441,11 +435,9 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 }
                 if (qrow < p.Lq) {
                     uint32_t o[16];
-                    float ra, rb;
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        o[i] = pack_half2(__uint_as_float(v[2 * i]) * inv_l, __uint_as_float(v[2 * i + 1]) * inv_l,
-                                          bf16, ra, rb);
+                        o[i] = pack2_rn(__uint_as_float(v[2 * i]) * inv_l, __uint_as_float(v[2 * i + 1]) * inv_l, bf16);
                     uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 64);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)

@@ -54,12 +54,6 @@ __device__ __forceinline__ uint32_t cluster_cta_rank()
     return r;
 }
 
-// Named barrier `id` (1-15) over `count` threads (a multiple of 32).
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
@@ -327,6 +321,19 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b
 // the tensor-memory addresses of the 32-bit columns that hold this
 // instruction's E8M0 scales (one byte per row, picked by the scale-ID fields
 // of idesc).
+// D (+)= A * B with A read from tensor memory (one TMEM lane per row of A,
+// two 16-bit elements per 32-bit column) and B from a shared-memory
+// descriptor: kind::f16, one CTA.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
 template <int CG, int KIND>
 __device__ __forceinline__ void mma_scaled(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
