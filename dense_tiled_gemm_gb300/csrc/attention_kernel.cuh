@@ -10,7 +10,8 @@
 //
 //   warp 0     producer: one thread loads both Q tiles once, then K and V
 //              blocks into two-slot rings (TMA, 128-byte swizzle);
-//   warp 1     MMA issuer, per key block j:
+//   warp 1     MMA issuer (the whole warp; one elected lane issues), per key
+//              block j:
 //                PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1)
 //              (S_g = Q_g K^T into tile g's TMEM score buffer, O_g += P_g V
 //              into tile g's FP32 accumulator, P_g read from TMEM); owns TMEM;
@@ -107,6 +108,14 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+// max(a, b, c) in one instruction (three-input form, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
 // Packed FP32 pairs (Blackwell f32x2 arithmetic): one instruction for two lanes of work.
 __device__ __forceinline__ void ffma2(float &x0, float &x1, float a0, float a1, float b, float c)
 {
@@ -153,8 +162,21 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         return;
     }
     const uint32_t warp = threadIdx.x / 32u, lane = threadIdx.x % 32u;
-    const int bh = static_cast<int>(blockIdx.y);
-    const int q0 = static_cast<int>(blockIdx.x) * ATT_ROWS;
+    // Causal tiles differ in work (a row block needs the key blocks up to its
+    // diagonal): CTAs take them in order of decreasing work, longest first
+    // (dispatch order is blockIdx.x fastest), so that the last wave holds the
+    // lightest ones. Otherwise x is the row block and y the head, and a head's
+    // row blocks run side by side and share its K and V in L2.
+    int bh, qt;
+    if (p.causal) {
+        const int64_t L = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
+        qt = static_cast<int>(gridDim.x - 1 - L / gridDim.y);
+        bh = static_cast<int>(L % gridDim.y);
+    } else {
+        qt = static_cast<int>(blockIdx.x);
+        bh = static_cast<int>(blockIdx.y);
+    }
+    const int q0 = qt * ATT_ROWS;
     // key blocks of each tile; tile B's (the later rows) are the CTA's
     const int nkv_a = att_num_blocks(q0, ATT_BM, p.Lq, p.Lk, p.causal != 0);
     const int nkv = att_num_blocks(q0, ATT_ROWS, p.Lq, p.Lk, p.causal != 0);
@@ -247,14 +269,22 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && nkv > 0) {
+        // The whole warp walks the schedule and waits; one elected lane issues
+        // each product and commit (see mma_elect).
+        if (nkv > 0) {
+            auto sync_abort = [&]() {
+                __syncwarp();
+                w.aborted = __any_sync(0xffffffffu, w.aborted);
+            };
             wait_bounded<false>(w, q_full, 0, SITE_ATT_Q);
+            sync_abort();
             tc_fence_after_sync();
             // S_g(j) = Q_g K_j^T into tile g's score buffer; after tile B, K_j's slot is free
             auto issue_qk = [&](int j, uint32_t g) {
                 const uint32_t s = j % ATT_STAGES, ph = (j / ATT_STAGES) & 1;
                 if (g == 0 || j >= nkv_a)
                     wait_bounded<false>(w, k_full(s), ph, SITE_ATT_K_FULL);
+                sync_abort();
                 tc_fence_after_sync();
                 if (w.aborted)
                     return;
@@ -266,12 +296,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     const uint64_t b_desc = smem_desc_sw128(k_addr + slab * ATT_SLAB, 16u, 1024u);
 #pragma unroll
                     for (uint32_t k = 0; k < 4; ++k)
-                        mma<1, KIND_F16>(tmem_base + g * ATT_BN, a_desc + 2u * k, b_desc + 2u * k, p.idesc_qk,
-                                         (slab > 0 || k > 0) ? 1u : 0u);
+                        mma_elect<1, KIND_F16>(tmem_base + g * ATT_BN, a_desc + 2u * k, b_desc + 2u * k, p.idesc_qk,
+                                               (slab > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit(s_full(g));
+                mma_commit_elect(s_full(g));
                 if (g == 1)
-                    mma_commit(k_empty(s));
+                    mma_commit_elect(k_empty(s));
             };
             // O_g += P_g V_j, P_g from TMEM (16 products of 16 keys, 8 columns each);
             // after tile B, V_j's slot is free
@@ -280,6 +310,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 wait_bounded<false>(w, p_full(g), j & 1, SITE_ATT_P_FULL);
                 if (g == 0 || j >= nkv_a)
                     wait_bounded<false>(w, v_full(s), ph, SITE_ATT_V_FULL);
+                sync_abort();
                 tc_fence_after_sync();
                 if (w.aborted)
                     return;
@@ -290,11 +321,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     const uint64_t b_desc = smem_desc_sw128(v_addr + slab * ATT_SLAB, 8192u, 1024u);
 #pragma unroll
                     for (uint32_t k = 0; k < 4; ++k)
-                        mma_f16_tmem_a(tmem_base + ATT_O_COL + g * ATT_BN, tmem_base + g * ATT_BN + slab * 32 + k * 8,
-                                       b_desc + (2048u >> 4) * k, p.idesc_pv, (j > 0 || slab > 0 || k > 0) ? 1u : 0u);
+                        mma_f16_tmem_a_elect(tmem_base + ATT_O_COL + g * ATT_BN,
+                                             tmem_base + g * ATT_BN + slab * 32 + k * 8, b_desc + (2048u >> 4) * k,
+                                             p.idesc_pv, (j > 0 || slab > 0 || k > 0) ? 1u : 0u);
                 }
                 if (g == 1)
-                    mma_commit(v_empty(s));
+                    mma_commit_elect(v_empty(s));
             };
             if (nkv_a > 0)
                 issue_qk(0, 0);
@@ -309,7 +341,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 if (j + 1 < nkv)
                     issue_qk(j + 1, 1);
             }
-            mma_commit(done_bar);
+            mma_commit_elect(done_bar);
             wait_drain<false>(done_bar, 0, w.limit_ns, w.id, w.status, SITE_ATT_DONE);
         }
     } else {
@@ -354,8 +386,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < ATT_BN; ++c)
-                mx4[c & 3] = fmaxf(mx4[c & 3], sv[c]);
+            for (int c = 0; c < ATT_BN; c += 2)
+                mx4[(c / 2) & 3] = fmax3(mx4[(c / 2) & 3], sv[c], sv[c + 1]);
             const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
             // raise the maximum only when some row of the warp outgrew it by more
             // than the threshold (always on the first block with a visible key)

@@ -321,6 +321,68 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b
 // the tensor-memory addresses of the 32-bit columns that hold this
 // instruction's E8M0 scales (one byte per row, picked by the scale-ID fields
 // of idesc).
+// The unscaled product issued by one elected lane of a converged warp. The
+// warp computes the (warp-uniform) operands together, so they stay in the
+// uniform datapath; issued from a single divergent lane, every instruction
+// first pays for moving its operands there, and under issue pressure from
+// other warps of the sub-partition that roughly halves the rate of short
+// (64-cycle) products.
+template <int CG, int KIND>
+__device__ __forceinline__ void mma_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    static_assert(KIND == KIND_F16 || KIND == KIND_F8, "unscaled kinds only");
+    if constexpr (CG == 1 && KIND == KIND_F16)
+        asm volatile("{\n\t.reg .pred e, p;\n\t"
+                     "elect.sync _|e, 0xffffffff;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                     : "memory");
+    else if constexpr (CG == 2 && KIND == KIND_F16)
+        asm volatile("{\n\t.reg .pred e, p;\n\t"
+                     "elect.sync _|e, 0xffffffff;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                     : "memory");
+    else if constexpr (CG == 1)
+        asm volatile("{\n\t.reg .pred e, p;\n\t"
+                     "elect.sync _|e, 0xffffffff;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                     : "memory");
+    else
+        asm volatile("{\n\t.reg .pred e, p;\n\t"
+                     "elect.sync _|e, 0xffffffff;\n\t"
+                     "setp.ne.b32 p, %4, 0;\n\t"
+                     "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                     : "memory");
+}
+
+// kind::f16 with A from tensor memory, issued by one elected lane of a converged warp.
+__device__ __forceinline__ void mma_f16_tmem_a_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                     uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred e, p;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// tcgen05.commit (one CTA) from one elected lane of a converged warp.
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar)
+{
+    asm volatile("{\n\t.reg .pred e;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+                 : "memory");
+}
+
 // D (+)= A * B with A read from tensor memory (one TMEM lane per row of A,
 // two 16-bit elements per 32-bit column) and B from a shared-memory
 // descriptor: kind::f16, one CTA.
