@@ -270,7 +270,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         // The whole warp walks the schedule and waits; one elected lane issues
-        // each product and commit (see mma_elect).
+        // each product and commit.
         if (nkv > 0) {
             auto sync_abort = [&]() {
                 __syncwarp();
@@ -296,12 +296,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     const uint64_t b_desc = smem_desc_sw128(k_addr + slab * ATT_SLAB, 16u, 1024u);
 #pragma unroll
                     for (uint32_t k = 0; k < 4; ++k)
-                        mma_elect<1, KIND_F16>(tmem_base + g * ATT_BN, a_desc + 2u * k, b_desc + 2u * k, p.idesc_qk,
+                        mma<1, KIND_F16>(tmem_base + g * ATT_BN, a_desc + 2u * k, b_desc + 2u * k, p.idesc_qk,
                                                (slab > 0 || k > 0) ? 1u : 0u);
                 }
-                mma_commit_elect(s_full(g));
+                mma_commit(s_full(g));
                 if (g == 1)
-                    mma_commit_elect(k_empty(s));
+                    mma_commit(k_empty(s));
             };
             // O_g += P_g V_j, P_g from TMEM (16 products of 16 keys, 8 columns each);
             // after tile B, V_j's slot is free
@@ -321,12 +321,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                     const uint64_t b_desc = smem_desc_sw128(v_addr + slab * ATT_SLAB, 8192u, 1024u);
 #pragma unroll
                     for (uint32_t k = 0; k < 4; ++k)
-                        mma_f16_tmem_a_elect(tmem_base + ATT_O_COL + g * ATT_BN,
+                        mma_tmem_a(tmem_base + ATT_O_COL + g * ATT_BN,
                                              tmem_base + g * ATT_BN + slab * 32 + k * 8, b_desc + (2048u >> 4) * k,
                                              p.idesc_pv, (j > 0 || slab > 0 || k > 0) ? 1u : 0u);
                 }
                 if (g == 1)
-                    mma_commit_elect(v_empty(s));
+                    mma_commit(v_empty(s));
             };
             if (nkv_a > 0)
                 issue_qk(0, 0);
@@ -341,7 +341,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 if (j + 1 < nkv)
                     issue_qk(j + 1, 1);
             }
-            mma_commit_elect(done_bar);
+            mma_commit(done_bar);
             wait_drain<false>(done_bar, 0, w.limit_ns, w.id, w.status, SITE_ATT_DONE);
         }
     } else {

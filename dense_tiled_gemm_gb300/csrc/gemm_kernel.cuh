@@ -535,7 +535,13 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && (CG == 1 || rank == 0)) {
+        // The whole warp walks the job list and waits; one elected lane issues
+        // each product, copy and commit.
+        if (CG == 1 || rank == 0) {
+            auto sync_abort = [&]() {
+                __syncwarp();
+                w.aborted = __any_sync(0xffffffffu, w.aborted);
+            };
             // 8-bit and 4-bit operands are K-major only (the host rejects MN-major B for them).
             const bool b_mn = KIND == KIND_F16 && p.b_mn_major != 0;
             // K-major: rows of 128 B in 8-row groups 1024 B apart; one MMA step = 32 B.
@@ -547,10 +553,12 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
             for (int i = 0; i < num_jobs; ++i) {
                 const Job jb = sch.job(i);
                 wait_bounded<CG == 2>(w, tempty_bar(acc), acc_ph ^ 1u, SITE_MMA_TMEM_EMPTY);
+                sync_abort();
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * ACC_STRIDE;
                 for (int kb = jb.kb0; kb < jb.kb1; ++kb) {
                     wait_bounded<CG == 2>(w, full_bar(s), ph, SITE_MMA_FULL);
+                    sync_abort();
                     tc_fence_after_sync();
                     if (!w.aborted) {
                         const uint32_t a_addr = base + s * Cfg::STAGE_BYTES;
@@ -559,7 +567,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         sf_sel ^= 1u;
                         if constexpr (Cfg::SCALED) {
                             // this stage's scale atoms into TMEM, in smem order (A's, then B's);
-                            // later MMAs of this thread see them
+                            // later MMAs of the issuing lane see them
                             const uint32_t src = a_addr + Cfg::AB_BYTES;
 #pragma unroll
                             for (int t = 0; t < Cfg::SF_GROUPS * (1 + Cfg::SFB_ATOMS); ++t)

@@ -285,6 +285,17 @@ enum : int { KIND_F16 = 0, KIND_F8 = 1, KIND_MXF8 = 2, KIND_MXF4 = 3 };
 
 __host__ __device__ constexpr bool kind_scaled(int kind) { return kind == KIND_MXF8 || kind == KIND_MXF4; }
 
+// tcgen05.mma, tcgen05.cp and tcgen05.commit are each issued by one thread.
+// The wrappers below are called by a whole converged warp: the warp computes
+// the (warp-uniform) operands together, so that they stay in the uniform
+// datapath, and the lane that elect.sync picks issues the instruction (the
+// same lane every time, so its commits cover its products). Issued from a
+// single divergent lane instead, every instruction first moves its operands
+// there; with other warps of the same SM sub-partition competing for issue
+// slots, that stretched a 64-cycle product (M128 N128 K16) to about 100
+// cycles.
+#define DTG_ELECT_PRED "{\n\t.reg .pred e, p;\n\telect.sync _|e, 0xffffffff;\n\t"
+
 // D[tmem] (+)= A[smem] · B[smem] with an FP32 accumulator (unscaled kinds).
 template <int CG, int KIND>
 __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -292,140 +303,69 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b
 {
     static_assert(KIND == KIND_F16 || KIND == KIND_F8, "unscaled kinds only");
     if constexpr (CG == 1 && KIND == KIND_F16)
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "setp.ne.b32 p, %4, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        asm volatile(DTG_ELECT_PRED "setp.ne.b32 p, %4, 0;\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
                      : "memory");
     else if constexpr (CG == 2 && KIND == KIND_F16)
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "setp.ne.b32 p, %4, 0;\n\t"
-                     "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        asm volatile(DTG_ELECT_PRED "setp.ne.b32 p, %4, 0;\n\t"
+                     "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
                      : "memory");
     else if constexpr (CG == 1)
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "setp.ne.b32 p, %4, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        asm volatile(DTG_ELECT_PRED "setp.ne.b32 p, %4, 0;\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
                      : "memory");
     else
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "setp.ne.b32 p, %4, 0;\n\t"
-                     "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        asm volatile(DTG_ELECT_PRED "setp.ne.b32 p, %4, 0;\n\t"
+                     "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
                      : "memory");
+}
+
+// D (+)= A * B with A read from tensor memory (one TMEM lane per row of A,
+// two 16-bit elements per 32-bit column) and B from a shared-memory
+// descriptor: kind::f16, one CTA.
+__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate)
+{
+    asm volatile(DTG_ELECT_PRED "setp.ne.b32 p, %4, 0;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
 }
 
 // Block-scaled MMA: D[tmem] (+)= (SFA ∘ A)·(SFB ∘ B). sfa_tmem / sfb_tmem are
 // the tensor-memory addresses of the 32-bit columns that hold this
 // instruction's E8M0 scales (one byte per row, picked by the scale-ID fields
 // of idesc).
-// The unscaled product issued by one elected lane of a converged warp. The
-// warp computes the (warp-uniform) operands together, so they stay in the
-// uniform datapath; issued from a single divergent lane, every instruction
-// first pays for moving its operands there, and under issue pressure from
-// other warps of the sub-partition that roughly halves the rate of short
-// (64-cycle) products.
-template <int CG, int KIND>
-__device__ __forceinline__ void mma_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate)
-{
-    static_assert(KIND == KIND_F16 || KIND == KIND_F8, "unscaled kinds only");
-    if constexpr (CG == 1 && KIND == KIND_F16)
-        asm volatile("{\n\t.reg .pred e, p;\n\t"
-                     "elect.sync _|e, 0xffffffff;\n\t"
-                     "setp.ne.b32 p, %4, 0;\n\t"
-                     "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                     : "memory");
-    else if constexpr (CG == 2 && KIND == KIND_F16)
-        asm volatile("{\n\t.reg .pred e, p;\n\t"
-                     "elect.sync _|e, 0xffffffff;\n\t"
-                     "setp.ne.b32 p, %4, 0;\n\t"
-                     "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                     : "memory");
-    else if constexpr (CG == 1)
-        asm volatile("{\n\t.reg .pred e, p;\n\t"
-                     "elect.sync _|e, 0xffffffff;\n\t"
-                     "setp.ne.b32 p, %4, 0;\n\t"
-                     "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                     : "memory");
-    else
-        asm volatile("{\n\t.reg .pred e, p;\n\t"
-                     "elect.sync _|e, 0xffffffff;\n\t"
-                     "setp.ne.b32 p, %4, 0;\n\t"
-                     "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                     : "memory");
-}
-
-// kind::f16 with A from tensor memory, issued by one elected lane of a converged warp.
-__device__ __forceinline__ void mma_f16_tmem_a_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                                     uint32_t idesc, uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred e, p;\n\t"
-                 "elect.sync _|e, 0xffffffff;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
-// tcgen05.commit (one CTA) from one elected lane of a converged warp.
-__device__ __forceinline__ void mma_commit_elect(uint32_t bar)
-{
-    asm volatile("{\n\t.reg .pred e;\n\t"
-                 "elect.sync _|e, 0xffffffff;\n\t"
-                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
-                 : "memory");
-}
-
-// D (+)= A * B with A read from tensor memory (one TMEM lane per row of A,
-// two 16-bit elements per 32-bit column) and B from a shared-memory
-// descriptor: kind::f16, one CTA.
-__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate)
-{
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "setp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-                 : "memory");
-}
-
 template <int CG, int KIND>
 __device__ __forceinline__ void mma_scaled(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
 {
     static_assert(kind_scaled(KIND), "block-scaled kinds only");
     if constexpr (CG == 1 && KIND == KIND_MXF8)
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "setp.ne.b32 p, %6, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        asm volatile(DTG_ELECT_PRED "setp.ne.b32 p, %6, 0;\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
                      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
                      : "memory");
     else if constexpr (CG == 2 && KIND == KIND_MXF8)
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "setp.ne.b32 p, %6, 0;\n\t"
-                     "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
+        asm volatile(DTG_ELECT_PRED "setp.ne.b32 p, %6, 0;\n\t"
+                     "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X "
                      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
                      : "memory");
     else if constexpr (CG == 1)
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "setp.ne.b32 p, %6, 0;\n\t"
-                     "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X "
+        asm volatile(DTG_ELECT_PRED "setp.ne.b32 p, %6, 0;\n\t"
+                     "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X "
                      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
                      : "memory");
     else
-        asm volatile("{\n\t.reg .pred p;\n\t"
-                     "setp.ne.b32 p, %6, 0;\n\t"
-                     "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X "
+        asm volatile(DTG_ELECT_PRED "setp.ne.b32 p, %6, 0;\n\t"
+                     "@e tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X "
                      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
                      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
                      : "memory");
@@ -439,16 +379,21 @@ template <int CG>
 __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t s_desc)
 {
     if constexpr (CG == 1)
-        asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+        asm volatile(DTG_ELECT_PRED "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+                     "l"(s_desc)
+                     : "memory");
     else
-        asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+        asm volatile(DTG_ELECT_PRED "@e tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+                     "l"(s_desc)
+                     : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 operation this thread issued
+// Arrive once on `bar` when every tcgen05 operation the elected lane issued
 // before has completed. Single-CTA form.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+    asm volatile(DTG_ELECT_PRED
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
                  : "memory");
 }
 
@@ -456,11 +401,11 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 // `cta_mask` (bit i = cluster rank i).
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
 {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
-        : "memory");
+    asm volatile(DTG_ELECT_PRED
+                 "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%0], %1;\n\t}" ::"r"(bar),
+                 "h"(cta_mask)
+                 : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread t gets lane (base + t).
