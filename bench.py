@@ -104,14 +104,15 @@ def dist_env():
     return world, rank, local
 
 
-# The files the GEMM kernel and its launcher are built from; a profile summary
+# The files each kernel and its launcher are built from; a profile summary
 # names this hash, and its DRAM traffic is reported only while it matches.
 GEMM_SOURCES = ("gemm.cu", "gemm_kernel.cuh", "ptx.cuh", "schedule.cuh", "runtime.h")
+ATTENTION_SOURCES = GEMM_SOURCES + ("attention.cu", "attention_kernel.cuh")
 
 
-def source_hash() -> str:
+def source_hash(sources=GEMM_SOURCES) -> str:
     h = hashlib.sha256()
-    for name in GEMM_SOURCES:
+    for name in sources:
         with open(os.path.join(ROOT, "dense_tiled_gemm_gb300", "csrc", name), "rb") as fh:
             h.update(name.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -140,7 +141,7 @@ def measured_peaks():
         return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, sources=GEMM_SOURCES):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the kernel source as it is now; otherwise None."""
     for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
@@ -149,7 +150,7 @@ def profiled_traffic(workload: str):
         wl = re.search(r"^workload:\s*(\S+)", text, re.M)
         src = re.search(r"^source_sha256:\s*(\S+)", text, re.M)
         tr = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-        if wl and src and tr and wl.group(1) == workload and src.group(1) == source_hash():
+        if wl and src and tr and wl.group(1) == workload and src.group(1) == source_hash(sources):
             return float(tr.group(1))
     return None
 
@@ -604,7 +605,7 @@ def run_attention(args):
                        "causal": w.causal, "flops_per_step": w.flops,
                        "l2": f"rotating {n_sets} (Q, K, V, O) sets", "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak, "traffic": profiled_traffic(w.name, ATTENTION_SOURCES),
                          "peak_source": f"{peak_src} bf16_tflops (burst)", "kernel_ms": kernel_ms,
                          "frac_of_nominal": achieved / NOMINAL_DENSE_TFLOPS},
             "clocks": clocks, "gpu_launches": launches, "e2e": None, "cpu_baseline": cpu,
