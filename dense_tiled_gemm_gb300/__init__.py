@@ -166,13 +166,14 @@ def gemm_mx(A: torch.Tensor, B: torch.Tensor, SFA: torch.Tensor, SFB: torch.Tens
 
 def attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool = False,
               scale: float | None = None, O: torch.Tensor | None = None, return_lse: bool = False,
-              stream=None):
-    """O = softmax(scale * Q K^T) V per (batch, head) on Q's CUDA device (attention_fwd).
+              stream=None, max_ctas: int = 0):
+    """O = softmax(scale * Q K^T) V per (batch, head) on Q's CUDA device (attention_fwd_ex).
 
     Q: (B, H, Lq, 128), K and V: (B, H, Lk, 128), float16 or bfloat16, contiguous.
     ``causal``: key k is visible to row i iff k <= i + (Lk - Lq). ``scale`` defaults to
-    1/sqrt(128). Returns O (B, H, Lq, 128), and with ``return_lse`` also the FP32 row
-    log-sum-exp (B, H, Lq).
+    1/sqrt(128). ``max_ctas`` > 0 caps the persistent grid (each CTA then takes more
+    256-row blocks; the result is the same). Returns O (B, H, Lq, 128), and with
+    ``return_lse`` also the FP32 row log-sum-exp (B, H, Lq).
     """
     for name, t in (("Q", Q), ("K", K), ("V", V)):
         if t.device.type != "cuda" or not t.is_contiguous() or t.dim() != 4:
@@ -190,10 +191,11 @@ def attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor, *, causal: bool
     lse = torch.empty((B, H, Lq), dtype=torch.float32, device=Q.device) if return_lse else None
     scale = float(d) ** -0.5 if scale is None else float(scale)
     with torch.cuda.device(Q.device):
-        _check(binding.lib.attention_fwd(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
-                                         lse.data_ptr() if lse is not None else None, B, H, Lq, Lk, d,
-                                         _DT_IN[Q.dtype], int(bool(causal)), scale, _stream_ptr(stream)),
-               "attention_fwd")
+        _check(binding.lib.attention_fwd_ex(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(),
+                                            lse.data_ptr() if lse is not None else None, B, H, Lq, Lk, d,
+                                            _DT_IN[Q.dtype], int(bool(causal)), scale, int(max_ctas),
+                                            _stream_ptr(stream)),
+               "attention_fwd_ex")
     return (O, lse) if return_lse else O
 
 

@@ -91,8 +91,11 @@ def _declare(lib):
     lib.gemm_launch_count.restype = ctypes.c_uint64
     lib.gemm_launch_count.argtypes = []
     lib.attention_fwd.restype = c_int
+    lib.attention_fwd_ex.restype = c_int
     lib.attention_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_int,
                                   ctypes.c_float, vp]
+    lib.attention_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_int,
+                                     ctypes.c_float, c_int, vp]
     lib.gemm_schedule_jobs.restype = c_int
     lib.gemm_schedule_jobs.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(GemmJob), i32,
                                        ctypes.POINTER(i32)]

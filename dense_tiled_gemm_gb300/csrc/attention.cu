@@ -1,12 +1,14 @@
 // attention.cu: host side of attention_fwd (include/attention.h).
 //
-// One launch of attention_fwd_kernel per call: a grid of ceil(Lq / 256)
-// query row blocks (two 128-row tiles each) by B * H heads, 320 threads and
-// ~192 KB of shared memory per CTA, with programmatic stream serialisation like the GEMM. The tensor maps
+// One launch of attention_fwd_kernel per call: a persistent grid of one CTA
+// per SM (at most one per row block; ceil(Lq / 256) row blocks of two
+// 128-row tiles per head), 320 threads and ~192 KB of shared memory per CTA,
+// with programmatic stream serialisation like the GEMM. The tensor maps
 // view Q, K and V as 3-D (d, rows, B * H) so that a tile never reads into
 // the next head: rows past Lq or Lk come back as zeros.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -57,6 +59,13 @@ extern "C" gemm_status_t attention_fwd(const void *Q, const void *K, const void 
                                        int64_t B, int64_t H, int64_t Lq, int64_t Lk, int64_t d, int dtype,
                                        int causal, float scale, void *stream)
 {
+    return attention_fwd_ex(Q, K, V, O, LSE, B, H, Lq, Lk, d, dtype, causal, scale, 0, stream);
+}
+
+extern "C" gemm_status_t attention_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                                          int64_t B, int64_t H, int64_t Lq, int64_t Lk, int64_t d, int dtype,
+                                          int causal, float scale, int max_ctas, void *stream)
+{
     if (!Q || !K || !V || !O)
         return GEMM_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || Lq < 1 || Lk < 1 || d < 1 || Lq > INT32_MAX / 2 || Lk > INT32_MAX / 2)
@@ -91,6 +100,8 @@ extern "C" gemm_status_t attention_fwd(const void *Q, const void *K, const void 
     AttParams p = {};
     p.Lq = static_cast<int32_t>(Lq);
     p.Lk = static_cast<int32_t>(Lk);
+    p.BH = static_cast<int32_t>(bh);
+    p.nq = static_cast<int32_t>((Lq + ATT_ROWS - 1) / ATT_ROWS);
     p.causal = static_cast<uint32_t>(causal);
     p.bf16 = dtype == GEMM_BF16 ? 1u : 0u;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);   // log2(e)
@@ -104,7 +115,11 @@ extern "C" gemm_status_t attention_fwd(const void *Q, const void *K, const void 
     p.status = rt.status;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>((Lq + ATT_ROWS - 1) / ATT_ROWS), static_cast<unsigned>(bh));
+    // persistent: one CTA per SM, each walking row blocks blockIdx.x + k * gridDim.x
+    int64_t ctas = std::min<int64_t>(static_cast<int64_t>(p.nq) * bh, rt.sms);
+    if (max_ctas > 0)
+        ctas = std::min<int64_t>(ctas, max_ctas);
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
     cfg.blockDim = dim3(ATT_THREADS);
     cfg.dynamicSmemBytes = ATT_SMEM;
     cfg.stream = static_cast<cudaStream_t>(stream);

@@ -54,6 +54,20 @@ gemm_status_t attention_fwd(const void *Q, const void *K, const void *V, void *O
                             int64_t B, int64_t H, int64_t Lq, int64_t Lk, int64_t d,
                             int dtype, int causal, float scale, void *stream);
 
+/*
+ * attention_fwd_ex: attention_fwd with a cap on the persistent grid.
+ *
+ * The kernel runs one CTA per SM (never more than one per row block of 256
+ * query rows of one head); each CTA takes one row block per round of G (the
+ * grid size), rounds alternating in direction. max_ctas > 0 caps G, so that
+ * each CTA takes more row blocks (the tests use it to reach that path on
+ * small problems); max_ctas <= 0 means no cap. Arguments, results and errors are
+ * attention_fwd's; max_ctas changes neither the result nor its bits.
+ */
+gemm_status_t attention_fwd_ex(const void *Q, const void *K, const void *V, void *O, float *LSE,
+                               int64_t B, int64_t H, int64_t Lq, int64_t Lk, int64_t d,
+                               int dtype, int causal, float scale, int max_ctas, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -38,17 +38,19 @@ def bits(t):
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def run(dtg, Q, K, V, causal=False, scale=None):
-    O, lse = dtg.attention(Q.cuda(), K.cuda(), V.cuda(), causal=causal, scale=scale, return_lse=True)
+def run(dtg, Q, K, V, causal=False, scale=None, max_ctas=0):
+    O, lse = dtg.attention(Q.cuda(), K.cuda(), V.cuda(), causal=causal, scale=scale, return_lse=True,
+                           max_ctas=max_ctas)
     status, detail = dtg.gemm_last_device_status()
     assert status == dtg.GEMM_OK, f"device status {dtg.gemm_status_string(status)} site {detail:#x}"
     return O.cpu(), lse.cpu()
 
 
-def case(dtg, B, H, Lq, Lk, dtype="bf16", causal=False, seed=0, q_scale=1.0, rows=None, scale=None):
+def case(dtg, B, H, Lq, Lk, dtype="bf16", causal=False, seed=0, q_scale=1.0, rows=None, scale=None,
+         max_ctas=0):
     Q, K, V = workloads.make_attention_operands(B, H, Lq, Lk, 128, dtype, ("normal", 1.0), seed)
     Q = (Q.float() * q_scale).to(TDT[dtype])
-    O, lse = run(dtg, Q, K, V, causal, scale)
+    O, lse = run(dtg, Q, K, V, causal, scale, max_ctas)
     O_ref, O_abs, L_ref = oracle.attention_ref(bits(Q), bits(K), bits(V), B, H, Lq, Lk, 128, dtype, causal,
                                                scale, rows=rows)
     got = O.float().numpy().astype(np.float64).reshape(-1, 128)
@@ -122,3 +124,21 @@ def test_workload_sampled(dtg, name):
     total = w.B * w.H * w.Lq
     rows = sorted(set(workloads.sample_rows(total, 64, w.seed)) | {0, w.Lq - 1, total - 1})
     case(dtg, w.B, w.H, w.Lq, w.Lk, w.dtype, w.causal, w.seed, rows=rows)
+
+
+# ---------------------------------------------------------------- persistent CTAs, many row blocks each
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("shape,cap", [((2, 3, 1000, 777), 1), ((1, 5, 600, 1100), 2), ((3, 2, 513, 300), 3),
+                                       ((1, 2, 300, 100), 2)], ids=lambda v: "x".join(map(str, v))
+                         if isinstance(v, tuple) else f"cap{v}")
+def test_capped_grid(dtg, shape, cap, causal):
+    """A capped grid makes every CTA walk several row blocks (different key-block
+    counts under the causal mask, rows with no visible key when Lk < Lq): the ring
+    and barrier phases carried from one block to the next must give the oracle's
+    result, and the same bits as the uncapped launch."""
+    B, H, Lq, Lk = shape
+    case(dtg, B, H, Lq, Lk, "bf16", causal, seed=sum(shape) + cap, max_ctas=cap)
+    Q, K, V = workloads.make_attention_operands(B, H, Lq, Lk, 128, "f16", ("normal", 1.0), 7)
+    O1, l1 = run(dtg, Q, K, V, causal, None, 0)
+    O2, l2 = run(dtg, Q, K, V, causal, None, cap)
+    assert torch.equal(O1, O2) and torch.equal(l1, l2)

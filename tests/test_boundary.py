@@ -38,7 +38,7 @@ def test_header_declares_the_entry_points():
     for required in ("gemm", "gemm_ex", "gemm_plan", "gemm_from_host", "gemm_last_device_status",
                      "gemm_status_string", "gemm_selftest_wait_timeout", "gemm_launch_count",
                      "gemm_release_workspace", "gemm_mx", "gemm_mx_ex", "gemm_mx_plan",
-                     "gemm_schedule_jobs", "gemm_no_alloc", "attention_fwd"):
+                     "gemm_schedule_jobs", "gemm_no_alloc", "attention_fwd", "attention_fwd_ex"):
         assert required in names
 
 
@@ -156,6 +156,14 @@ def att_call(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, lse=None, B=1, H=1, Lq=128, Lk=128,
 ])
 def test_attention_rejects_on_host(kwargs, expect):
     assert att_call(**kwargs) == expect
+    # the capped-grid entry validates the same way, whatever the cap
+    a = dict(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, lse=None, B=1, H=1, Lq=128, Lk=128, d=128, dt=1, causal=0,
+             scale=0.088)
+    a.update(kwargs)
+    for cap in (0, 3, -1):
+        assert binding.lib.attention_fwd_ex(a["Q"], a["K"], a["V"], a["O"], a["lse"], a["B"], a["H"], a["Lq"],
+                                            a["Lk"], a["d"], a["dt"], a["causal"], a["scale"], cap,
+                                            None) == expect
 
 
 def test_attention_no_device():
