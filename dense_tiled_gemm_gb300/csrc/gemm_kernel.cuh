@@ -10,9 +10,9 @@
 //
 //   warp 0     producer: one thread issues TMA loads of A and B k-blocks into
 //              a ring of STAGES shared-memory slots;
-//   warp 1     MMA issuer: one thread issues tcgen05.mma on each filled slot
-//              and frees it with tcgen05.commit; the warp owns the TMEM
-//              allocation;
+//   warp 1     MMA issuer: the warp walks the job list together and one
+//              elected lane issues tcgen05.mma on each filled slot and frees
+//              it with tcgen05.commit; the warp owns the TMEM allocation;
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator, FP32 -> output cast,
 //              swizzled staging in shared memory, TMA store.
 //
