@@ -330,14 +330,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             tc_fence_after_sync();
             // S_g(j) = Q_g K_j^T into tile g's score buffer; after tile B, K_j's slot
             // is free, and after tile B's last one, so is Q
-            auto issue_qk = [&](int j, uint32_t g) {
-                const uint32_t r = rb + j, s = r % ATT_STAGES, ph = (r / ATT_STAGES) & 1;
-                if (g == 0 || j >= nkv_a)
-                    wait_bounded<false>(w, k_full(s), ph, SITE_ATT_K_FULL);
-                sync_abort();
-                tc_fence_after_sync();
-                if (w.aborted)
-                    return;
+            auto mma_qk = [&](int j, uint32_t g) {
+                const uint32_t r = rb + j, s = r % ATT_STAGES;
                 const uint32_t k_addr = base + ATT_K_OFF + s * ATT_TILE;
                 const uint32_t q_addr = base + ATT_Q_OFF + g * ATT_TILE;
 #pragma unroll
@@ -358,15 +352,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
             };
             // O_g += P_g V_j, P_g from TMEM (16 products of 16 keys, 8 columns each);
             // after tile B, V_j's slot is free
-            auto issue_pv = [&](int j, uint32_t g) {
-                const uint32_t r = rb + j, s = r % ATT_STAGES, ph = (r / ATT_STAGES) & 1;
-                wait_bounded<false>(w, p_full(g), (pb[g] + j) & 1, SITE_ATT_P_FULL);
-                if (g == 0 || j >= nkv_a)
-                    wait_bounded<false>(w, v_full(s), ph, SITE_ATT_V_FULL);
-                sync_abort();
-                tc_fence_after_sync();
-                if (w.aborted)
-                    return;
+            auto mma_pv = [&](int j, uint32_t g) {
+                const uint32_t r = rb + j, s = r % ATT_STAGES;
                 const uint32_t v_addr = base + ATT_V_OFF + s * ATT_TILE;
 #pragma unroll
                 for (int slab = 0; slab < 2; ++slab) {
@@ -380,20 +367,53 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_co
                 if (g == 1)
                     mma_commit(v_empty(s));
             };
-            if (nkv_a > 0)
-                issue_qk(0, 0);
-            issue_qk(0, 1);
+            auto wait_k = [&](int j) {
+                const uint32_t r = rb + j;
+                wait_bounded<false>(w, k_full(r % ATT_STAGES), (r / ATT_STAGES) & 1, SITE_ATT_K_FULL);
+            };
+            auto wait_v = [&](int j) {
+                const uint32_t r = rb + j;
+                wait_bounded<false>(w, v_full(r % ATT_STAGES), (r / ATT_STAGES) & 1, SITE_ATT_V_FULL);
+            };
+            // Each step waits for its ring slots first (they fill well ahead) and
+            // for the group's probabilities last, so that once those arrive the
+            // products issue back to back.
+            wait_k(0);
+            sync_abort();
+            tc_fence_after_sync();
+            if (!w.aborted) {
+                if (nkv_a > 0)
+                    mma_qk(0, 0);
+                mma_qk(0, 1);
+            }
             for (int j = 0; j < nkv; ++j) {
                 if (j < nkv_a) {
-                    issue_pv(j, 0);
-                    if (j + 1 == nkv_a)
-                        mma_commit(done(0));   // tile A's output may be read
-                    else
-                        issue_qk(j + 1, 0);    // tile A's next scores while group B finishes block j
+                    wait_v(j);
+                    if (j + 1 < nkv_a)
+                        wait_k(j + 1);
+                    wait_bounded<false>(w, p_full(0), (pb[0] + j) & 1, SITE_ATT_P_FULL);
+                    sync_abort();
+                    tc_fence_after_sync();
+                    if (!w.aborted) {
+                        mma_pv(j, 0);
+                        if (j + 1 == nkv_a)
+                            mma_commit(done(0));   // tile A's output may be read
+                        else
+                            mma_qk(j + 1, 0);      // tile A's next scores while group B finishes block j
+                    }
                 }
-                issue_pv(j, 1);
-                if (j + 1 < nkv)
-                    issue_qk(j + 1, 1);
+                if (j >= nkv_a)
+                    wait_v(j);
+                if (j + 1 < nkv && j + 1 >= nkv_a)
+                    wait_k(j + 1);
+                wait_bounded<false>(w, p_full(1), (pb[1] + j) & 1, SITE_ATT_P_FULL);
+                sync_abort();
+                tc_fence_after_sync();
+                if (!w.aborted) {
+                    mma_pv(j, 1);
+                    if (j + 1 < nkv)
+                        mma_qk(j + 1, 1);
+                }
             }
             mma_commit(done(1));
             ++nd;
