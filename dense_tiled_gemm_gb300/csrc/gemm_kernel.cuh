@@ -73,14 +73,14 @@ __host__ __device__ constexpr int kind_slab_k(int kind) { return kind == KIND_F1
 // whole tile width). The MMA thread copies them into a TMEM scale buffer
 // before the stage's MMAs; tcgen05.cp and tcgen05.mma of one thread run in
 // issue order. Consecutive stages alternate between two buffers, at columns
-// SF_COL0 and SF_COL0 + 256 (beside each accumulator), so a stage's copies
+// columns BN and BN + 256 (beside each accumulator), so a stage's copies
 // never overwrite scales that the previous stage's MMAs may still read and
 // the tensor pipe does not drain between stages. Accumulators use columns
-// [0, BN) and [256, 256 + BN), so block-scaled tiles are at most 224 wide.
+// [0, BN) and [256, 256 + BN), so block-scaled tiles are at most 224 wide
+// (192 wide for packed FP4 stages of two slabs, whose scales take 48 columns).
 constexpr int SF_ATOM_BYTES = 512;
 constexpr int SF_ATOM_ROWS = 32;
 constexpr int SF_ROW_BYTES = 16;
-constexpr uint32_t SF_COL0 = 224;
 constexpr int MX_MAX_STAGES = 8;
 constexpr int NUM_THREADS = 192;     // producer warp, MMA warp, 4 epilogue warps
 constexpr int EPI_WARP0 = 2;
@@ -150,10 +150,11 @@ struct TileConfig {
     static constexpr int SFB_BYTES = SF_GROUPS * SFB_ATOMS * SF_ATOM_BYTES;
     static constexpr int STAGE_BYTES = AB_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int STAGE_TX = STAGE_BYTES;   // bytes the TMA engine delivers per stage and CTA
-    // TMEM scale buffer (at SF_COL0, or SF_COL0 + 256 for odd stages): A at +4g,
+    // TMEM scale buffer (at SF_COL = BN, or SF_COL + 256 for odd stages): A at +4g,
     // B at +4 * SF_GROUPS + 4 * (g * SFB_ATOMS + atom)
-    static constexpr uint32_t SFB_COL = SF_COL0 + 4u * SF_GROUPS;
-    static_assert(!SCALED || (SF_GROUPS >= 1 && SFB_COL + 4u * SF_GROUPS * SFB_ATOMS <= 256u),
+    static constexpr uint32_t SF_COL = SCALED ? static_cast<uint32_t>(BN) : 0u;
+    static constexpr uint32_t SFB_COL = SF_COL + 4u * SF_GROUPS;
+    static_assert(!SCALED || (SF_GROUPS >= 1 && SF_COL % 4u == 0 && SFB_COL + 4u * SF_GROUPS * SFB_ATOMS <= 256u),
                   "the TMEM scale buffer fits between the two accumulators");
     // TMA x coordinate units per slab: FP16/BF16 elements, or bytes for the 8- and 4-bit kinds
     static constexpr int SLAB_X = KIND == KIND_F16 ? 64 : 128;
@@ -562,8 +563,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     tc_fence_after_sync();
                     if (!w.aborted) {
                         const uint32_t a_addr = base + s * Cfg::STAGE_BYTES;
-                        const uint32_t sf_a = tmem_base + SF_COL0 + 256u * sf_sel;
-                        const uint32_t sf_b = sf_a + (Cfg::SFB_COL - SF_COL0);
+                        const uint32_t sf_a = tmem_base + Cfg::SF_COL + 256u * sf_sel;
+                        const uint32_t sf_b = sf_a + (Cfg::SFB_COL - Cfg::SF_COL);
                         sf_sel ^= 1u;
                         if constexpr (Cfg::SCALED) {
                             // this stage's scale atoms into TMEM, in smem order (A's, then B's);

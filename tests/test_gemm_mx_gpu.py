@@ -129,3 +129,17 @@ def test_workload_sampled(dtg, name):
     ok, ratio, n_bad, first = tolerance.check(C.float().cpu().numpy().astype(np.float64)[rows], C_ref, C_abs,
                                               w.dtype_out)
     assert ok, f"{n_bad} out of bound (worst {ratio:.3g}) first {first}"
+
+
+# ---------------------------------------------------------------- both MXFP4 stage depths
+@pytest.mark.parametrize("shape", [(512, 448, 2048), (300, 500, 700), (257, 225, 100)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("k_stage", [256, 512], ids=["one_slab_224", "two_slabs_192"])
+def test_mxfp4_stage_depths_integer_exact(dtg, shape, k_stage):
+    """Packed FP4 runs 192-wide tiles with two-slab (512 K) stages by default and
+    224-wide tiles with one-slab stages on request; both place their scales in
+    TMEM beside the accumulators and must match the oracle bit for bit."""
+    plan = dtg.gemm_plan(*shape, dtype_in=torch.uint8, dtype_out=torch.float32, block_scaled=True,
+                         options={"k_stage": k_stage})
+    assert plan["block_n"] == (224 if k_stage == 256 else 192)
+    exact_case(dtg, *shape, "mxfp4", options={"k_stage": k_stage}, seed=sum(shape) + k_stage)
