@@ -76,7 +76,8 @@ extern "C" gemm_status_t attention_fwd_ex(const void *Q, const void *K, const vo
         return GEMM_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.0f))
         return GEMM_ERR_INVALID_ARG;
-    if (d != ATT_D || B * H > 65535)
+    // heads index a 1-D persistent grid's row blocks and a tensor map dimension (int32)
+    if (d != ATT_D || B > INT32_MAX || H > INT32_MAX || B * H > INT32_MAX)
         return GEMM_ERR_UNSUPPORTED;
     for (const void *ptr : {Q, K, V, const_cast<const void *>(O)})
         if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0)

@@ -37,7 +37,7 @@ extern "C" {
  *   LSE     device pointer, [B][H][Lq] FP32 natural-log row log-sum-exp
  *           (written), or NULL. A row with no visible key gets -inf and an
  *           all-zero O row.
- *   B, H, Lq, Lk  sizes >= 1, B * H <= 65535.
+ *   B, H, Lq, Lk  sizes >= 1, B * H <= 2^31 - 1 (GEMM_ERR_UNSUPPORTED otherwise).
  *   d       head dimension; must be 128 (otherwise GEMM_ERR_UNSUPPORTED).
  *   dtype   GEMM_F16 or GEMM_BF16 for Q, K, V and O.
  *   causal  0: every key is visible; 1: key k is visible to query row i iff

@@ -142,3 +142,10 @@ def test_capped_grid(dtg, shape, cap, causal):
     O1, l1 = run(dtg, Q, K, V, causal, None, 0)
     O2, l2 = run(dtg, Q, K, V, causal, None, cap)
     assert torch.equal(O1, O2) and torch.equal(l1, l2)
+
+
+def test_many_heads(dtg):
+    """70,007 heads of 3 query rows and 5 keys: more (batch, head) pairs than a 2-D
+    grid's y extent, so each persistent CTA walks hundreds of row blocks."""
+    case(dtg, 7, 10001, 3, 5, "bf16", False, seed=31)
+    case(dtg, 7, 10001, 3, 5, "bf16", True, seed=32)

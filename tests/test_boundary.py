@@ -152,7 +152,7 @@ def att_call(Q=FAKE, K=FAKE, V=FAKE, O=FAKE, lse=None, B=1, H=1, Lq=128, Lk=128,
     (dict(Q=None), 1), (dict(O=None), 1), (dict(B=0), 1), (dict(Lk=0), 1), (dict(dt=7), 1),
     (dict(dt=2), 2), (dict(d=64), 2), (dict(causal=2), 1), (dict(scale=float("inf")), 1),
     (dict(scale=0.0), 1), (dict(scale=-0.5), 1),
-    (dict(B=300, H=300), 2), (dict(Q=FAKE + 8), 2), (dict(lse=FAKE + 2), 1),
+    (dict(B=65536, H=32768), 2), (dict(B=1 << 31, H=1), 2), (dict(Q=FAKE + 8), 2), (dict(lse=FAKE + 2), 1),
 ])
 def test_attention_rejects_on_host(kwargs, expect):
     assert att_call(**kwargs) == expect
