@@ -49,6 +49,14 @@ FALLBACK_BF16_TFLOPS = 1900.0
 NOMINAL_DENSE_TFLOPS = 2250.0     # GB300 dense FP16/BF16 tensor peak, nominal
 FP8_RATE = 2.0                    # nominal dense FP8 / FP16 rate on GB300 (4.5 vs 2.25 PFLOP/s)
 FP4_RATE = 6.0                    # nominal dense FP4 / FP16 rate on GB300 (13.5 vs 2.25 PFLOP/s)
+# Dense tensor flop per SM clock, measured with back-to-back tcgen05.mma products:
+# FP16/BF16 8,192; FP8 and MXFP8 twice that; every packed-FP4 form four times.
+FLOP_PER_SM_CLOCK = {1.0: 8192.0, FP8_RATE: 16384.0, FP4_RATE: 32768.0}
+
+
+def clock_peak_tflops(rate: float, sms: int, sm_mhz: float) -> float:
+    """Tensor peak at the sampled SM clock: SMs x measured flop per SM clock x clock."""
+    return sms * FLOP_PER_SM_CLOCK[rate] * sm_mhz * 1e6 / 1e12
 
 
 def is_mx(w) -> bool:
@@ -483,9 +491,11 @@ def run_ours(args):
             "cublas_comparison": cublas,
         }
         line["roofline"]["frac_of_nominal"] = achieved / nominal
-        if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
-            line["roofline"]["frac_of_nominal_at_measured_clock"] = achieved / (
-                nominal * clocks["sm_mhz"] / clocks["sm_max_mhz"])
+        if clocks and clocks.get("sm_mhz"):
+            cp = clock_peak_tflops(rate, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                   clocks["sm_mhz"])
+            line["roofline"]["clock_peak_tflops"] = cp
+            line["roofline"]["frac_of_clock_peak"] = achieved / cp
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
@@ -611,6 +621,11 @@ def run_attention(args):
             "clocks": clocks, "gpu_launches": launches, "e2e": None, "cpu_baseline": cpu,
             "library_comparison": comparison,
         }
+        if clocks and clocks.get("sm_mhz"):
+            cp = clock_peak_tflops(1.0, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                   clocks["sm_mhz"])
+            line["roofline"]["clock_peak_tflops"] = cp
+            line["roofline"]["frac_of_clock_peak"] = achieved / cp
         print(json.dumps(line), flush=True)
     if pg:
         pg.destroy_process_group()
