@@ -38,9 +38,9 @@ constexpr uint64_t DEFAULT_TIMEOUT_MS = 2000;
 // stage leaves room for only two of them).
 int default_k_slabs(int cg, int kind)
 {
-    // Packed FP4 slabs already hold 256 K: one per stage, in 224-wide tiles. Two per
-    // stage (k_stage = 512) need 48 TMEM columns of scales, so 192-wide tiles; at
-    // 4096 x 4096 x 65536 those measure 441 us against 361 us.
+    // Pairs take stages of two 128-byte slabs (256 K of FP8), except packed FP4: its
+    // slabs already hold 256 K, and at 4096 x 4096 x 65536 one-slab stages (six in
+    // the ring) measure 357 us against 376 us for two-slab ones (three in the ring).
     return kind == KIND_MXF4 ? 1 : cg == 2 ? 2 : 1;
 }
 
@@ -66,7 +66,7 @@ const Variant kVariants[] = {
     variant<2, 256, 2, KIND_F16>(true),  variant<2, 224, 2, KIND_F16>(false), variant<1, 256, 2, KIND_F16>(true),
     variant<2, 256, 1, KIND_F8>(false),  variant<2, 224, 1, KIND_F8>(false),  variant<1, 256, 1, KIND_F8>(false),
     variant<2, 256, 2, KIND_F8>(false),  variant<2, 224, 2, KIND_F8>(false),  variant<1, 256, 2, KIND_F8>(false),
-    variant<2, 224, 2, KIND_MXF8>(false), variant<2, 224, 1, KIND_MXF4>(false), variant<2, 192, 2, KIND_MXF4>(false),
+    variant<2, 224, 2, KIND_MXF8>(false), variant<2, 224, 1, KIND_MXF4>(false), variant<2, 224, 2, KIND_MXF4>(false),
 };
 constexpr int NUM_VARIANTS = sizeof(kVariants) / sizeof(kVariants[0]);
 
@@ -490,7 +490,7 @@ cudaError_t launch_any(const Variant &v, int grid_ctas, uint32_t smem, const CUt
     DTG_LAUNCH(1, 256, 2, KIND_F8)
     DTG_LAUNCH(2, 224, 2, KIND_MXF8)
     DTG_LAUNCH(2, 224, 1, KIND_MXF4)
-    DTG_LAUNCH(2, 192, 2, KIND_MXF4)
+    DTG_LAUNCH(2, 224, 2, KIND_MXF4)
 #undef DTG_LAUNCH
     return cudaErrorInvalidValue;
 }

@@ -70,14 +70,13 @@ __host__ __device__ constexpr int kind_slab_k(int kind) { return kind == KIND_F1
 // all N columns of the instruction (each CTA of a pair holds all of them), in
 // the byte its descriptor's scale-ID picks. A ring stage carries SF_GROUPS
 // groups of 4 blocks: per group one atom of A and SFB_ATOMS atoms of B (the
-// whole tile width). The MMA thread copies them into a TMEM scale buffer
-// before the stage's MMAs; tcgen05.cp and tcgen05.mma of one thread run in
-// issue order. Consecutive stages alternate between two buffers, at columns
-// columns BN and BN + 256 (beside each accumulator), so a stage's copies
-// never overwrite scales that the previous stage's MMAs may still read and
-// the tensor pipe does not drain between stages. Accumulators use columns
-// [0, BN) and [256, 256 + BN), so block-scaled tiles are at most 224 wide
-// (192 wide for packed FP4 stages of two slabs, whose scales take 48 columns).
+// whole tile width). Before each K slab's MMAs the MMA warp copies that
+// slab's groups into a TMEM scale buffer; tcgen05.cp and tcgen05.mma of one
+// thread run in issue order. Consecutive slabs alternate between two
+// buffers, at columns BN and BN + 256 (beside each accumulator), so a slab's
+// copies never overwrite scales that the previous slab's MMAs may still read
+// and the tensor pipe does not drain between slabs. Accumulators use columns
+// [0, BN) and [256, 256 + BN), so block-scaled tiles are at most 224 wide.
 constexpr int SF_ATOM_BYTES = 512;
 constexpr int SF_ATOM_ROWS = 32;
 constexpr int SF_ROW_BYTES = 16;
@@ -150,12 +149,15 @@ struct TileConfig {
     static constexpr int SFB_BYTES = SF_GROUPS * SFB_ATOMS * SF_ATOM_BYTES;
     static constexpr int STAGE_BYTES = AB_BYTES + SFA_BYTES + SFB_BYTES;
     static constexpr int STAGE_TX = STAGE_BYTES;   // bytes the TMA engine delivers per stage and CTA
-    // TMEM scale buffer (at SF_COL = BN, or SF_COL + 256 for odd stages): A at +4g,
-    // B at +4 * SF_GROUPS + 4 * (g * SFB_ATOMS + atom)
+    // TMEM scale buffers, one per K slab, alternating between SF_COL = BN and
+    // SF_COL + 256: a slab's groups g < SLAB_SF_GROUPS, A at +4g, B at
+    // +4 * SLAB_SF_GROUPS + 4 * (g * SFB_ATOMS + atom)
+    static constexpr int SLAB_SF_GROUPS = SCALED ? SLAB_K / 128 : 0;
     static constexpr uint32_t SF_COL = SCALED ? static_cast<uint32_t>(BN) : 0u;
-    static constexpr uint32_t SFB_COL = SF_COL + 4u * SF_GROUPS;
-    static_assert(!SCALED || (SF_GROUPS >= 1 && SF_COL % 4u == 0 && SFB_COL + 4u * SF_GROUPS * SFB_ATOMS <= 256u),
-                  "the TMEM scale buffer fits between the two accumulators");
+    static constexpr uint32_t SF_B_OFF = 4u * SLAB_SF_GROUPS;
+    static_assert(!SCALED || (SLAB_SF_GROUPS >= 1 && SF_COL % 4u == 0 &&
+                              SF_COL + SF_B_OFF + 4u * SLAB_SF_GROUPS * SFB_ATOMS <= 256u),
+                  "a slab's TMEM scale buffer fits between the two accumulators");
     // TMA x coordinate units per slab: FP16/BF16 elements, or bytes for the 8- and 4-bit kinds
     static constexpr int SLAB_X = KIND == KIND_F16 ? 64 : 128;
     // K blocks of 32 per MMA: 2 for packed FP4 (K = 64), else 1 (K <= 32)
@@ -563,22 +565,31 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     tc_fence_after_sync();
                     if (!w.aborted) {
                         const uint32_t a_addr = base + s * Cfg::STAGE_BYTES;
-                        const uint32_t sf_a = tmem_base + Cfg::SF_COL + 256u * sf_sel;
-                        const uint32_t sf_b = sf_a + (Cfg::SFB_COL - Cfg::SF_COL);
-                        sf_sel ^= 1u;
-                        if constexpr (Cfg::SCALED) {
-                            // this stage's scale atoms into TMEM, in smem order (A's, then B's);
-                            // later MMAs of the issuing lane see them
-                            const uint32_t src = a_addr + Cfg::AB_BYTES;
-#pragma unroll
-                            for (int t = 0; t < Cfg::SF_GROUPS * (1 + Cfg::SFB_ATOMS); ++t)
-                                tmem_cp_32x128b_warpx4<CG>(sf_a + 4u * t, smem_desc_plain(src + t * SF_ATOM_BYTES, 128u));
-                        }
 #pragma unroll
                         for (int j = 0; j < KS; ++j) {
                             // a slab wholly past K holds only TMA zero fill: skip its MMAs
                             if (j > 0 && kb * Cfg::STAGE_K + j * Cfg::SLAB_K >= p.K)
                                 break;
+                            // this slab's scale atoms (its groups of the stage's A atoms, then of
+                            // its B atoms) into the next scale buffer; later MMAs of the issuing
+                            // lane see them
+                            const uint32_t sf_a = tmem_base + Cfg::SF_COL + 256u * sf_sel;
+                            const uint32_t sf_b = sf_a + Cfg::SF_B_OFF;
+                            if constexpr (Cfg::SCALED) {
+                                sf_sel ^= 1u;
+                                const uint32_t src_a = a_addr + Cfg::AB_BYTES, src_b = src_a + Cfg::SFA_BYTES;
+#pragma unroll
+                                for (int gi = 0; gi < Cfg::SLAB_SF_GROUPS; ++gi) {
+                                    const int gs = j * Cfg::SLAB_SF_GROUPS + gi;
+                                    tmem_cp_32x128b_warpx4<CG>(sf_a + 4u * gi,
+                                                               smem_desc_plain(src_a + gs * SF_ATOM_BYTES, 128u));
+#pragma unroll
+                                    for (int at = 0; at < Cfg::SFB_ATOMS; ++at)
+                                        tmem_cp_32x128b_warpx4<CG>(
+                                            sf_b + 4u * (gi * Cfg::SFB_ATOMS + at),
+                                            smem_desc_plain(src_b + (gs * Cfg::SFB_ATOMS + at) * SF_ATOM_BYTES, 128u));
+                                }
+                            }
                             const uint64_t a_desc = smem_desc_sw128(a_addr + j * Cfg::A_SLAB, 16u, 1024u);
                             const uint64_t b_desc = smem_desc_sw128(a_addr + Cfg::A_BYTES + j * Cfg::B_SLAB,
                                                                     b_lbo, 1024u);
@@ -586,9 +597,9 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                             for (uint32_t k = 0; k < SLAB_MMAS; ++k) {
                                 const uint32_t acc_in = (kb > jb.kb0 || j > 0 || k > 0) ? 1u : 0u;
                                 if constexpr (Cfg::SCALED) {
-                                    // first 32-K block of this MMA within the stage: its scales
-                                    // are byte blk % 4 of atom blk / 4 (4 TMEM columns)
-                                    const uint32_t blk = (j * SLAB_MMAS + k) * Cfg::MMA_SF_BLOCKS;
+                                    // first 32-K block of this MMA within the slab: its scales
+                                    // are byte blk % 4 of the slab's atom blk / 4 (4 TMEM columns)
+                                    const uint32_t blk = k * Cfg::MMA_SF_BLOCKS;
                                     mma_scaled<CG, KIND>(d_tmem, a_desc + 2u * k, b_desc + b_step * k,
                                                          p.idesc | mx_sf_id(blk % 4u), sf_a + 4u * (blk / 4u),
                                                          sf_b + 4u * Cfg::SFB_ATOMS * (blk / 4u), acc_in);

@@ -134,12 +134,12 @@ def test_workload_sampled(dtg, name):
 # ---------------------------------------------------------------- both MXFP4 stage depths
 @pytest.mark.parametrize("shape", [(512, 448, 2048), (300, 500, 700), (257, 225, 100)],
                          ids=lambda s: "x".join(map(str, s)))
-@pytest.mark.parametrize("k_stage", [256, 512], ids=["one_slab_224", "two_slabs_192"])
+@pytest.mark.parametrize("k_stage", [256, 512], ids=["one_slab", "two_slabs"])
 def test_mxfp4_stage_depths_integer_exact(dtg, shape, k_stage):
-    """Packed FP4 runs 192-wide tiles with two-slab (512 K) stages by default and
-    224-wide tiles with one-slab stages on request; both place their scales in
-    TMEM beside the accumulators and must match the oracle bit for bit."""
+    """Packed FP4 runs one-slab (256 K) stages by default and two-slab stages on
+    request; each slab's scales go to the next of two TMEM buffers beside the
+    accumulators. Both must match the oracle bit for bit."""
     plan = dtg.gemm_plan(*shape, dtype_in=torch.uint8, dtype_out=torch.float32, block_scaled=True,
                          options={"k_stage": k_stage})
-    assert plan["block_n"] == (224 if k_stage == 256 else 192)
+    assert plan["block_n"] == 224 and plan["block_k"] == k_stage
     exact_case(dtg, *shape, "mxfp4", options={"k_stage": k_stage}, seed=sum(shape) + k_stage)
