@@ -491,6 +491,11 @@ def run_ours(args):
             "cublas_comparison": cublas,
         }
         line["roofline"]["frac_of_nominal"] = achieved / nominal
+        if "bf16_tflops_sustained" in peaks:
+            # cuBLAS in a seconds-long loop under the power cap: the figure for runs the cap reaches
+            sus = float(peaks["bf16_tflops_sustained"]) * rate
+            line["roofline"]["sustained_peak"] = sus
+            line["roofline"]["frac_of_sustained_peak"] = achieved / sus
         if clocks and clocks.get("sm_mhz"):
             cp = clock_peak_tflops(rate, torch.cuda.get_device_properties(dev).multi_processor_count,
                                    clocks["sm_mhz"])
@@ -621,6 +626,10 @@ def run_attention(args):
             "clocks": clocks, "gpu_launches": launches, "e2e": None, "cpu_baseline": cpu,
             "library_comparison": comparison,
         }
+        if "bf16_tflops_sustained" in peaks:
+            sus = float(peaks["bf16_tflops_sustained"])
+            line["roofline"]["sustained_peak"] = sus
+            line["roofline"]["frac_of_sustained_peak"] = achieved / sus
         if clocks and clocks.get("sm_mhz"):
             cp = clock_peak_tflops(1.0, torch.cuda.get_device_properties(dev).multi_processor_count,
                                    clocks["sm_mhz"])
