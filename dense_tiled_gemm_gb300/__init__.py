@@ -18,7 +18,8 @@ from .binding import (GEMM_BF16, GEMM_E2M1, GEMM_E4M3, GEMM_E5M2, GEMM_F16, GEMM
                       GEMM_MN_MAJOR, GEMM_OK, GEMM_ERR_TIMEOUT, GEMM_JOB_FULL, GEMM_JOB_OWNER,
                       GEMM_JOB_WRITER, GemmError, GemmJob, GemmOptions, GemmPlan, STATUS_NAMES)
 
-__all__ = ["gemm", "gemm_ex", "gemm_mx", "attention", "gemm_plan", "gemm_from_host", "gemm_release_workspace",
+__all__ = ["gemm", "gemm_ex", "gemm_mx", "attention", "gemm_plan", "gemm_from_host", "gemm_from_host_async",
+           "gemm_release_workspace",
            "gemm_last_device_status", "gemm_selftest_wait_timeout", "gemm_status_string",
            "gemm_launch_count", "gemm_schedule_jobs", "GemmError", "GemmOptions", "GemmPlan"]
 
@@ -226,6 +227,22 @@ def gemm_from_host(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = No
                                           _DT_IN[A.dtype], _DT_OUT[C.dtype], GEMM_K_MAJOR,
                                           _LAYOUT[layout_b], _stream_ptr(stream)),
                "gemm_from_host")
+    return C
+
+
+def gemm_from_host_async(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *,
+                   layout_b: str = "k", out_dtype: torch.dtype | None = None, stream=None,
+                   device=None) -> torch.Tensor:
+    """gemm_from_host without the final synchronisation: C is complete once ``stream``
+    (default: the current stream) has passed the call; A and B must stay unchanged until
+    then. Consecutive calls overlap one call's uploads with the previous call's product
+    and read-back. Use pinned host tensors for the overlap."""
+    M, N, K, C = _prepare(A, B, C, layout_b, out_dtype, "cpu")
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        _check(binding.lib.gemm_from_host_async(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                                          _DT_IN[A.dtype], _DT_OUT[C.dtype], GEMM_K_MAJOR,
+                                          _LAYOUT[layout_b], _stream_ptr(stream)),
+               "gemm_from_host_async")
     return C
 
 

@@ -80,6 +80,8 @@ def _declare(lib):
     lib.gemm_mx_plan.argtypes = lib.gemm_plan.argtypes
     lib.gemm_from_host.restype = c_int
     lib.gemm_from_host.argtypes = gemm_args + [vp]
+    lib.gemm_from_host_async.restype = c_int
+    lib.gemm_from_host_async.argtypes = gemm_args + [vp]
     lib.gemm_release_workspace.restype = c_int
     lib.gemm_release_workspace.argtypes = []
     lib.gemm_last_device_status.restype = c_int

@@ -95,9 +95,19 @@ struct DeviceState {
     int sms = 0;
     unsigned long long *status = nullptr;
     int max_units[NUM_VARIANTS] = {};   // co-resident CTAs (cg 1) or CTA pairs (cg 2)
+    // gemm_from_host(_async) staging: two slots of device copies of A, B and C, so
+    // that one call's uploads (on h2d) overlap the previous call's product and
+    // read-back (on the caller's stream)
     std::mutex ws_mu;
-    void *ws = nullptr;
-    size_t ws_bytes = 0;
+    struct HostSlot {
+        void *ws = nullptr;
+        size_t bytes = 0;
+        cudaEvent_t uploaded = nullptr;   // A and B are on the device
+        cudaEvent_t released = nullptr;   // the product and the read-back of C are done
+        bool used = false;
+    } slots[2];
+    unsigned next_slot = 0;
+    cudaStream_t h2d = nullptr;
 };
 
 std::mutex g_mu;
@@ -786,8 +796,8 @@ gemm_status_t gemm_mx_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dt
     return plan_query(M, N, K, dtype_in, dtype_out, layoutA, layoutB, A, B, C, opts, plan, true);
 }
 
-gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_host, int64_t M, int64_t N,
-                             int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB, void *stream)
+gemm_status_t gemm_from_host_async(const void *A_host, const void *B_host, void *C_host, int64_t M, int64_t N,
+                                   int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB, void *stream)
 {
     gemm_status_t rc = validate(A_host, B_host, C_host, M, N, K, dtype_in, dtype_out, layoutA, layoutB,
                                 nullptr);
@@ -804,32 +814,64 @@ gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_hos
     const size_t c_bytes = static_cast<size_t>(M * N * out_bytes(dtype_out));
     const size_t need = up256(a_bytes) + up256(b_bytes) + up256(c_bytes);
     std::lock_guard<std::mutex> lock(d->ws_mu);
-    if (d->ws_bytes < need) {
-        if (d->ws) {
-            cudaFree(d->ws);   // synchronises the device
-            d->ws = nullptr;
-            d->ws_bytes = 0;
+    auto cuda_failed = [](cudaError_t e) {
+        if (e == cudaSuccess)
+            return false;
+        cudaGetLastError();
+        return true;
+    };
+    if (!d->h2d && cuda_failed(cudaStreamCreateWithFlags(&d->h2d, cudaStreamNonBlocking)))
+        return GEMM_ERR_CUDA;
+    DeviceState::HostSlot &slot = d->slots[d->next_slot];
+    if (!slot.uploaded && (cuda_failed(cudaEventCreateWithFlags(&slot.uploaded, cudaEventDisableTiming)) ||
+                           cuda_failed(cudaEventCreateWithFlags(&slot.released, cudaEventDisableTiming))))
+        return GEMM_ERR_CUDA;
+    if (slot.bytes < need) {
+        // the slot's previous call must be done with it before it is replaced
+        if (slot.used && cuda_failed(cudaEventSynchronize(slot.released)))
+            return GEMM_ERR_CUDA;
+        if (slot.ws) {
+            cudaFree(slot.ws);
+            slot.ws = nullptr;
+            slot.bytes = 0;
         }
-        if (cudaMalloc(&d->ws, need) != cudaSuccess) {
+        if (cudaMalloc(&slot.ws, need) != cudaSuccess) {
             cudaGetLastError();
-            d->ws = nullptr;
+            slot.ws = nullptr;
             return GEMM_ERR_OUT_OF_MEMORY;
         }
-        d->ws_bytes = need;
+        slot.bytes = need;
+        slot.used = false;
     }
-    char *dA = static_cast<char *>(d->ws);
+    char *dA = static_cast<char *>(slot.ws);
     char *dB = dA + up256(a_bytes);
     char *dC = dB + up256(b_bytes);
-    if (cudaMemcpyAsync(dA, A_host, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(dB, B_host, b_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
-        cudaGetLastError();
+    // uploads on the library's copy stream, once the slot's previous product and read-back are done
+    if ((slot.used && cuda_failed(cudaStreamWaitEvent(d->h2d, slot.released, 0))) ||
+        cuda_failed(cudaMemcpyAsync(dA, A_host, a_bytes, cudaMemcpyHostToDevice, d->h2d)) ||
+        cuda_failed(cudaMemcpyAsync(dB, B_host, b_bytes, cudaMemcpyHostToDevice, d->h2d)) ||
+        cuda_failed(cudaEventRecord(slot.uploaded, d->h2d)) || cuda_failed(cudaStreamWaitEvent(st, slot.uploaded, 0)))
         return GEMM_ERR_CUDA;
-    }
+    // the product and the read-back on the caller's stream
     rc = run(dA, dB, nullptr, nullptr, dC, M, N, K, dtype_in, dtype_out, layoutA, layoutB, nullptr, st);
     if (rc != GEMM_OK)
         return rc;
-    if (cudaMemcpyAsync(C_host, dC, c_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        cudaStreamSynchronize(st) != cudaSuccess) {
+    if (cuda_failed(cudaMemcpyAsync(C_host, dC, c_bytes, cudaMemcpyDeviceToHost, st)) ||
+        cuda_failed(cudaEventRecord(slot.released, st)))
+        return GEMM_ERR_CUDA;
+    slot.used = true;
+    d->next_slot ^= 1u;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_host, int64_t M, int64_t N,
+                             int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB, void *stream)
+{
+    gemm_status_t rc = gemm_from_host_async(A_host, B_host, C_host, M, N, K, dtype_in, dtype_out, layoutA,
+                                            layoutB, stream);
+    if (rc != GEMM_OK)
+        return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -843,13 +885,18 @@ gemm_status_t gemm_release_workspace(void)
     if (rc != GEMM_OK)
         return rc;
     std::lock_guard<std::mutex> lock(d->ws_mu);
-    if (d->ws) {
-        if (cudaFree(d->ws) != cudaSuccess) {
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    for (DeviceState::HostSlot &slot : d->slots) {
+        if (slot.ws && cudaFree(slot.ws) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
-        d->ws = nullptr;
-        d->ws_bytes = 0;
+        slot.ws = nullptr;
+        slot.bytes = 0;
+        slot.used = false;
     }
     return GEMM_OK;
 }

@@ -230,17 +230,34 @@ gemm_status_t gemm_mx_plan(int64_t M, int64_t N, int64_t K,
  * pageable). It copies A and B to a device workspace, runs gemm on `stream`,
  * copies C back, and synchronises the stream before returning: C_host is
  * complete when the call returns GEMM_OK. The workspace belongs to the
- * library. It is cached per device and grows to the largest problem seen;
- * gemm_release_workspace frees it. The errors are gemm's, plus
- * GEMM_ERR_OUT_OF_MEMORY when the workspace cannot grow.
+ * library: two staging slots per device, each cached and grown to the
+ * largest problem seen; gemm_release_workspace frees them. The errors are
+ * gemm's, plus GEMM_ERR_OUT_OF_MEMORY when a slot cannot grow.
  */
 gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_host,
                              int64_t M, int64_t N, int64_t K,
                              int dtype_in, int dtype_out, int layoutA, int layoutB,
                              void *stream);
 
-/* Free the gemm_from_host workspace of the current device. Synchronises the
- * device first. */
+/*
+ * gemm_from_host_async: gemm_from_host without the final synchronisation.
+ * The uploads of A and B run on a copy stream of the library, in the next of
+ * the two staging slots, once that slot's previous call has finished with
+ * it; the product and the read-back of C run on `stream`, after the uploads.
+ * So consecutive calls overlap: one call's uploads run while the previous
+ * call's product and read-back run. C_host is complete once `stream` has
+ * passed the call (cudaStreamSynchronize, or an event recorded after it);
+ * A_host and B_host must stay unchanged until then. With pinned host memory
+ * the call returns without waiting for the copies. Arguments and errors are
+ * gemm_from_host's.
+ */
+gemm_status_t gemm_from_host_async(const void *A_host, const void *B_host, void *C_host,
+                                   int64_t M, int64_t N, int64_t K,
+                                   int dtype_in, int dtype_out, int layoutA, int layoutB,
+                                   void *stream);
+
+/* Free the gemm_from_host staging slots of the current device. Synchronises
+ * the device first. */
 gemm_status_t gemm_release_workspace(void);
 
 /*

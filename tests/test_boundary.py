@@ -38,7 +38,8 @@ def test_header_declares_the_entry_points():
     for required in ("gemm", "gemm_ex", "gemm_plan", "gemm_from_host", "gemm_last_device_status",
                      "gemm_status_string", "gemm_selftest_wait_timeout", "gemm_launch_count",
                      "gemm_release_workspace", "gemm_mx", "gemm_mx_ex", "gemm_mx_plan",
-                     "gemm_schedule_jobs", "gemm_no_alloc", "attention_fwd", "attention_fwd_ex"):
+                     "gemm_schedule_jobs", "gemm_no_alloc", "attention_fwd", "attention_fwd_ex",
+                     "gemm_from_host_async"):
         assert required in names
 
 

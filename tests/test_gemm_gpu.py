@@ -257,6 +257,27 @@ def test_from_host_matches_device(dtg):
     dtg.gemm_release_workspace()
 
 
+def test_from_host_async_overlapping_calls(dtg):
+    """Five asynchronous host calls in flight at once, of three sizes (the two staging
+    slots grow while the other slot is still busy), each with its own pinned inputs and
+    output: after one synchronisation every C equals the device-side gemm bit for bit."""
+    shapes = [(300, 400, 500), (700, 900, 600), (300, 400, 500), (1000, 520, 777), (64, 64, 64)]
+    cases = []
+    for i, (M, N, K) in enumerate(shapes):
+        A, B = workloads.make_operands(M, N, K, "bf16", "k", ("normal", 1.0), 40 + i)
+        Ah, Bh = A.pin_memory(), B.pin_memory()
+        Ch = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+        dtg.gemm_from_host_async(Ah, Bh, Ch, out_dtype=torch.float32)
+        cases.append((A, B, Ch))
+    torch.cuda.synchronize()
+    for A, B, Ch in cases:
+        C_dev = run_gpu(dtg, A, B, "k", "f32")
+        assert torch.equal(Ch, C_dev.cpu())
+    status, detail = dtg.gemm_last_device_status()
+    assert status == dtg.GEMM_OK
+    dtg.gemm_release_workspace()
+
+
 def test_plan_reports_launch(dtg):
     p = dtg.gemm_plan(4096, 4096, 8192)
     assert p["cta_group"] == 2 and p["block_k"] == 128 and p["num_sms"] > 0
