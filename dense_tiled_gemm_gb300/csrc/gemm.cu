@@ -35,13 +35,14 @@ constexpr uint64_t DEFAULT_TIMEOUT_MS = 2000;
 // K per ring stage, unless gemm_options_t.k_stage says otherwise: 128 for CTA
 // pairs (8 MMAs per barrier wait; the MMA issuer's wait costs ~60-100 cycles
 // of tensor idle, so fewer waits per MMA pay), 64 for single CTAs (a 128-deep
-// stage leaves room for only two of them).
+// stage leaves room for only two of them); one slab for the block-scaled kinds.
 int default_k_slabs(int cg, int kind)
 {
-    // Pairs take stages of two 128-byte slabs (256 K of FP8), except packed FP4: its
-    // slabs already hold 256 K, and at 4096 x 4096 x 65536 one-slab stages (six in
-    // the ring) measure 357 us against 376 us for two-slab ones (three in the ring).
-    return kind == KIND_MXF4 ? 1 : cg == 2 ? 2 : 1;
+    // Pairs take stages of two 128-byte slabs (256 K of FP8), except the
+    // block-scaled kinds: at 4096 x 4096 x 65536 one-slab stages (six in the
+    // ring) measure 357 us against 376 us for two-slab ones (three in the ring)
+    // with packed FP4, and 701-744 us against 782-792 us with MXFP8.
+    return kind_scaled(kind) ? 1 : cg == 2 ? 2 : 1;
 }
 
 struct Variant {
@@ -66,7 +67,8 @@ const Variant kVariants[] = {
     variant<2, 256, 2, KIND_F16>(true),  variant<2, 224, 2, KIND_F16>(false), variant<1, 256, 2, KIND_F16>(true),
     variant<2, 256, 1, KIND_F8>(false),  variant<2, 224, 1, KIND_F8>(false),  variant<1, 256, 1, KIND_F8>(false),
     variant<2, 256, 2, KIND_F8>(false),  variant<2, 224, 2, KIND_F8>(false),  variant<1, 256, 2, KIND_F8>(false),
-    variant<2, 224, 2, KIND_MXF8>(false), variant<2, 224, 1, KIND_MXF4>(false), variant<2, 224, 2, KIND_MXF4>(false),
+    variant<2, 224, 1, KIND_MXF8>(false), variant<2, 224, 2, KIND_MXF8>(false),
+    variant<2, 224, 1, KIND_MXF4>(false), variant<2, 224, 2, KIND_MXF4>(false),
 };
 constexpr int NUM_VARIANTS = sizeof(kVariants) / sizeof(kVariants[0]);
 
@@ -498,6 +500,7 @@ cudaError_t launch_any(const Variant &v, int grid_ctas, uint32_t smem, const CUt
     DTG_LAUNCH(2, 256, 2, KIND_F8)
     DTG_LAUNCH(2, 224, 2, KIND_F8)
     DTG_LAUNCH(1, 256, 2, KIND_F8)
+    DTG_LAUNCH(2, 224, 1, KIND_MXF8)
     DTG_LAUNCH(2, 224, 2, KIND_MXF8)
     DTG_LAUNCH(2, 224, 1, KIND_MXF4)
     DTG_LAUNCH(2, 224, 2, KIND_MXF4)

@@ -147,8 +147,11 @@ struct TileConfig {
     static constexpr int SFB_ATOMS = (BN + 127) / 128;
     static constexpr int SFA_BYTES = SF_GROUPS * SF_ATOM_BYTES;
     static constexpr int SFB_BYTES = SF_GROUPS * SFB_ATOMS * SF_ATOM_BYTES;
-    static constexpr int STAGE_BYTES = AB_BYTES + SFA_BYTES + SFB_BYTES;
-    static constexpr int STAGE_TX = STAGE_BYTES;   // bytes the TMA engine delivers per stage and CTA
+    static constexpr int STAGE_TX = AB_BYTES + SFA_BYTES + SFB_BYTES;   // bytes TMA delivers per stage and CTA
+    // distance between ring slots: the next 1024-byte boundary, so that every
+    // slot's slabs keep the alignment of the 128-byte swizzle (one-slab MXFP8
+    // stages carry 31.5 KB)
+    static constexpr int STAGE_BYTES = (STAGE_TX + 1023) / 1024 * 1024;
     // TMEM scale buffers, one per K slab, alternating between SF_COL = BN and
     // SF_COL + 256: a slab's groups g < SLAB_SF_GROUPS, A at +4g, B at
     // +4 * SLAB_SF_GROUPS + 4 * (g * SFB_ATOMS + atom)

@@ -156,7 +156,10 @@ gemm_status_t gemm_mx(const void *A, const void *B, const uint8_t *SFA, const ui
  *   timeout_ms    per-wait limit inside the kernel (default 2000).
  *   k_stage       K depth of one shared-memory ring stage, in elements: one or
  *                 two 128-byte slabs, so 64 or 128 for FP16/BF16 and 128 or
- *                 256 for FP8. Other values give GEMM_ERR_UNSUPPORTED.
+ *                 256 for FP8 (and for MXFP8), 256 or 512 for packed FP4.
+ *                 The default (0) is two slabs for CTA pairs, one slab for
+ *                 single CTAs and for the block-scaled kinds. Other values
+ *                 give GEMM_ERR_UNSUPPORTED.
  *   stream_k      tail scheduling: 0 lets the planner choose, 1 keeps every
  *                 tile whole (data-parallel), 2 forces stream-K on the last
  *                 tiles (see gemm_schedule_jobs). Other values give
@@ -182,7 +185,8 @@ gemm_status_t gemm_ex(const void *A, const void *B, void *C,
                       const gemm_options_t *opts, void *stream);
 
 /* gemm_mx with overrides (cta_group must be 0 or 2, block_n 0 or 224,
- * k_stage 0 or the one offered depth: 256 for MXFP8, 256 for MXFP4). */
+ * k_stage 0 or one of the offered depths: 128 or 256 for MXFP8, 256 or 512
+ * for MXFP4). */
 gemm_status_t gemm_mx_ex(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C,
                          int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA,
                          int layoutB, const gemm_options_t *opts, void *stream);

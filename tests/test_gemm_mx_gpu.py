@@ -143,3 +143,15 @@ def test_mxfp4_stage_depths_integer_exact(dtg, shape, k_stage):
                          options={"k_stage": k_stage})
     assert plan["block_n"] == 224 and plan["block_k"] == k_stage
     exact_case(dtg, *shape, "mxfp4", options={"k_stage": k_stage}, seed=sum(shape) + k_stage)
+
+
+@pytest.mark.parametrize("shape", [(512, 448, 1024), (300, 500, 700), (257, 225, 100)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("k_stage", [128, 256], ids=["one_slab", "two_slabs"])
+def test_mxfp8_stage_depths_integer_exact(dtg, shape, k_stage):
+    """MXFP8 stages hold one 128-K slab (one scale group per stage) or two; both
+    must match the oracle bit for bit, ragged K included."""
+    plan = dtg.gemm_plan(*shape, dtype_in=torch.float8_e4m3fn, dtype_out=torch.float32, block_scaled=True,
+                         options={"k_stage": k_stage})
+    assert plan["block_n"] == 224 and plan["block_k"] == k_stage
+    exact_case(dtg, *shape, "mxfp8", options={"k_stage": k_stage}, seed=sum(shape) + k_stage)
