@@ -248,6 +248,26 @@ def test_headline_shape_integer_exact(dtg):
     exact_case(dtg, 4096, 4096, 8192, "f16", "k", seed=12, rows=workloads.sample_rows(4096, 64, 12))
 
 
+@pytest.mark.parametrize("N", [32776, 32769], ids=["tma_store", "direct_store"])
+def test_output_beyond_int32_elements(dtg, N):
+    """C with more than 2^31 elements (4.3 GB of FP16): row offsets past the
+    32-bit range, through the TMA store (pitch a multiple of 16 bytes) and
+    through the direct store (odd N). Sampled rows, first and last included,
+    are bit-exact on small integers."""
+    M, K = 65573, 72
+    assert M * N > 2**31
+    A, B = workloads.make_operands(M, N, K, "f16", "k", ("int", -3, 3), 21)
+    C = run_gpu(dtg, A, B, "k", "f16")
+    plan = dtg.gemm_plan(M, N, K, dtype_in=torch.float16, dtype_out=torch.float16)
+    assert plan["direct_store"] == (1 if N % 8 else 0)
+    rows = sorted(set([0, 1, M // 2, M - 2, M - 1] + list(workloads.sample_rows(M, 8, 21))))
+    got = C[torch.tensor(rows, device=C.device)].float().cpu().numpy().astype(np.float64)
+    del C
+    C_ref, _ = oracle.gemm_ref(workloads.as_bits(A), workloads.as_bits(B), M, N, K, "f16", "k", rows=rows)
+    bad = np.argwhere(got != C_ref)
+    assert bad.size == 0, f"{len(bad)} inexact elements, first {tuple(bad[0])}"
+
+
 # ---------------------------------------------------------------- other entry points
 def test_from_host_matches_device(dtg):
     A, B = workloads.make_operands(700, 900, 600, "f16", "k", ("normal", 1.0), 13)
