@@ -748,6 +748,17 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     st_release_gpu(&p.flags[static_cast<size_t>(blockIdx.x) * 4u + quarter], p.launch_id);
                 }
             }
+            if (jb.kind == JOB_OWNER && !skip) {
+                // Every writer's partial has been read: clear the flags this owner
+                // consumed (each has exactly one reader). A replay of the same
+                // launch (a captured CUDA graph keeps its launch id and its
+                // workspace) then cannot mistake the last replay's flags for new ones.
+                __syncwarp();
+                if (lane == 0)
+                    for (int u = cluster_id - 1; u >= w_first; --u)
+                        if (sch.has_range(u))
+                            p.flags[(static_cast<size_t>(u) * CG + rank) * 4u + quarter] = 0ull;
+            }
             if (++acc == 2) {
                 acc = 0;
                 acc_ph ^= 1u;

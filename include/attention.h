@@ -46,7 +46,8 @@ extern "C" {
  *   stream  cudaStream_t as void*.
  *
  * Base addresses must be 16-byte aligned (GEMM_ERR_UNSUPPORTED otherwise).
- * The caller owns all memory; nothing is allocated. Errors: host-side
+ * The caller owns all memory; nothing is allocated. The call may be captured
+ * into a CUDA graph once one call on the device has run outside the capture. Errors: host-side
  * argument checks return before launch; a kernel wait past its limit (2 s)
  * is reported through gemm_last_device_status.
  */

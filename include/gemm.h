@@ -27,6 +27,11 @@
  *     default stream.
  *   - Host-side argument errors are reported by the return value before
  *     anything is enqueued. They never abort the process.
+ *   - The stream-taking calls (gemm, gemm_ex, gemm_mx, gemm_mx_ex,
+ *     gemm_no_alloc) may be captured into a CUDA graph once one call on the
+ *     device has run outside the capture (per-device setup). A replay runs
+ *     the captured launch again, with the captured pointers, and gives the
+ *     same result as a new call on the same inputs.
  */
 #ifndef DENSE_TILED_GEMM_GEMM_H
 #define DENSE_TILED_GEMM_GEMM_H
