@@ -99,6 +99,9 @@ def parse_args():
     ap.add_argument("--stream-k", choices=["auto", "off", "on"], default="auto",
                     help="tail scheduling of the GEMM (gemm_options_t.stream_k); auto = the planner")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the timed steps into one CUDA graph and time its replay "
+                         "(no per-launch host cost; GEMM workloads)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
     return ap.parse_args()
@@ -373,13 +376,13 @@ def run_ours(args):
 
     opts = None if args.stream_k == "auto" else {"stream_k": {"off": 1, "on": 2}[args.stream_k]}
 
-    def step(i):
+    def step(i, st=stream):
         j = i % n_sets
         if is_mx(w):
             A, B, SFA, SFB = sets[j]
-            dtg.gemm_mx(A, B, SFA, SFB, Cs[j], K=w.K, stream=stream, options=opts)
+            dtg.gemm_mx(A, B, SFA, SFB, Cs[j], K=w.K, stream=st, options=opts)
         else:
-            dtg.gemm(As[j], Bs[j], Cs[j], layout_b=w.layout_b, stream=stream, options=opts)
+            dtg.gemm(As[j], Bs[j], Cs[j], layout_b=w.layout_b, stream=st, options=opts)
 
     for i in range(args.warmup):
         step(i)
@@ -397,20 +400,38 @@ def run_ours(args):
         smi_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:  # noqa: BLE001  (older torch: fall back to the CUDA index)
         smi_id = str(local)
+    graph = None
+    if args.graph:
+        # the same steps, captured once (launches are counted at capture) and replayed
+        # once untimed; the timed region is then one replay on this stream
+        graph = torch.cuda.CUDAGraph()
+        torch.cuda.synchronize(dev)
+        launches0 = dtg.gemm_launch_count()
+        with torch.cuda.graph(graph):
+            for i in range(args.steps):
+                step(args.warmup + i, st=None)
+        launches = dtg.gemm_launch_count() - launches0
+        graph.replay()
+        torch.cuda.synchronize(dev)
     sampler = ClockSampler(smi_id)
     sampler.start()
     if pg:
         pg.barrier()
     torch.cuda.synchronize(dev)
-    launches0 = dtg.gemm_launch_count()
+    if graph is None:
+        launches0 = dtg.gemm_launch_count()
     ev_start.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i)
+    if graph is None:
+        for i in range(args.steps):
+            step(args.warmup + i)
+    else:
+        graph.replay()
     ev_end.record(stream)
     torch.cuda.synchronize(dev)
     if pg:
         pg.barrier()
-    launches = dtg.gemm_launch_count() - launches0
+    if graph is None:
+        launches = dtg.gemm_launch_count() - launches0
     clocks = sampler.stop()
     status, detail = dtg.gemm_last_device_status(stream)
     if status != dtg.GEMM_OK:
@@ -486,7 +507,9 @@ def run_ours(args):
                        "dtype_out": w.dtype_out, "layout_b": w.layout_b,
                        "l2": f"rotating {n_sets} operand sets "
                              f"({n_sets * set_bytes / 1e6:.0f} MB > 2 x {l2 / 1e6:.0f} MB L2)",
-                       "parallelism": f"replicas x{world}", "plan": plan},
+                       "parallelism": f"replicas x{world}", "plan": plan,
+                       "timing": "one CUDA graph replay of all steps" if graph is not None
+                                 else "back-to-back launches"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                          "peak_source": peak_note,
@@ -654,6 +677,8 @@ def main():
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the GEMM workloads"}))
             return 0
+        if args.graph:
+            sys.exit("--graph times GEMM workloads only (an attention launch is not launch-bound)")
         return run_attention(args)
     if args.impl == "reference":
         return run_reference(args)
