@@ -77,6 +77,7 @@ constexpr int NUM_VARIANTS = sizeof(kVariants) / sizeof(kVariants[0]);
 struct Layout {
     uint32_t stages;
     uint32_t staging_bytes;
+    uint32_t staging_bufs;
     uint32_t smem;
 };
 
@@ -85,10 +86,20 @@ Layout layout_for(const Variant &v, int dtype_out)
     Layout l;
     l.staging_bytes = dtype_out == GEMM_F32 ? 4096u : 2048u;
     // block-scaled kinds keep one TMEM scale slot per ring stage (MX_MAX_STAGES of them)
-    l.stages = kind_scaled(v.kind) ? MX_MAX_STAGES : MAX_STAGES;
-    while (l.stages > 2 && smem_bytes_for(v.stage_bytes, l.stages, l.staging_bytes) > SMEM_LIMIT)
-        --l.stages;
-    l.smem = smem_bytes_for(v.stage_bytes, l.stages, l.staging_bytes);
+    const uint32_t max_stages = kind_scaled(v.kind) ? MX_MAX_STAGES : MAX_STAGES;
+    auto deepest = [&](uint32_t bufs) {
+        uint32_t st = max_stages;
+        while (st > 2 && smem_bytes_for(v.stage_bytes, st, l.staging_bytes, bufs) > SMEM_LIMIT)
+            --st;
+        return st;
+    };
+    // Four staging buffers per epilogue warp where they fit and cost no ring
+    // stage: a chunk's TMA store then rarely waits for the store three chunks back.
+    const uint32_t d4 = deepest(4);
+    l.staging_bufs =
+        (d4 == deepest(2) && smem_bytes_for(v.stage_bytes, d4, l.staging_bytes, 4u) <= SMEM_LIMIT) ? 4u : 2u;
+    l.stages = deepest(l.staging_bufs);
+    l.smem = smem_bytes_for(v.stage_bytes, l.stages, l.staging_bytes, l.staging_bufs);
     return l;
 }
 
@@ -597,6 +608,7 @@ gemm_status_t encode_and_launch(const DeviceState &d, const Plan &pl, Operand a,
     const Layout lay = layout_for(var, dtype_out);
     kp.stages = lay.stages;
     kp.staging_bytes = lay.staging_bytes;
+    kp.staging_bufs = lay.staging_bufs;
     kp.C = C;
     kp.sk_tiles = pl.sk_tiles;
     if (pl.sk_tiles) {

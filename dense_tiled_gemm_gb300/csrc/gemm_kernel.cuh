@@ -113,6 +113,7 @@ struct KernelParams {
     uint32_t direct_store;     // 1: write C with ordinary stores (unaligned C)
     uint32_t stages;           // ring depth (2 .. MAX_STAGES)
     uint32_t staging_bytes;    // one epilogue staging buffer: 32 rows x 32 columns of C
+    uint32_t staging_bufs;     // staging buffers per epilogue warp: 2 or 4
     void *C;                   // used by the direct-store path
     int32_t sk_tiles;          // trailing tiles scheduled stream-K (0: all tiles data-parallel)
     float4 *partials;          // stream-K partial sums: one slot per CTA (128 rows x block_n FP32)
@@ -170,13 +171,13 @@ struct TileConfig {
 
 // Dynamic shared memory, from a 1024-byte aligned base:
 //   ring      stages x {KS slabs of A 128 x 128 B, KS slabs of B BN_CTA x 128 B} (128-byte swizzle)
-//   staging   4 epilogue warps x 2 buffers x staging_bytes (2 KB for 16-bit C, 4 KB for FP32 C)
+//   staging   4 epilogue warps x 2 or 4 buffers x staging_bytes (2 KB for 16-bit C, 4 KB for FP32 C)
 //   barriers  full[stages], empty[stages], tmem_full[2], tmem_empty[2], mma_done
 //   TMEM base address written by tcgen05.alloc
 __host__ __device__ constexpr uint32_t smem_bytes_for(uint32_t stage_bytes, uint32_t stages,
-                                                      uint32_t staging_bytes)
+                                                      uint32_t staging_bytes, uint32_t staging_bufs)
 {
-    return stages * stage_bytes + 8u * staging_bytes + (2u * stages + 5u) * 8u + 16u;
+    return stages * stage_bytes + 4u * staging_bufs * staging_bytes + (2u * stages + 5u) * 8u + 16u;
 }
 
 // ------------------------------------------------------------------ bounded waits
@@ -410,7 +411,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
     const int num_clusters = static_cast<int>(gridDim.x) / CG;
 
     const uint32_t staging_off = stages * Cfg::STAGE_BYTES;
-    const uint32_t bar_off = staging_off + 8u * p.staging_bytes;
+    const uint32_t bar_off = staging_off + 4u * p.staging_bufs * p.staging_bytes;
     const uint32_t bar0 = base + bar_off;
     auto full_bar = [&](uint32_t s) { return bar0 + 8u * s; };
     auto empty_bar = [&](uint32_t s) { return bar0 + 8u * (stages + s); };
@@ -642,7 +643,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
     } else {
         // ------------------------------------------------------------ epilogue
         const uint32_t quarter = warp & 3u;      // the TMEM lane quarter this warp may access
-        const uint32_t staging = base + staging_off + (warp - EPI_WARP0) * 2u * p.staging_bytes;
+        const uint32_t staging = base + staging_off + (warp - EPI_WARP0) * p.staging_bufs * p.staging_bytes;
         const uint64_t c_policy = l2_evict_first_policy();   // C is written once: keep A and B in L2
         constexpr int CHUNKS = BN / EPI_COLS;
         // Stream-K partial slot of CTA `cta`, this warp's 32 rows, chunk c: 32 lanes x 8 float4,
@@ -684,8 +685,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * EPI_COLS), v);
                     tmem_ld_wait();
                 }
-                if (c == CHUNKS - 1) {
-                    // accumulator fully read: hand it back to the MMA issuer
+                if (c == CHUNKS - 1 && i + 1 < num_jobs) {
+                    // accumulator fully read: hand it back to the MMA issuer (after this
+                    // unit's last tile nothing waits for it; teardown's cluster barrier
+                    // orders the reads before TMEM is freed)
                     tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0 && !skip) {
@@ -728,8 +731,13 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     continue;
                 }
                 const uint32_t buf = staging + sb * p.staging_bytes;
-                if (lane == 0)
-                    bulk_wait_group_read<1>();   // the store that last used `buf` has read it
+                if (lane == 0) {
+                    // the store that last used `buf` has read it
+                    if (p.staging_bufs == 4)
+                        bulk_wait_group_read<3>();
+                    else
+                        bulk_wait_group_read<1>();
+                }
                 __syncwarp();
                 stage_row(buf, lane, v, p.out_dtype);
                 fence_proxy_async_smem();
@@ -738,7 +746,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     tma_store_2d_hint(&tmap_c, buf, gcol, row0, c_policy);
                     bulk_commit_group();
                 }
-                sb ^= 1u;
+                sb = (sb + 1u) & (p.staging_bufs - 1u);
             }
             if (jb.kind == JOB_WRITER && !skip) {
                 // publish: every lane's partial stores, then the flag
