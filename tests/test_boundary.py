@@ -89,6 +89,21 @@ def test_invalid_arguments_rejected_on_host(kwargs, expect):
     assert call(**kwargs) == expect
 
 
+@pytest.mark.parametrize("fn", ["gemm_from_host", "gemm_from_host_async", "gemm_no_alloc"])
+@pytest.mark.parametrize("kwargs,expect", [
+    (dict(a=None), 1), (dict(c=None), 1), (dict(K=0), 1), (dict(N=-1), 1), (dict(din=7), 1),
+    (dict(din=2), 2), (dict(dout=3), 2), (dict(la=1), 2), (dict(din=3, lb=1), 2), (dict(din=5), 2),
+])
+def test_other_entry_points_validate_on_host(fn, kwargs, expect):
+    """The host-buffer and allocation-free entry points run the same argument
+    checks before they touch a device (or, here, find none)."""
+    args = dict(M=64, N=64, K=64, din=0, dout=0, la=0, lb=0, a=FAKE, b=FAKE, c=FAKE)
+    args.update(kwargs)
+    rc = getattr(binding.lib, fn)(args["a"], args["b"], args["c"], args["M"], args["N"], args["K"],
+                                  args["din"], args["dout"], args["la"], args["lb"], None)
+    assert rc == expect
+
+
 def test_invalid_options_rejected_on_host():
     for field, val, expect in (("cta_group", 3, 1), ("cta_group", -1, 1), ("block_n", 128, 2),
                                ("max_clusters", -2, 1), ("group_m", -1, 1), ("timeout_ms", -1, 1),
