@@ -257,15 +257,17 @@ def run_reference(args):
     w = workloads.WORKLOADS[args.workload]
     threads = oracle.host_threads()
     ops = oracle_operands(w)
-    # Each oracle call decodes B once (a fixed cost) and then computes its rows.
-    # Calibrate both: one call with a single row, one with 2 rows per thread.
+    # Each oracle call decodes B once (a fixed cost) and then computes its rows,
+    # one per thread at a time. Calibrate both: one call with a single row (the
+    # fixed cost and one row time), one with two rows per thread (one more row
+    # time), so a row costs (difference) / threads at full width.
     t0 = time.perf_counter()
     oracle_rows(oracle, w, ops, [0], threads)
     t_one = time.perf_counter() - t0
-    n_cal = 2 * threads
+    n_cal = min(2 * threads, w.M)
     t0 = time.perf_counter()
-    oracle_rows(oracle, w, ops, list(range(min(n_cal, w.M))), threads)
-    t_row = max((time.perf_counter() - t0 - t_one) / max(1, min(n_cal, w.M) - 1), 1e-6)
+    oracle_rows(oracle, w, ops, list(range(n_cal)), threads)
+    t_row = max((time.perf_counter() - t0 - t_one) / threads, 1e-6)
     # every timed step takes the same number of rows; the whole timed run is one
     # oracle call over all steps' rows (so B is decoded once), sized to ~60 s
     budget = 60.0
