@@ -19,7 +19,7 @@ from .binding import (GEMM_BF16, GEMM_E2M1, GEMM_E4M3, GEMM_E5M2, GEMM_F16, GEMM
                       GEMM_JOB_WRITER, GemmError, GemmJob, GemmOptions, GemmPlan, STATUS_NAMES)
 
 __all__ = ["gemm", "gemm_ex", "gemm_mx", "attention", "gemm_plan", "gemm_from_host", "gemm_from_host_async",
-           "gemm_release_workspace",
+           "gemm_release_workspace", "gemm_cache_stats", "gemm_cache_clear", "gemm_selftest_withheld_load",
            "gemm_last_device_status", "gemm_selftest_wait_timeout", "gemm_status_string",
            "gemm_launch_count", "gemm_schedule_jobs", "GemmError", "GemmOptions", "GemmPlan"]
 
@@ -47,7 +47,25 @@ def _options(options) -> GemmOptions | None:
     return o
 
 
-def _shapes(A: torch.Tensor, B: torch.Tensor, layout_b: str):
+def _check(status: int, what: str):
+    if status != GEMM_OK:
+        raise GemmError(status, what)
+
+
+def _prepare(A, B, C, layout_b, out_dtype, device_kind):
+    """Check A, B (and C, or allocate it) for a GEMM on `device_kind` tensors.
+    Returns M, N, K, C and the input type code. Type errors come first."""
+    din = _DT_IN.get(A.dtype)
+    if din is None or B.dtype not in _DT_IN:
+        name, t = ("A", A) if din is None else ("B", B)
+        raise TypeError(f"{name} must be float16, bfloat16, float8_e4m3fn or float8_e5m2, got {t.dtype}")
+    if A.dtype != B.dtype:
+        raise TypeError("A and B must have the same dtype")
+    want_cuda = device_kind == "cuda"
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous")
+    if A.is_cuda != want_cuda or B.is_cuda != want_cuda:
+        raise ValueError(f"A and B must be {device_kind} tensors")
     if A.dim() != 2 or B.dim() != 2:
         raise ValueError("A and B must be 2-D")
     M, K = A.shape
@@ -59,35 +77,31 @@ def _shapes(A: torch.Tensor, B: torch.Tensor, layout_b: str):
         raise ValueError("layout_b must be 'k' (B is N x K) or 'mn' (B is K x N)")
     if Kb != K:
         raise ValueError(f"K mismatch: A has {K}, B has {Kb}")
-    return int(M), int(N), int(K)
-
-
-def _check(status: int, what: str):
-    if status != GEMM_OK:
-        raise GemmError(status, what)
-
-
-def _prepare(A, B, C, layout_b, out_dtype, device_kind):
-    for name, t in (("A", A), ("B", B)):
-        if t.dtype not in _DT_IN:
-            raise TypeError(f"{name} must be float16, bfloat16, float8_e4m3fn or float8_e5m2, "
-                            f"got {t.dtype}")
-        if not t.is_contiguous():
-            raise ValueError(f"{name} must be contiguous")
-        if t.device.type != device_kind:
-            raise ValueError(f"{name} must be a {device_kind} tensor")
-    if A.dtype != B.dtype:
-        raise TypeError("A and B must have the same dtype")
-    M, N, K = _shapes(A, B, layout_b)
     if C is None:
         default_out = torch.bfloat16 if A.dtype in _FP8 else A.dtype
         C = torch.empty((M, N), dtype=out_dtype or default_out, device=A.device,
-                        pin_memory=(device_kind == "cpu" and torch.cuda.is_available()))
-    if C.dtype not in _DT_OUT or tuple(C.shape) != (M, N) or not C.is_contiguous():
+                        pin_memory=(not want_cuda and torch.cuda.is_available()))
+    elif (C.dtype not in _DT_OUT or C.dim() != 2 or C.shape[0] != M or C.shape[1] != N
+          or not C.is_contiguous()):
         raise ValueError("C must be a contiguous (M, N) float16/bfloat16/float32 tensor")
-    if C.device.type != device_kind:
+    if C.is_cuda != want_cuda:
         raise ValueError(f"C must be a {device_kind} tensor")
-    return M, N, K, C
+    return M, N, K, C, din
+
+
+def _on_device(dev: int, fn, *args):
+    """Call fn(*args) with CUDA device `dev` current (no device switch when it already is)."""
+    if dev == torch.cuda.current_device():
+        return fn(*args)
+    with torch.cuda.device(dev):
+        return fn(*args)
+
+
+def _gemm_call(a, b, c, M, N, K, din, dout, lb, opts, stream):
+    st = _stream_ptr(stream)
+    if opts is None:
+        return binding.lib.gemm(a, b, c, M, N, K, din, dout, GEMM_K_MAJOR, lb, st), "gemm"
+    return binding.lib.gemm_ex(a, b, c, M, N, K, din, dout, GEMM_K_MAJOR, lb, ctypes.byref(opts), st), "gemm_ex"
 
 
 def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *,
@@ -100,15 +114,11 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *,
     allocated when not given.
     ``options``: dict or GemmOptions of gemm_ex overrides.
     """
-    M, N, K, C = _prepare(A, B, C, layout_b, out_dtype, "cuda")
-    opts = _options(options)
-    args = (A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _DT_IN[A.dtype],
-            _DT_OUT[C.dtype], GEMM_K_MAJOR, _LAYOUT[layout_b])
-    with torch.cuda.device(A.device):
-        if opts is None:
-            _check(binding.lib.gemm(*args, _stream_ptr(stream)), "gemm")
-        else:
-            _check(binding.lib.gemm_ex(*args, ctypes.byref(opts), _stream_ptr(stream)), "gemm_ex")
+    M, N, K, C, din = _prepare(A, B, C, layout_b, out_dtype, "cuda")
+    status, what = _on_device(A.get_device(), _gemm_call, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                              din, _DT_OUT[C.dtype], _LAYOUT[layout_b], _options(options), stream)
+    if status != GEMM_OK:
+        raise GemmError(status, what)
     return C
 
 
@@ -221,10 +231,10 @@ def gemm_from_host(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = No
                    device=None) -> torch.Tensor:
     """C = A·B with host (CPU) tensors; copies in, computes and copies out on the current
     CUDA device, and returns when C is complete."""
-    M, N, K, C = _prepare(A, B, C, layout_b, out_dtype, "cpu")
+    M, N, K, C, din = _prepare(A, B, C, layout_b, out_dtype, "cpu")
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         _check(binding.lib.gemm_from_host(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
-                                          _DT_IN[A.dtype], _DT_OUT[C.dtype], GEMM_K_MAJOR,
+                                          din, _DT_OUT[C.dtype], GEMM_K_MAJOR,
                                           _LAYOUT[layout_b], _stream_ptr(stream)),
                "gemm_from_host")
     return C
@@ -237,10 +247,10 @@ def gemm_from_host_async(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | Non
     (default: the current stream) has passed the call; A and B must stay unchanged until
     then. Consecutive calls overlap one call's uploads with the previous call's product
     and read-back. Use pinned host tensors for the overlap."""
-    M, N, K, C = _prepare(A, B, C, layout_b, out_dtype, "cpu")
+    M, N, K, C, din = _prepare(A, B, C, layout_b, out_dtype, "cpu")
     with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
         _check(binding.lib.gemm_from_host_async(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
-                                          _DT_IN[A.dtype], _DT_OUT[C.dtype], GEMM_K_MAJOR,
+                                          din, _DT_OUT[C.dtype], GEMM_K_MAJOR,
                                           _LAYOUT[layout_b], _stream_ptr(stream)),
                "gemm_from_host_async")
     return C
@@ -261,6 +271,32 @@ def gemm_last_device_status(stream=None) -> tuple[int, int]:
 def gemm_selftest_wait_timeout(timeout_ms: int = 50, stream=None) -> None:
     _check(binding.lib.gemm_selftest_wait_timeout(int(timeout_ms), _stream_ptr(stream)),
            "gemm_selftest_wait_timeout")
+
+
+def gemm_selftest_withheld_load(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *, layout_b: str = "k",
+                                cta_group: int = 2, withhold_kb: int = 1, timeout_ms: int = 20,
+                                stream=None) -> None:
+    """Run the GEMM kernel with the first unit's producer withholding the loads of
+    k-block ``withhold_kb`` of its first tile, so that its waits run out after
+    ``timeout_ms``. Read the outcome with gemm_last_device_status."""
+    M, N, K, C, din = _prepare(A, B, C, layout_b, None, "cuda")
+    with torch.cuda.device(A.device):
+        _check(binding.lib.gemm_selftest_withheld_load(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, din,
+                                                       _DT_OUT[C.dtype], _LAYOUT[layout_b], int(cta_group),
+                                                       int(withhold_kb), int(timeout_ms), _stream_ptr(stream)),
+               "gemm_selftest_withheld_load")
+
+
+def gemm_cache_stats() -> dict:
+    """Launch-cache counters of this process: plan and tensor-map hits and misses."""
+    v = [ctypes.c_uint64(0) for _ in range(4)]
+    binding.lib.gemm_cache_stats(*(ctypes.byref(x) for x in v))
+    return dict(zip(("plan_hits", "plan_misses", "map_hits", "map_misses"), (int(x.value) for x in v)))
+
+
+def gemm_cache_clear() -> None:
+    """Empty the launch cache of the current device."""
+    _check(binding.lib.gemm_cache_clear(), "gemm_cache_clear")
 
 
 def gemm_status_string(status: int) -> str:
@@ -294,10 +330,10 @@ def gemm_no_alloc(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *, layout_b
     (GEMM_ERR_UNSUPPORTED). Calls that overlap on the GPU share the array and race."""
     if C is None:
         raise ValueError("gemm_no_alloc needs the caller's C")
-    M, N, K, C = _prepare(A, B, C, layout_b, None, "cuda")
+    M, N, K, C, din = _prepare(A, B, C, layout_b, None, "cuda")
     with torch.cuda.device(A.device):
         _check(binding.lib.gemm_no_alloc(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
-                                         _DT_IN[A.dtype], _DT_OUT[C.dtype], GEMM_K_MAJOR,
+                                         din, _DT_OUT[C.dtype], GEMM_K_MAJOR,
                                          _LAYOUT[layout_b], _stream_ptr(stream)),
                "gemm_no_alloc")
     return C

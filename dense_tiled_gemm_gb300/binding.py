@@ -30,7 +30,8 @@ class GemmOptions(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int32), ("block_n", ctypes.c_int32),
                 ("max_clusters", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("timeout_ms", ctypes.c_int32), ("k_stage", ctypes.c_int32),
-                ("stream_k", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("stream_k", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("clock_trace", ctypes.c_void_p)]
 
 
 class GemmPlan(ctypes.Structure):
@@ -98,6 +99,14 @@ def _declare(lib):
                                   ctypes.c_float, vp]
     lib.attention_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_int,
                                      ctypes.c_float, c_int, vp]
+    u64p = ctypes.POINTER(ctypes.c_uint64)
+    lib.gemm_cache_stats.restype = None
+    lib.gemm_cache_stats.argtypes = [u64p, u64p, u64p, u64p]
+    lib.gemm_cache_clear.restype = c_int
+    lib.gemm_cache_clear.argtypes = []
+    lib.gemm_selftest_withheld_load.restype = c_int
+    lib.gemm_selftest_withheld_load.argtypes = [vp, vp, vp, i64, i64, i64, c_int, c_int, c_int, i32, i32,
+                                                i32, vp]
     lib.gemm_schedule_jobs.restype = c_int
     lib.gemm_schedule_jobs.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(GemmJob), i32,
                                        ctypes.POINTER(i32)]

@@ -1,12 +1,15 @@
 // gemm.cu: host side of the C ABI declared in gemm.h.
 //
-// One call validates its arguments, picks a tile plan, builds three TMA
-// tensor maps (A, B, C), optionally re-pitches an operand that the TMA engine
-// cannot describe, and launches one persistent kernel on the caller's
-// stream. Nothing is allocated per call on the common path. The launcher of
-// "Porting High-Performance HIP Kernels to FlyDSL" (section "Structure of a
-// FlyDSL Kernel") is the model for the interface: prebuilt code, caller's
-// stream, no stream created per call.
+// One call validates its arguments, picks a tile plan, builds the TMA tensor
+// maps (A, B, C), optionally re-pitches an operand that the TMA engine cannot
+// describe, and launches one persistent kernel on the caller's stream. Plans
+// and tensor maps are cached per device, so a repeated call does neither the
+// plan search nor the encoding. Stream-ordered scratch is taken only for a
+// re-pitched operand, the stream-K partial sums and the MX scale repack. The
+// launcher of "Porting High-Performance HIP Kernels to FlyDSL" (section
+// "Structure of a FlyDSL Kernel") is the model for the interface: prebuilt
+// code, caller's stream, no stream created per call, no per-call setup
+// beyond the launch.
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -105,6 +108,7 @@ Layout layout_for(const Variant &v, int dtype_out)
 
 struct DeviceState {
     bool ready = false;
+    int dev = 0;
     int sms = 0;
     unsigned long long *status = nullptr;
     int max_units[NUM_VARIANTS] = {};   // co-resident CTAs (cg 1) or CTA pairs (cg 2)
@@ -194,6 +198,7 @@ gemm_status_t device_state(DeviceState **out)
         }
         if (major != 10 || minor != 3)   // the library holds sm_103a code only
             return GEMM_ERR_NO_DEVICE;
+        d.dev = dev;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return GEMM_ERR_CUDA;
         void *status = nullptr;
@@ -293,6 +298,74 @@ struct Plan {
     size_t ws_bytes;       // stream-K workspace: flags, then partial sums
     bool realign_a, realign_b, direct_store;
 };
+
+// ------------------------------------------------------------------ launch cache
+// Per device, the plans and TMA tensor maps of the most recent launches, so
+// that a repeated call skips the planner's variant search and the
+// cuTensorMapEncodeTiled calls. Keys are compared bytewise (every key is
+// zeroed before it is filled, padding included). Entries are replaced least
+// recently used first. A tensor map holds only the numbers it was encoded
+// from, so a cached one equals a fresh encoding of the same key.
+struct PlanKey {
+    int64_t M, N, K;
+    int32_t dtype_in, dtype_out, layoutB, scaled;
+    int32_t misalign;   // bit 0: A, bit 1: B, bit 2: C not describable to the TMA engine
+    int32_t cta_group, block_n, max_clusters, group_m, k_stage, stream_k;
+    int32_t pad;
+};
+
+struct MapKey {
+    PlanKey plan;
+    int32_t variant, pad;
+    const void *a, *b, *c, *sfa, *sfb;   // the addresses the maps describe
+    int64_t lda, ldb;                    // their row pitches, in TMA elements
+};
+
+constexpr int CACHE_ENTRIES = GEMM_LAUNCH_CACHE_ENTRIES;
+
+struct LaunchCache {
+    std::mutex mu;
+    uint64_t clock = 0;
+    struct PlanEntry {
+        PlanKey key;
+        Plan plan;
+        uint64_t used = 0;   // 0: empty
+    } plans[CACHE_ENTRIES];
+    struct MapEntry {
+        MapKey key;
+        CUtensorMap maps[5];
+        uint64_t used = 0;
+    } maps[CACHE_ENTRIES];
+
+    template <typename E, typename Key>
+    static E *find(E (&tab)[CACHE_ENTRIES], const Key &k)
+    {
+        for (E &e : tab)
+            if (e.used && std::memcmp(&e.key, &k, sizeof(Key)) == 0)
+                return &e;
+        return nullptr;
+    }
+    template <typename E>
+    static E *victim(E (&tab)[CACHE_ENTRIES])
+    {
+        E *v = &tab[0];
+        for (E &e : tab)
+            if (e.used < v->used)
+                v = &e;
+        return v;
+    }
+    void clear()
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (PlanEntry &e : plans)
+            e.used = 0;
+        for (MapEntry &e : maps)
+            e.used = 0;
+    }
+};
+
+LaunchCache g_cache[MAX_DEVICES];
+std::atomic<uint64_t> g_plan_hits{0}, g_plan_misses{0}, g_map_hits{0}, g_map_misses{0};
 
 // Stream-K workspace of a launch: one flag per (CTA, epilogue warp), then one
 // partial-sum slot per CTA (128 rows x block_n FP32).
@@ -404,6 +477,62 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
     return GEMM_OK;
 }
 
+PlanKey plan_key(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutB, bool scaled,
+                 const void *A, const void *B, const void *C, const gemm_options_t *o)
+{
+    PlanKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.M = M;
+    k.N = N;
+    k.K = K;
+    k.dtype_in = dtype_in;
+    k.dtype_out = dtype_out;
+    k.layoutB = layoutB;
+    k.scaled = scaled ? 1 : 0;
+    const int kind = kind_for(dtype_in, scaled);
+    const bool b_mn = layoutB == GEMM_MN_MAJOR;
+    k.misalign = (misaligned(A, row_bytes(kind, K), 1) ? 1 : 0) |
+                 (misaligned(B, b_mn ? row_bytes(kind, N) : row_bytes(kind, K), 1) ? 2 : 0) |
+                 (misaligned(C, N, out_bytes(dtype_out)) ? 4 : 0);
+    if (o) {   // the fields that steer the planner (not timeout_ms or clock_trace)
+        k.cta_group = o->cta_group;
+        k.block_n = o->block_n;
+        k.max_clusters = o->max_clusters;
+        k.group_m = o->group_m;
+        k.k_stage = o->k_stage;
+        k.stream_k = o->stream_k;
+    }
+    return k;
+}
+
+// make_plan through the device's launch cache. The plan depends only on the
+// key: make_plan reads the operand pointers for their alignment alone.
+gemm_status_t cached_plan(const DeviceState &d, const PlanKey &k, const void *A, const void *B, const void *C,
+                          const gemm_options_t *o, Plan *pl)
+{
+    LaunchCache &c = g_cache[d.dev];
+    {
+        std::lock_guard<std::mutex> lock(c.mu);
+        if (LaunchCache::PlanEntry *e = LaunchCache::find(c.plans, k)) {
+            e->used = ++c.clock;
+            *pl = e->plan;
+            g_plan_hits.fetch_add(1, std::memory_order_relaxed);
+            return GEMM_OK;
+        }
+    }
+    g_plan_misses.fetch_add(1, std::memory_order_relaxed);
+    const gemm_status_t rc =
+        make_plan(d, k.M, k.N, k.K, k.dtype_in, k.dtype_out, k.layoutB, A, B, C, o, pl, k.scaled != 0);
+    if (rc != GEMM_OK)
+        return rc;
+    std::lock_guard<std::mutex> lock(c.mu);
+    LaunchCache::PlanEntry *e = LaunchCache::victim(c.plans);
+    e->key = k;
+    e->plan = *pl;
+    e->used = ++c.clock;
+    return GEMM_OK;
+}
+
 bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
                uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapSwizzle swizzle)
@@ -436,15 +565,22 @@ CUtensorMapDataType tma_dtype(int dtype)
 gemm_status_t realign_into(const void *src, int64_t rows, int64_t cols, int64_t ld, int eb, int sms,
                            cudaStream_t st, void *dst)
 {
-    const int64_t total = rows * cols;
-    const unsigned blocks = static_cast<unsigned>(
-        std::max<int64_t>(std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(sms) * 8), 1));
-    if (eb == 1)
-        realign_rows_kernel<uint8_t><<<blocks, 256, 0, st>>>(static_cast<const uint8_t *>(src),
-                                                             static_cast<uint8_t *>(dst), rows, cols, ld);
-    else
-        realign_rows_kernel<uint16_t><<<blocks, 256, 0, st>>>(static_cast<const uint16_t *>(src),
-                                                              static_cast<uint16_t *>(dst), rows, cols, ld);
+    const int64_t row_bytes = cols * eb, pitch = ld * eb;
+    // widest word (<= 16 bytes) dividing the source base and the row length, so
+    // that every source row starts on a word boundary
+    const uint64_t align = static_cast<uint64_t>(reinterpret_cast<uintptr_t>(src)) | static_cast<uint64_t>(row_bytes);
+    const int v = (align % 16 == 0) ? 16 : (align % 8 == 0) ? 8 : (align % 4 == 0) ? 4 : (align % 2 == 0) ? 2 : 1;
+    // one block per row at a time, up to 8 resident blocks per SM
+    const unsigned blocks = static_cast<unsigned>(std::max<int64_t>(std::min<int64_t>(rows, static_cast<int64_t>(sms) * 8), 1));
+    const uint8_t *s = static_cast<const uint8_t *>(src);
+    uint8_t *d = static_cast<uint8_t *>(dst);
+    switch (v) {
+    case 16: realign_rows_kernel<16><<<blocks, 256, 0, st>>>(s, d, rows, row_bytes, pitch); break;
+    case 8: realign_rows_kernel<8><<<blocks, 256, 0, st>>>(s, d, rows, row_bytes, pitch); break;
+    case 4: realign_rows_kernel<4><<<blocks, 256, 0, st>>>(s, d, rows, row_bytes, pitch); break;
+    case 2: realign_rows_kernel<2><<<blocks, 256, 0, st>>>(s, d, rows, row_bytes, pitch); break;
+    default: realign_rows_kernel<1><<<blocks, 256, 0, st>>>(s, d, rows, row_bytes, pitch); break;
+    }
     if (cudaGetLastError() != cudaSuccess)
         return GEMM_ERR_CUDA;
     g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -551,19 +687,16 @@ struct Operand {
     int64_t ld;
 };
 
-// Build the tensor maps and the kernel parameters for operands already at
-// TMA-describable addresses, and launch the plan's kernel on `st`. For the
-// block-scaled kinds sfa/sfb are the packed scales (rows x num_kb x 16 bytes).
-gemm_status_t encode_and_launch(const DeviceState &d, const Plan &pl, Operand a, Operand b, const void *sfa,
-                                const void *sfb, void *C, int64_t M, int64_t N, int64_t K, int dtype_in,
-                                int dtype_out, bool b_mn, uint64_t timeout_ms, void *workspace, cudaStream_t st)
+// Encode the plan's tensor maps (A, B, C and, block-scaled, the packed
+// scales sfa/sfb) for operands already at TMA-describable addresses.
+bool encode_maps(const Plan &pl, Operand a, Operand b, const void *sfa, const void *sfb, void *C, int64_t M,
+                 int64_t N, int64_t K, int dtype_in, int dtype_out, bool b_mn, CUtensorMap *maps)
 {
     const Variant &var = kVariants[pl.variant];
     const int eb = tma_elem_bytes(var.kind);
     const int64_t width = row_bytes(var.kind, K) / eb;   // K in TMA elements
     const uint32_t box_k = var.kind == KIND_F16 ? 64 : 128;
-    alignas(64) CUtensorMap maps[5];
-    std::memset(maps, 0, sizeof(maps));
+    std::memset(maps, 0, 5 * sizeof(CUtensorMap));
     const CUtensorMapDataType in_dt = tma_dtype(dtype_in);
     bool ok = encode_2d(&maps[0], in_dt, a.ptr, width, M, a.ld * eb, box_k, BLOCK_M_CTA, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!b_mn)
@@ -582,8 +715,59 @@ gemm_status_t encode_and_launch(const DeviceState &d, const Plan &pl, Operand a,
         ok = ok && encode_2d(&maps[4], CU_TENSOR_MAP_DATA_TYPE_UINT8, sfb, SF_ROW_BYTES, gb.atom_rows, SF_ROW_BYTES,
                              SF_ROW_BYTES, gb.box_rows(), CU_TENSOR_MAP_SWIZZLE_NONE);
     }
-    if (!ok)
-        return GEMM_ERR_CUDA;
+    return ok;
+}
+
+// Per-launch extras: the clock trace words (gemm_options_t.clock_trace) and
+// the self-test's withheld k-block (-1: none).
+struct Extras {
+    unsigned long long *trace = nullptr;
+    int32_t withhold_kb = -1;
+};
+
+// Fetch the tensor maps from the launch cache (or encode and insert them),
+// fill the kernel parameters and launch the plan's kernel on `st`. For the
+// block-scaled kinds sfa/sfb are the packed scales (rows x num_kb x 16 bytes).
+gemm_status_t encode_and_launch(const DeviceState &d, const PlanKey &pk, const Plan &pl, Operand a, Operand b,
+                                const void *sfa, const void *sfb, void *C, int64_t M, int64_t N, int64_t K,
+                                int dtype_in, int dtype_out, bool b_mn, uint64_t timeout_ms, void *workspace,
+                                const Extras &x, cudaStream_t st)
+{
+    const Variant &var = kVariants[pl.variant];
+    CUtensorMap maps[5];
+    MapKey mk;
+    std::memset(&mk, 0, sizeof(mk));
+    mk.plan = pk;
+    mk.variant = pl.variant;
+    mk.a = a.ptr;
+    mk.b = b.ptr;
+    mk.c = C;
+    mk.sfa = sfa;
+    mk.sfb = sfb;
+    mk.lda = a.ld;
+    mk.ldb = b.ld;
+    LaunchCache &cache = g_cache[d.dev];
+    bool hit = false;
+    {
+        std::lock_guard<std::mutex> lock(cache.mu);
+        if (LaunchCache::MapEntry *e = LaunchCache::find(cache.maps, mk)) {
+            e->used = ++cache.clock;
+            std::memcpy(maps, e->maps, sizeof(maps));
+            hit = true;
+        }
+    }
+    if (hit) {
+        g_map_hits.fetch_add(1, std::memory_order_relaxed);
+    } else {
+        g_map_misses.fetch_add(1, std::memory_order_relaxed);
+        if (!encode_maps(pl, a, b, sfa, sfb, C, M, N, K, dtype_in, dtype_out, b_mn, maps))
+            return GEMM_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(cache.mu);
+        LaunchCache::MapEntry *e = LaunchCache::victim(cache.maps);
+        e->key = mk;
+        std::memcpy(e->maps, maps, sizeof(maps));
+        e->used = ++cache.clock;
+    }
 
     KernelParams kp = {};
     kp.M = static_cast<int32_t>(M);
@@ -618,6 +802,8 @@ gemm_status_t encode_and_launch(const DeviceState &d, const Plan &pl, Operand a,
     kp.timeout_ns = timeout_ms * 1000000ull;
     kp.launch_id = next_launch_id();
     kp.status = d.status;
+    kp.trace = x.trace;
+    kp.withhold_kb = x.withhold_kb;
 
     if (launch_any(var, pl.grid_ctas, lay.smem, maps, kp, st) != cudaSuccess) {
         cudaGetLastError();
@@ -647,7 +833,7 @@ gemm_status_t pack_scales(const uint8_t *sf, int64_t rows, int64_t K, const SfGe
 
 gemm_status_t run(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C, int64_t M,
                   int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB,
-                  const gemm_options_t *opts, cudaStream_t st)
+                  const gemm_options_t *opts, cudaStream_t st, int32_t withhold_kb = -1)
 {
     const bool scaled = SFA != nullptr;
     gemm_status_t rc = validate(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, opts, scaled);
@@ -656,9 +842,15 @@ gemm_status_t run(const void *A, const void *B, const uint8_t *SFA, const uint8_
     DeviceState *d = nullptr;
     if ((rc = device_state(&d)) != GEMM_OK)
         return rc;
+    const PlanKey pk = plan_key(M, N, K, dtype_in, dtype_out, layoutB, scaled, A, B, C, opts);
     Plan pl;
-    if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, opts, &pl, scaled)) != GEMM_OK)
+    if ((rc = cached_plan(*d, pk, A, B, C, opts, &pl)) != GEMM_OK)
         return rc;
+    if (withhold_kb >= pl.num_kb)
+        return GEMM_ERR_INVALID_ARG;
+    Extras x;
+    x.trace = opts ? reinterpret_cast<unsigned long long *>(opts->clock_trace) : nullptr;
+    x.withhold_kb = withhold_kb;
     const Variant &var = kVariants[pl.variant];
     const bool b_mn = layoutB == GEMM_MN_MAJOR;
     const int eb = tma_elem_bytes(var.kind);
@@ -710,7 +902,8 @@ gemm_status_t run(const void *A, const void *B, const uint8_t *SFA, const uint8_
 
     const uint64_t timeout_ms = opts && opts->timeout_ms ? static_cast<uint64_t>(opts->timeout_ms)
                                                          : DEFAULT_TIMEOUT_MS;
-    rc = encode_and_launch(*d, pl, a, b, sfa, sfb, C, M, N, K, dtype_in, dtype_out, b_mn, timeout_ms, ws, st);
+    rc = encode_and_launch(*d, pk, pl, a, b, sfa, sfb, C, M, N, K, dtype_in, dtype_out, b_mn, timeout_ms, ws, x,
+                           st);
     release();
     return rc;
 }
@@ -719,23 +912,24 @@ gemm_status_t run(const void *A, const void *B, const uint8_t *SFA, const uint8_
 
 extern "C" {
 
-gemm_status_t gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, int dtype_in,
-                   int dtype_out, int layoutA, int layoutB, void *stream)
+gemm_status_t gemm(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in,
+                   gemm_dtype_t dtype_out, gemm_layout_t layoutA, gemm_layout_t layoutB, void *stream)
 {
     return run(A, B, nullptr, nullptr, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, nullptr,
                static_cast<cudaStream_t>(stream));
 }
 
 gemm_status_t gemm_ex(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
-                      int dtype_in, int dtype_out, int layoutA, int layoutB, const gemm_options_t *opts,
-                      void *stream)
+                      gemm_dtype_t dtype_in, gemm_dtype_t dtype_out, gemm_layout_t layoutA, gemm_layout_t layoutB,
+                      const gemm_options_t *opts, void *stream)
 {
     return run(A, B, nullptr, nullptr, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB, opts,
                static_cast<cudaStream_t>(stream));
 }
 
 gemm_status_t gemm_mx(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C, int64_t M,
-                      int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB, void *stream)
+                      int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out, gemm_layout_t layoutA,
+                      gemm_layout_t layoutB, void *stream)
 {
     if (!SFA || !SFB)
         return GEMM_ERR_INVALID_ARG;
@@ -744,8 +938,8 @@ gemm_status_t gemm_mx(const void *A, const void *B, const uint8_t *SFA, const ui
 }
 
 gemm_status_t gemm_mx_ex(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C,
-                         int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB,
-                         const gemm_options_t *opts, void *stream)
+                         int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                         gemm_layout_t layoutA, gemm_layout_t layoutB, const gemm_options_t *opts, void *stream)
 {
     if (!SFA || !SFB)
         return GEMM_ERR_INVALID_ARG;
@@ -770,7 +964,8 @@ gemm_status_t plan_query(int64_t M, int64_t N, int64_t K, int dtype_in, int dtyp
     if ((rc = device_state(&d)) != GEMM_OK)
         return rc;
     Plan pl;
-    if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, opts, &pl, scaled)) != GEMM_OK)
+    const PlanKey pk = plan_key(M, N, K, dtype_in, dtype_out, layoutB, scaled, A, B, C, opts);
+    if ((rc = cached_plan(*d, pk, A, B, C, opts, &pl)) != GEMM_OK)
         return rc;
     const Variant &var = kVariants[pl.variant];
     std::memset(plan, 0, sizeof(*plan));
@@ -797,22 +992,23 @@ gemm_status_t plan_query(int64_t M, int64_t N, int64_t K, int dtype_in, int dtyp
 
 extern "C" {
 
-gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA,
-                        int layoutB, const void *A, const void *B, const void *C,
+gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                        gemm_layout_t layoutA, gemm_layout_t layoutB, const void *A, const void *B, const void *C,
                         const gemm_options_t *opts, gemm_plan_t *plan)
 {
     return plan_query(M, N, K, dtype_in, dtype_out, layoutA, layoutB, A, B, C, opts, plan, false);
 }
 
-gemm_status_t gemm_mx_plan(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA,
-                           int layoutB, const void *A, const void *B, const void *C,
+gemm_status_t gemm_mx_plan(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                           gemm_layout_t layoutA, gemm_layout_t layoutB, const void *A, const void *B, const void *C,
                            const gemm_options_t *opts, gemm_plan_t *plan)
 {
     return plan_query(M, N, K, dtype_in, dtype_out, layoutA, layoutB, A, B, C, opts, plan, true);
 }
 
 gemm_status_t gemm_from_host_async(const void *A_host, const void *B_host, void *C_host, int64_t M, int64_t N,
-                                   int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB, void *stream)
+                                   int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out, gemm_layout_t layoutA,
+                                   gemm_layout_t layoutB, void *stream)
 {
     gemm_status_t rc = validate(A_host, B_host, C_host, M, N, K, dtype_in, dtype_out, layoutA, layoutB,
                                 nullptr);
@@ -880,7 +1076,8 @@ gemm_status_t gemm_from_host_async(const void *A_host, const void *B_host, void 
 }
 
 gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_host, int64_t M, int64_t N,
-                             int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB, void *stream)
+                             int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out, gemm_layout_t layoutA,
+                             gemm_layout_t layoutB, void *stream)
 {
     gemm_status_t rc = gemm_from_host_async(A_host, B_host, C_host, M, N, K, dtype_in, dtype_out, layoutA,
                                             layoutB, stream);
@@ -913,6 +1110,29 @@ gemm_status_t gemm_release_workspace(void)
         slot.bytes = 0;
         slot.used = false;
     }
+    g_cache[d->dev].clear();
+    return GEMM_OK;
+}
+
+void gemm_cache_stats(uint64_t *plan_hits, uint64_t *plan_misses, uint64_t *map_hits, uint64_t *map_misses)
+{
+    if (plan_hits)
+        *plan_hits = g_plan_hits.load(std::memory_order_relaxed);
+    if (plan_misses)
+        *plan_misses = g_plan_misses.load(std::memory_order_relaxed);
+    if (map_hits)
+        *map_hits = g_map_hits.load(std::memory_order_relaxed);
+    if (map_misses)
+        *map_misses = g_map_misses.load(std::memory_order_relaxed);
+}
+
+gemm_status_t gemm_cache_clear(void)
+{
+    DeviceState *d = nullptr;
+    const gemm_status_t rc = device_state(&d);
+    if (rc != GEMM_OK)
+        return rc;
+    g_cache[d->dev].clear();
     return GEMM_OK;
 }
 
@@ -960,7 +1180,21 @@ gemm_status_t gemm_selftest_wait_timeout(int32_t timeout_ms, void *stream)
     return GEMM_OK;
 }
 
-const char *gemm_status_string(int status)
+gemm_status_t gemm_selftest_withheld_load(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                                          gemm_dtype_t dtype_in, gemm_dtype_t dtype_out, gemm_layout_t layoutB,
+                                          int32_t cta_group, int32_t withhold_kb, int32_t timeout_ms, void *stream)
+{
+    if (timeout_ms < 1 || timeout_ms > 10000 || withhold_kb < 0 || (cta_group != 1 && cta_group != 2))
+        return GEMM_ERR_INVALID_ARG;
+    gemm_options_t o = {};
+    o.cta_group = cta_group;
+    o.timeout_ms = timeout_ms;
+    o.stream_k = 1;   // whole tiles: unit 0's first job is a full tile
+    return run(A, B, nullptr, nullptr, C, M, N, K, dtype_in, dtype_out, GEMM_K_MAJOR, layoutB, &o,
+               static_cast<cudaStream_t>(stream), withhold_kb);
+}
+
+const char *gemm_status_string(gemm_status_t status)
 {
     switch (status) {
     case GEMM_OK: return "GEMM_OK";
@@ -1000,9 +1234,11 @@ gemm_status_t gemm_schedule_jobs(int32_t num_tiles, int32_t units, int32_t k_blo
 // For callers that cannot allocate device memory, for example a serving
 // runtime that has given all of the GPU's memory to its own pool, or a
 // latency-critical loop where cudaMalloc/cudaFree could synchronise the device
-// or fail. The only allocation gemm makes is the re-pitch scratch of a
-// misaligned A or B. Here that scratch is this fixed array, held on every GPU
-// that loads the library until the process exits. Host code must not use
+// or fail. gemm allocates stream-ordered scratch for the re-pitched copy of a
+// misaligned A or B and for the stream-K partial sums and flags. Here both go
+// into this fixed array, held on every GPU that loads the library until the
+// process exits (or, when the partial sums do not fit, the plan keeps every
+// tile whole). Host code must not use
 // the name g_no_alloc_scratch as a device address: it stands for a host-side
 // shadow. The device address comes from cudaGetSymbolAddress, looked up once
 // per device with that device current.
@@ -1044,8 +1280,14 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
     DeviceState *d = nullptr;
     if ((rc = device_state(&d)) != GEMM_OK)
         return rc;
+    // the array's address is looked up on every device's first call, whether or
+    // not that call needs it, so that a later call inside a stream capture never does
+    void *scratch = nullptr;
+    if ((rc = no_alloc_scratch(&scratch)) != GEMM_OK)
+        return rc;
+    PlanKey pk = plan_key(M, N, K, dtype_in, dtype_out, layoutB, false, A, B, C, nullptr);
     Plan pl;
-    if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, nullptr, &pl)) != GEMM_OK)
+    if ((rc = cached_plan(*d, pk, A, B, C, nullptr, &pl)) != GEMM_OK)
         return rc;
     const bool b_mn = layoutB == GEMM_MN_MAJOR;
     const int kind = kind_for(dtype_in, false);
@@ -1066,16 +1308,14 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
         // no room for the partial sums: keep every tile whole
         gemm_options_t dp = {};
         dp.stream_k = 1;
-        if ((rc = make_plan(*d, M, N, K, dtype_in, dtype_out, layoutB, A, B, C, &dp, &pl)) != GEMM_OK)
+        pk = plan_key(M, N, K, dtype_in, dtype_out, layoutB, false, A, B, C, &dp);
+        if ((rc = cached_plan(*d, pk, A, B, C, &dp, &pl)) != GEMM_OK)
             return rc;
     }
 
     Operand a{A, a_cols}, b{B, b_cols};
     void *ws = nullptr;
     if (pl.realign_a || pl.realign_b || pl.sk_tiles) {
-        void *scratch = nullptr;
-        if ((rc = no_alloc_scratch(&scratch)) != GEMM_OK)
-            return rc;
         char *base = static_cast<char *>(scratch);
         if (pl.sk_tiles)
             ws = base + ws_off;
@@ -1090,8 +1330,8 @@ gemm_status_t run_no_alloc(const void *A, const void *B, void *C, int64_t M, int
             b = {base + b_off, ldb_pad};
         }
     }
-    return encode_and_launch(*d, pl, a, b, nullptr, nullptr, C, M, N, K, dtype_in, dtype_out, b_mn,
-                             DEFAULT_TIMEOUT_MS, ws, st);
+    return encode_and_launch(*d, pk, pl, a, b, nullptr, nullptr, C, M, N, K, dtype_in, dtype_out, b_mn,
+                             DEFAULT_TIMEOUT_MS, ws, Extras{}, st);
 }
 
 } // namespace
@@ -1137,8 +1377,8 @@ bool runtime_encode(CUtensorMap *map, CUtensorMapDataType dt, uint32_t rank, con
 } // namespace dtg
 
 extern "C" gemm_status_t gemm_no_alloc(const void *A, const void *B, void *C, int64_t M, int64_t N,
-                                       int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB,
-                                       void *stream)
+                                       int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                                       gemm_layout_t layoutA, gemm_layout_t layoutB, void *stream)
 {
     return run_no_alloc(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB,
                         static_cast<cudaStream_t>(stream));

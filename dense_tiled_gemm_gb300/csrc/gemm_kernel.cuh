@@ -47,6 +47,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "ptx.cuh"
 #include "schedule.cuh"
 
@@ -121,6 +123,15 @@ struct KernelParams {
     uint64_t timeout_ns;       // per-wait limit
     unsigned long long launch_id;
     unsigned long long *status;  // [0] first timed-out launch, [1] site, [2] last timed-out launch
+    // Optional clock trace (null: off): CTA 0 writes %globaltimer (ns) and
+    // clock64 (SM cycles) once global memory may be touched, [0] and [1], and
+    // again after its teardown barrier, [2] and [3]. Their ratio is the SM
+    // clock over the launch.
+    unsigned long long *trace;
+    // Self-test only (-1: off): unit 0's producer issues neither the
+    // expect-tx arrive nor the loads of k-block `withhold_kb` of its first
+    // job, so that stage never fills and the waits behind it run out.
+    int32_t withhold_kb;
 };
 
 // KS = K slabs per ring stage, KIND = operand kind (KIND_F16, KIND_F8,
@@ -448,6 +459,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // read or written before that grid has completed.
     grid_dependency_wait();
     grid_launch_dependents();
+    if (p.trace != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+        p.trace[0] = global_timer_ns();
+        p.trace[1] = static_cast<unsigned long long>(clock64());
+    }
 
     WaitCtx w{p.timeout_ns, p.launch_id, p.status, false};
     // This unit's jobs: whole tiles and, with stream-K, at most one writer and
@@ -465,6 +480,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 prefetch_tensor_map(&tmap_sfb);
             }
             uint32_t s = 0, ph = 0, pend_mask = 0, pend_par = 0;
+            // self-test: the k-block of the first job whose stage is never filled (-1: none)
+            const int withhold = cluster_id == 0 ? p.withhold_kb : -1;
             for (int i = 0; i < num_jobs; ++i) {
                 const Job jb = sch.job(i);
                 int m_blk, n_blk;
@@ -473,7 +490,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const int b_off = n_blk * BN + static_cast<int>(rank) * Cfg::BN_CTA;
                 for (int kb = jb.kb0; kb < jb.kb1; ++kb) {
                     wait_bounded<CG == 2>(w, empty_bar(s), ph ^ 1u, SITE_PRODUCER_EMPTY);
-                    if (!w.aborted) {
+                    if (!w.aborted && !(i == 0 && kb == withhold)) {
                         const uint32_t a_dst = base + s * Cfg::STAGE_BYTES;
                         const uint32_t b_dst = a_dst + Cfg::A_BYTES;
                         const int x0 = kb * KS * Cfg::SLAB_X;
@@ -783,6 +800,10 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
         cluster_sync();   // the peer no longer touches this CTA's barriers or TMEM
     else
         __syncthreads();
+    if (p.trace != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+        p.trace[2] = global_timer_ns();
+        p.trace[3] = static_cast<unsigned long long>(clock64());
+    }
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<CG>(tmem_base, TMEM_COLS);
@@ -850,19 +871,45 @@ static __global__ void pack_scales_kernel(const uint8_t *__restrict__ sf, uint8_
     }
 }
 
-// Copy a rows x cols matrix of T (row pitch `cols`, any alignment of T) to a
-// buffer whose row pitch `ld_dst` is a multiple of 16 bytes and whose base is
-// 256-byte aligned, so the TMA engine can describe it.
-template <typename T>
-__global__ void realign_rows_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t rows,
-                                    int64_t cols, int64_t ld_dst)
+// Copy `rows` rows of `row_bytes` bytes each (source pitch row_bytes, densely
+// packed) into a buffer whose row pitch `dst_pitch` is a multiple of 16 bytes
+// and whose base is 256-byte aligned, so the TMA engine can describe it. The
+// bytes past row_bytes in each destination row are not written: the tensor
+// map keeps the logical width, and TMA zero-fills past it.
+//
+// V is the widest word that divides the source base, row_bytes and hence
+// every source row start (4 for a 4100-byte BF16 row), so every access is an
+// aligned V-byte word inside the source or destination row. Each block walks
+// whole rows (grid-stride); consecutive threads take consecutive words, so
+// both the loads and the stores of a warp are contiguous.
+template <int V>
+__global__ void __launch_bounds__(256) realign_rows_kernel(const uint8_t *__restrict__ src,
+                                                           uint8_t *__restrict__ dst, int64_t rows,
+                                                           int64_t row_bytes, int64_t dst_pitch)
 {
-    const int64_t total = rows * cols;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / cols;
-        const int64_t c = i - r * cols;
-        dst[r * ld_dst + c] = src[i];
+    using W = typename std::conditional<
+        V == 16, uint4,
+        typename std::conditional<V == 8, uint2,
+                                  typename std::conditional<V == 4, uint32_t,
+                                                            typename std::conditional<V == 2, uint16_t,
+                                                                                      uint8_t>::type>::type>::type>::type;
+    const int64_t words = row_bytes / V;
+    // independent loads in flight per thread before their stores (~64 KB per SM at 8 blocks)
+    constexpr int UNROLL = V >= 16 ? 2 : V == 8 ? 4 : 8;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const W *s = reinterpret_cast<const W *>(src + r * row_bytes);
+        W *d = reinterpret_cast<W *>(dst + r * dst_pitch);
+        for (int64_t i0 = threadIdx.x; i0 < words; i0 += UNROLL * 256) {
+            W v[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u)
+                if (i0 + u * 256 < words)
+                    v[u] = __ldg(s + i0 + u * 256);
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u)
+                if (i0 + u * 256 < words)
+                    d[i0 + u * 256] = v[u];
+        }
     }
 }
 

@@ -107,14 +107,26 @@ typedef enum {
  * with ordinary stores instead of bulk tensor stores. Results do not depend
  * on either path.
  *
+ * Per-call host work: the library keeps, per device, the plans and the TMA
+ * tensor maps of its most recent launches (GEMM_LAUNCH_CACHE_ENTRIES of
+ * each). A call whose sizes, types, layouts, options and pointer alignment
+ * match a cached plan skips the planner; one whose operand, scratch and C
+ * addresses also match skips the tensor-map encoding. A tensor map holds only
+ * the numbers it was encoded from (addresses, sizes, pitches, tile shape), so
+ * a cached one is the same bytes as a fresh encoding of the same call.
+ * gemm_cache_stats counts hits and misses; gemm_cache_clear empties the
+ * cache.
+ *
  * Errors: returns GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED,
  * GEMM_ERR_NO_DEVICE, GEMM_ERR_OUT_OF_MEMORY or GEMM_ERR_CUDA before or at
  * launch. A kernel that stalls past the wait limit (2 s per wait) sets the
  * library's device status word and exits; gemm_last_device_status reports it.
  */
+#define GEMM_LAUNCH_CACHE_ENTRIES 32
 gemm_status_t gemm(const void *A, const void *B, void *C,
                    int64_t M, int64_t N, int64_t K,
-                   int dtype_in, int dtype_out, int layoutA, int layoutB,
+                   gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                   gemm_layout_t layoutA, gemm_layout_t layoutB,
                    void *stream);
 
 /*
@@ -143,8 +155,8 @@ gemm_status_t gemm(const void *A, const void *B, void *C,
  * computed by CTA pairs. Errors as for gemm.
  */
 gemm_status_t gemm_mx(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C,
-                      int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA,
-                      int layoutB, void *stream);
+                      int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                      gemm_layout_t layoutA, gemm_layout_t layoutB, void *stream);
 
 /*
  * gemm_options_t: overrides for gemm_ex and gemm_mx_ex. A zero field means the library
@@ -170,6 +182,14 @@ gemm_status_t gemm_mx(const void *A, const void *B, const uint8_t *SFA, const ui
  *                 tiles (see gemm_schedule_jobs). Other values give
  *                 GEMM_ERR_INVALID_ARG (negative) or GEMM_ERR_UNSUPPORTED.
  *   reserved      must be 0.
+ *   clock_trace   NULL, or a device pointer to 4 writable, 8-byte aligned
+ *                 uint64 words. The launch's first CTA then writes the
+ *                 global timer (ns) and its SM cycle counter as it starts
+ *                 work ([0], [1]) and again as it finishes ([2], [3]), so
+ *                 that ([3]-[1]) / ([2]-[0]) is the SM clock, in GHz, that
+ *                 the launch ran at. The words are written by the kernel,
+ *                 asynchronously on the call's stream; the caller owns them.
+ *                 It does not change the plan or the result.
  */
 typedef struct {
     int32_t cta_group;
@@ -180,21 +200,24 @@ typedef struct {
     int32_t k_stage;
     int32_t stream_k;
     int32_t reserved;
+    uint64_t *clock_trace;
 } gemm_options_t;
 
 /* gemm with overrides. opts may be NULL. An unsupported override combination
  * gives GEMM_ERR_UNSUPPORTED. */
 gemm_status_t gemm_ex(const void *A, const void *B, void *C,
                       int64_t M, int64_t N, int64_t K,
-                      int dtype_in, int dtype_out, int layoutA, int layoutB,
+                      gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                      gemm_layout_t layoutA, gemm_layout_t layoutB,
                       const gemm_options_t *opts, void *stream);
 
 /* gemm_mx with overrides (cta_group must be 0 or 2, block_n 0 or 224,
  * k_stage 0 or one of the offered depths: 128 or 256 for MXFP8, 256 or 512
  * for MXFP4). */
 gemm_status_t gemm_mx_ex(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C,
-                         int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA,
-                         int layoutB, const gemm_options_t *opts, void *stream);
+                         int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                         gemm_layout_t layoutA, gemm_layout_t layoutB, const gemm_options_t *opts,
+                         void *stream);
 
 /*
  * gemm_plan_t: the launch gemm_ex would make for a problem. Filled by
@@ -222,7 +245,8 @@ typedef struct {
 /* Fill *plan for a problem on the current device. Same validation and
  * errors as gemm_ex. Needs a GPU, for the SM count and cluster occupancy. */
 gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K,
-                        int dtype_in, int dtype_out, int layoutA, int layoutB,
+                        gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                        gemm_layout_t layoutA, gemm_layout_t layoutB,
                         const void *A, const void *B, const void *C,
                         const gemm_options_t *opts, gemm_plan_t *plan);
 
@@ -230,7 +254,8 @@ gemm_status_t gemm_plan(int64_t M, int64_t N, int64_t K,
  * scale pointers do not affect the plan). workspace_bytes counts the
  * stream-K partial sums only, not the repacked scales. */
 gemm_status_t gemm_mx_plan(int64_t M, int64_t N, int64_t K,
-                           int dtype_in, int dtype_out, int layoutA, int layoutB,
+                           gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                           gemm_layout_t layoutA, gemm_layout_t layoutB,
                            const void *A, const void *B, const void *C,
                            const gemm_options_t *opts, gemm_plan_t *plan);
 
@@ -245,7 +270,8 @@ gemm_status_t gemm_mx_plan(int64_t M, int64_t N, int64_t K,
  */
 gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_host,
                              int64_t M, int64_t N, int64_t K,
-                             int dtype_in, int dtype_out, int layoutA, int layoutB,
+                             gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                             gemm_layout_t layoutA, gemm_layout_t layoutB,
                              void *stream);
 
 /*
@@ -262,12 +288,22 @@ gemm_status_t gemm_from_host(const void *A_host, const void *B_host, void *C_hos
  */
 gemm_status_t gemm_from_host_async(const void *A_host, const void *B_host, void *C_host,
                                    int64_t M, int64_t N, int64_t K,
-                                   int dtype_in, int dtype_out, int layoutA, int layoutB,
+                                   gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                                   gemm_layout_t layoutA, gemm_layout_t layoutB,
                                    void *stream);
 
-/* Free the gemm_from_host staging slots of the current device. Synchronises
- * the device first. */
+/* Free the gemm_from_host staging slots of the current device and empty its
+ * launch cache. Synchronises the device first. */
 gemm_status_t gemm_release_workspace(void);
+
+/* Launch-cache counters of this process, over all devices: plan lookups that
+ * hit or missed, and tensor-map lookups that hit or missed. Any pointer may
+ * be NULL. */
+void gemm_cache_stats(uint64_t *plan_hits, uint64_t *plan_misses, uint64_t *map_hits,
+                      uint64_t *map_misses);
+
+/* Empty the launch cache of the current device (the counters keep counting). */
+gemm_status_t gemm_cache_clear(void);
 
 /*
  * gemm_last_device_status: synchronise `stream`, then read and clear the
@@ -289,6 +325,29 @@ gemm_status_t gemm_last_device_status(void *stream, uint32_t *detail);
 gemm_status_t gemm_selftest_wait_timeout(int32_t timeout_ms, void *stream);
 
 /*
+ * gemm_selftest_withheld_load: run the real GEMM kernel (gemm's arguments,
+ * whole tiles only, cta_group 1 or 2) with the tile producer of the first
+ * unit withholding one stage: for k-block withhold_kb of its first tile it
+ * issues neither the expected-bytes arrive nor the tensor loads. Every
+ * address stays valid and no copy is left in flight; the stage simply never
+ * fills, so the matrix issuer and the epilogue behind it wait until
+ * timeout_ms runs out. The kernel then records GEMM_ERR_TIMEOUT with the
+ * site of the first wait that ran out in the device status word, every role
+ * stops issuing, and the launch returns. C is left partly written. Exists so
+ * that tests can prove that the product kernel's abort path ends.
+ *   withhold_kb  0 <= withhold_kb < the number of ring stages K spans
+ *                (ceil(K / block_k)); otherwise GEMM_ERR_INVALID_ARG.
+ *   timeout_ms   1 .. 10000; otherwise GEMM_ERR_INVALID_ARG.
+ *   cta_group    1 or 2; otherwise GEMM_ERR_INVALID_ARG.
+ * Other errors are gemm's.
+ */
+gemm_status_t gemm_selftest_withheld_load(const void *A, const void *B, void *C,
+                                          int64_t M, int64_t N, int64_t K,
+                                          gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                                          gemm_layout_t layoutB, int32_t cta_group,
+                                          int32_t withhold_kb, int32_t timeout_ms, void *stream);
+
+/*
  * gemm_no_alloc: gemm for callers that must not allocate device memory.
  *
  * The pages have no counterpart to this entry point; it exists for callers
@@ -297,11 +356,12 @@ gemm_status_t gemm_selftest_wait_timeout(int32_t timeout_ms, void *stream);
  * cudaFree could synchronise the device or fail. gemm itself calls
  * cudaMallocAsync/cudaFreeAsync whenever A or B must be re-pitched (a base
  * or row pitch that is not a multiple of 16 bytes, for example K*2 bytes
- * not a multiple of 16). gemm_no_alloc takes the same arguments and computes
- * the same result, but it never allocates or frees: the re-pitched copies go
- * into one fixed device array that the library holds on every GPU that
- * loads it, GEMM_NO_ALLOC_SCRATCH_BYTES (32 MiB) in size, until the process
- * exits.
+ * not a multiple of 16) and whenever its plan splits tiles along K (the
+ * stream-K partial sums and flags). gemm_no_alloc takes the same arguments
+ * and computes the same result, but it never allocates or frees: the
+ * re-pitched copies and the stream-K workspace go into one fixed device
+ * array that the library holds on every GPU that loads it,
+ * GEMM_NO_ALLOC_SCRATCH_BYTES (32 MiB) in size, until the process exits.
  *
  *   - Limit: the padded copies (rows x row bytes rounded up to 16, A then B,
  *     each started on a 256-byte boundary) must fit in
@@ -312,9 +372,9 @@ gemm_status_t gemm_selftest_wait_timeout(int32_t timeout_ms, void *stream);
  *   - Stream-K: when the plan splits tiles along K, the partial sums and
  *     flags go into the same array after the copies. When they do not fit,
  *     the call keeps every tile whole instead (same result bound).
- *   - Set-up: the first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current. Make this first call
- *     before any stream capture.
+ *   - Set-up: the first call on a device (whether or not it needs the
+ *     array) looks up the array's device address (cudaGetSymbolAddress) with
+ *     that device current. Make this first call before any stream capture.
  *   - Sharing: every call on a device uses the same array, and the array
  *     keeps the previous call's contents. Nothing in it has to start at zero:
  *     each call writes every element it later reads. Calls whose work
@@ -326,7 +386,8 @@ gemm_status_t gemm_selftest_wait_timeout(int32_t timeout_ms, void *stream);
 
 gemm_status_t gemm_no_alloc(const void *A, const void *B, void *C,
                             int64_t M, int64_t N, int64_t K,
-                            int dtype_in, int dtype_out, int layoutA, int layoutB,
+                            gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
+                            gemm_layout_t layoutA, gemm_layout_t layoutB,
                             void *stream);
 
 /*
@@ -362,7 +423,7 @@ gemm_status_t gemm_schedule_jobs(int32_t num_tiles, int32_t units, int32_t k_blo
                                  int32_t unit, gemm_job_t *jobs, int32_t max_jobs, int32_t *n_jobs);
 
 /* Human-readable name of a status code. Never NULL. */
-const char *gemm_status_string(int status);
+const char *gemm_status_string(gemm_status_t status);
 
 /* Number of GEMM kernel launches (main kernel and operand copies) this
  * process made on any device. Used to count launches in a timed region. */

@@ -39,7 +39,8 @@ def test_header_declares_the_entry_points():
                      "gemm_status_string", "gemm_selftest_wait_timeout", "gemm_launch_count",
                      "gemm_release_workspace", "gemm_mx", "gemm_mx_ex", "gemm_mx_plan",
                      "gemm_schedule_jobs", "gemm_no_alloc", "attention_fwd", "attention_fwd_ex",
-                     "gemm_from_host_async"):
+                     "gemm_from_host_async", "gemm_cache_stats", "gemm_cache_clear",
+                     "gemm_selftest_withheld_load"):
         assert required in names
 
 
@@ -60,9 +61,38 @@ def test_enums_match_header():
 
 
 def test_struct_sizes():
-    # gemm_options_t: 8 int32 fields; gemm_plan_t: 16 int32 fields
-    assert ctypes.sizeof(binding.GemmOptions) == 32
+    # gemm_options_t: 8 int32 fields and the clock-trace pointer; gemm_plan_t: 16 int32 fields
+    assert ctypes.sizeof(binding.GemmOptions) == 40
+    assert binding.GemmOptions.clock_trace.offset == 32
     assert ctypes.sizeof(binding.GemmPlan) == 64
+    assert re.search(r"int32_t reserved;\s*uint64_t \*clock_trace;\s*\} gemm_options_t;", header_text())
+
+
+def test_prototypes_use_the_enum_types():
+    """Every entry point that takes an element type or a layout declares it with
+    gemm_dtype_t / gemm_layout_t, so that a C caller gets type checking."""
+    text = re.sub(r"/\*.*?\*/", "", header_text(), flags=re.S)
+    assert not re.search(r"\bint\s+(dtype_in|dtype_out|layoutA|layoutB)\b", text)
+    assert len(re.findall(r"gemm_dtype_t dtype_in", text)) >= 10
+    assert len(re.findall(r"gemm_layout_t layoutB", text)) >= 10
+    assert "const char *gemm_status_string(gemm_status_t status);" in text
+
+
+def test_cache_entry_points_without_gpu():
+    """The cache counters are readable without a device; clearing needs one."""
+    stats = dtg.gemm_cache_stats()
+    assert set(stats) == {"plan_hits", "plan_misses", "map_hits", "map_misses"}
+    assert all(v >= 0 for v in stats.values())
+    import torch
+    if not torch.cuda.is_available():
+        assert binding.lib.gemm_cache_clear() == binding.GEMM_ERR_NO_DEVICE
+
+
+@pytest.mark.parametrize("cg,kb,ms,expect", [(3, 0, 20, 1), (0, 0, 20, 1), (2, -1, 20, 1), (2, 0, 0, 1),
+                                              (1, 0, 20000, 1)])
+def test_withheld_load_selftest_validates_on_host(cg, kb, ms, expect):
+    rc = binding.lib.gemm_selftest_withheld_load(FAKE, FAKE, FAKE, 256, 256, 256, 0, 2, 0, cg, kb, ms, None)
+    assert rc == expect
 
 
 def test_status_strings():
