@@ -13,7 +13,10 @@ torch.cuda.synchronize() on both sides. CUDA events are recorded on the
 launching stream at both ends of the timed region; the mean launch duration
 is the region time over K. Operands rotate over enough
 (A, B, C) sets to exceed twice the L2 size, so every step reads from HBM.
-SM clocks are sampled with nvidia-smi during the timed region.
+The SM clock of each timed launch is measured inside the kernel (the clock
+trace option: CTA 0's cycle counter over the global timer), and nvidia-smi
+is sampled during the timed region for throttle reasons; its clock counts
+only from samples that drew load power.
 Under torchrun (N > 1) every rank runs its own replica; the time is the
 maximum over ranks, and rank 0 prints one JSON line.
 
@@ -218,10 +221,39 @@ class ClockSampler:
                     reasons.add(name)
         if not sm:
             return None
-        loaded = [s for s, p in zip(sm, power) if p > 300.0] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": sm_max,
+        # only samples taken while the GPU drew load power count; a region shorter
+        # than the sampling period may have none, and then no clock is claimed
+        loaded = [s for s, p in zip(sm, power) if p > 300.0]
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": sm_max,
                 "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(loaded),
                 "power_w_max": max(power) if power else None}
+
+
+def kernel_clock_mhz(trace: torch.Tensor):
+    """SM clock of each traced launch from its clock_trace words (global timer ns and
+    SM cycles of CTA 0 at its start and end): cycles / ns * 1000, in MHz."""
+    t = trace.cpu().tolist()
+    mhz = [(c1 - c0) / (n1 - n0) * 1e3 for n0, c0, n1, c1 in t if n1 > n0 and c1 > c0]
+    return mhz
+
+
+def merge_clocks(smi: dict | None, mhz: list) -> dict | None:
+    """The line's clock record: the in-kernel SM clock (median over the timed launches)
+    where the launches were traced, nvidia-smi's samples under load otherwise; throttle
+    reasons and the maximum clock always come from nvidia-smi."""
+    out = dict(smi) if smi else {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                                 "samples_under_load": 0, "power_w_max": None}
+    out["smi_sm_mhz_under_load"] = out.get("sm_mhz")
+    if mhz:
+        out["sm_mhz"] = statistics.median(mhz)
+        out["sm_mhz_source"] = (f"in-kernel: SM cycles over global-timer ns of CTA 0, median of {len(mhz)} "
+                                "timed launches")
+        out["kernel_mhz_min"] = min(mhz)
+        out["kernel_mhz_max"] = max(mhz)
+    else:
+        out["sm_mhz_source"] = ("nvidia-smi samples drawing > 300 W" if out.get("sm_mhz") is not None
+                                else "none: no sample under load")
+    return out
 
 
 def oracle_sample(w, ops, rows_total: int, threads: int):
@@ -271,16 +303,17 @@ def run_reference(args):
     # every timed step takes the same number of rows; the whole timed run is one
     # oracle call over all steps' rows (so B is decoded once), sized to ~60 s
     budget = 60.0
-    rows = max(1, min(4 * threads, int(max(budget - t_one, 1.0) / t_row / max(1, args.steps))))
+    rows = max(1, min(4 * threads, w.M, int(max(budget - t_one, 1.0) / t_row / max(1, args.steps))))
     stride = max(1, w.M // rows)
     samples = [list(range((s * 7) % stride, w.M, stride))[:rows] for s in range(args.steps + args.warmup)]
     for s in range(min(args.warmup, 2)):
         oracle_rows(oracle, w, ops, samples[s], threads)
     timed_rows = [r for s in range(args.steps) for r in samples[args.warmup + s]]
+    rows = len(timed_rows) // max(1, args.steps)
     t0 = time.perf_counter()
     oracle_rows(oracle, w, ops, timed_rows, threads)
     dt = time.perf_counter() - t0
-    flops = 2.0 * rows * w.N * w.K * args.steps
+    flops = 2.0 * len(timed_rows) * w.N * w.K
     value = flops / dt / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
@@ -384,14 +417,24 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     opts = None if args.stream_k == "auto" else {"stream_k": {"off": 1, "on": 2}[args.stream_k]}
+    # each timed launch writes its own clock-trace words (CTA 0's global timer and SM
+    # cycle counter at its start and end): the clock the kernel ran at
+    trace = torch.zeros((args.steps, 4), dtype=torch.int64, device=dev)
+    timed_opts = []
+    for i in range(args.steps):
+        o = dtg.GemmOptions()
+        if opts:
+            o.stream_k = opts["stream_k"]
+        o.clock_trace = trace[i].data_ptr()
+        timed_opts.append(o)
 
-    def step(i, st=stream):
+    def step(i, st=stream, o=opts):
         j = i % n_sets
         if is_mx(w):
             A, B, SFA, SFB = sets[j]
-            dtg.gemm_mx(A, B, SFA, SFB, Cs[j], K=w.K, stream=st, options=opts)
+            dtg.gemm_mx(A, B, SFA, SFB, Cs[j], K=w.K, stream=st, options=o)
         else:
-            dtg.gemm(As[j], Bs[j], Cs[j], layout_b=w.layout_b, stream=st, options=opts)
+            dtg.gemm(As[j], Bs[j], Cs[j], layout_b=w.layout_b, stream=st, options=o)
 
     for i in range(args.warmup):
         step(i)
@@ -418,7 +461,7 @@ def run_ours(args):
         launches0 = dtg.gemm_launch_count()
         with torch.cuda.graph(graph):
             for i in range(args.steps):
-                step(args.warmup + i, st=None)
+                step(args.warmup + i, st=None, o=timed_opts[i])
         launches = dtg.gemm_launch_count() - launches0
         graph.replay()
         torch.cuda.synchronize(dev)
@@ -432,7 +475,7 @@ def run_ours(args):
     ev_start.record(stream)
     if graph is None:
         for i in range(args.steps):
-            step(args.warmup + i)
+            step(args.warmup + i, o=timed_opts[i])
     else:
         graph.replay()
     ev_end.record(stream)
@@ -441,7 +484,7 @@ def run_ours(args):
         pg.barrier()
     if graph is None:
         launches = dtg.gemm_launch_count() - launches0
-    clocks = sampler.stop()
+    clocks = merge_clocks(sampler.stop(), kernel_clock_mhz(trace))
     status, detail = dtg.gemm_last_device_status(stream)
     if status != dtg.GEMM_OK:
         raise RuntimeError(f"device status {dtg.gemm_status_string(status)} site {detail:#x}")
@@ -600,6 +643,7 @@ def run_attention(args):
     torch.cuda.synchronize(dev)
     launches = dtg.gemm_launch_count() - launches0
     clocks = sampler.stop()
+    clocks = merge_clocks(clocks, [])
     status, detail = dtg.gemm_last_device_status(stream)
     if status != dtg.GEMM_OK:
         raise RuntimeError(f"device status {dtg.gemm_status_string(status)} site {detail:#x}")
