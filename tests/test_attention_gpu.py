@@ -1,8 +1,10 @@
 """Parity of the attention forward pass (attention_fwd) against the FP64 oracle.
 
 Bound (oracle/tolerance.py): |O - O_ref| <= 2^-7 * sum_k p_k |v_k| / l + 1e-6
-+ one output ulp, and |LSE - LSE_ref| <= 2^-7, from the rounding of the
-probabilities to the operand type before the PV product. Closed forms are
++ one output ulp, from the rounding of the probabilities to the operand type
+before the PV product; and |LSE - LSE_ref| <= 2^-16 * S_abs + 2^-16 + 4 ulps,
+from the FP32 scores (S_abs = scale * max_j sum_i |q_i k_ji|) and the FP32
+row sum. Closed forms are
 checked exactly: with Q = 0 every visible key has probability 1, so O is the
 mean of the visible value rows; causal row 0 sees only key 0, so it returns
 V[0]; a row with no visible key returns zeros and LSE = -inf.
@@ -46,11 +48,26 @@ def run(dtg, Q, K, V, causal=False, scale=None, max_ctas=0):
     return O.cpu(), lse.cpu()
 
 
-def case(dtg, B, H, Lq, Lk, dtype="bf16", causal=False, seed=0, q_scale=1.0, rows=None, scale=None,
-         max_ctas=0):
-    Q, K, V = workloads.make_attention_operands(B, H, Lq, Lk, 128, dtype, ("normal", 1.0), seed)
-    Q = (Q.float() * q_scale).to(TDT[dtype])
-    O, lse = run(dtg, Q, K, V, causal, scale, max_ctas)
+def score_abs_max(Q, K, scale, rows=None):
+    """scale * max_j sum_i |q_i k_ji| for each query row (over every key of its head):
+    the size of the FP32 score error, for the log-sum-exp bound."""
+    B, H, Lq, d = Q.shape
+    Lk = K.shape[2]
+    scale = d ** -0.5 if scale is None else scale
+    Qa = Q.double().abs().reshape(B * H, Lq, d)
+    Ka = K.double().abs().reshape(B * H, Lk, d)
+    if rows is None:
+        return (torch.bmm(Qa, Ka.transpose(1, 2)).amax(dim=2).reshape(-1) * scale).numpy()
+    rows = np.asarray(rows)
+    head, qi = rows // Lq, rows % Lq
+    out = np.empty(len(rows))
+    for h in np.unique(head):
+        sel = np.nonzero(head == h)[0]
+        out[sel] = (Qa[h, qi[sel]] @ Ka[h].T).amax(dim=1).numpy() * scale
+    return out
+
+
+def check(Q, K, V, O, lse, B, H, Lq, Lk, dtype, causal, scale=None, rows=None):
     O_ref, O_abs, L_ref = oracle.attention_ref(bits(Q), bits(K), bits(V), B, H, Lq, Lk, 128, dtype, causal,
                                                scale, rows=rows)
     got = O.float().numpy().astype(np.float64).reshape(-1, 128)
@@ -59,9 +76,17 @@ def case(dtg, B, H, Lq, Lk, dtype="bf16", causal=False, seed=0, q_scale=1.0, row
         got, lse = got[rows], lse[rows]
     ok, ratio, n_bad, first = tolerance.check_attention(got, O_ref, O_abs, dtype)
     assert ok, f"{n_bad} out of bound (worst {ratio:.3g}) first {first}: gpu {got[first]} ref {O_ref[first]}"
-    fin = np.isfinite(L_ref)
-    assert np.array_equal(np.isfinite(lse), fin)
-    assert np.all(np.abs(lse[fin] - L_ref[fin]) <= tolerance.ATT_LSE_ABS)
+    ok, lratio, n_bad = tolerance.check_lse(lse, L_ref, score_abs_max(Q, K, scale, rows))
+    assert ok, f"log-sum-exp: {n_bad} rows out of bound (worst error/bound {lratio:.3g})"
+    return ratio, lratio
+
+
+def case(dtg, B, H, Lq, Lk, dtype="bf16", causal=False, seed=0, q_scale=1.0, rows=None, scale=None,
+         max_ctas=0):
+    Q, K, V = workloads.make_attention_operands(B, H, Lq, Lk, 128, dtype, ("normal", 1.0), seed)
+    Q = (Q.float() * q_scale).to(TDT[dtype])
+    O, lse = run(dtg, Q, K, V, causal, scale, max_ctas)
+    return check(Q, K, V, O, lse, B, H, Lq, Lk, dtype, causal, scale, rows)
 
 
 # ---------------------------------------------------------------- one tile, one block
@@ -111,6 +136,36 @@ def test_shapes(dtg, shape, causal):
 def test_large_scores_rescale(dtg, dtype):
     """Scores in the tens: the running maximum grows across blocks and O is rescaled."""
     case(dtg, 1, 2, 256, 1024, dtype, seed=4, q_scale=6.0)
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("profile", ["jump", "ramp", "fall"])
+def test_row_maximum_moves_mid_row(dtg, profile, causal):
+    """Key blocks scaled so that the row maxima (in log2 units of the scaled scores)
+    jump by far more than the lazy-rescale threshold of 2^8 mid-row ("jump": blocks 3
+    and later x12), climb past it in steps each below it ("ramp": block j x (1 + j/2)),
+    or fall after the first blocks ("fall": x8 then x1). O and the log-sum-exp must
+    match the oracle in every case."""
+    B, H, Lq, Lk = 1, 2, 256, 1024
+    Q, K, V = workloads.make_attention_operands(B, H, Lq, Lk, 128, "bf16", ("normal", 1.0), 40)
+    blk = torch.arange(Lk) // 128
+    if profile == "jump":
+        f = torch.where(blk >= 3, 12.0, 1.0)
+    elif profile == "ramp":
+        f = 1.0 + blk.double() / 2
+    else:
+        f = torch.where(blk < 2, 8.0, 1.0)
+    K = (K.double() * f[None, None, :, None]).to(torch.bfloat16)
+    O, lse = run(dtg, Q, K, V, causal)
+    check(Q, K, V, O, lse, B, H, Lq, Lk, "bf16", causal)
+    # the scaled scores' row maxima (log2 units) do what the profile says: grow by more
+    # than 2^8 past the first block, or never rise after the first two blocks
+    t = (Q.double() @ K.double().transpose(-1, -2)) * 128 ** -0.5 / math.log(2)
+    if profile in ("jump", "ramp"):
+        grew = (t.amax(-1) - t[..., :128].amax(-1) > 8).double().mean().item()
+        assert grew > 0.9, grew
+    else:
+        assert bool((t[..., 256:].amax(-1) < t[..., :256].amax(-1)).all())
 
 
 def test_custom_scale(dtg):

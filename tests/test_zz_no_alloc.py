@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from oracle import tolerance
 import workloads
 
@@ -60,10 +61,16 @@ def test_no_alloc_matches_gemm_on_two_calls_in_a_row(lib):
         ref = C_gemm.double().cpu().numpy()
         ok, ratio, n_bad, first = tolerance.check(C_new.double().cpu().numpy(), ref, C_abs, dout)
         assert ok, f"{n_bad} elements differ beyond the bound, first {first}"
+        # and directly against the FP64 oracle, so that a fault in the re-pitch copy
+        # that both entry points share cannot pass unnoticed
+        C_ref, C_ref_abs = oracle.gemm_ref(workloads.as_bits(A), workloads.as_bits(B), M, N, K, din, layout_b)
+        ok, ratio, n_bad, first = tolerance.check(C_new.double().cpu().numpy(), C_ref, C_ref_abs, dout)
+        assert ok, f"{n_bad} elements out of the oracle's bound, first {first}"
 
 
 def test_no_alloc_rejects_operands_beyond_its_array(lib):
-    # Padded A alone needs 8200 x 2056 x 2 bytes > 32 MiB: refused before any launch.
+    # Padded A alone needs 8200 x 2112 x 2 bytes (rows padded to 128-byte multiples)
+    # > 32 MiB: refused before any launch.
     M, N, K = 8200, 64, 2050
     A = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
     B = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
