@@ -700,7 +700,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 uint32_t v[32];
                 if (!skip) {
                     tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * EPI_COLS), v);
-                    tmem_ld_wait();
+                    tmem_ld_wait_regs(v);
                 }
                 if (c == CHUNKS - 1 && i + 1 < num_jobs) {
                     // accumulator fully read: hand it back to the MMA issuer (after this
@@ -873,15 +873,24 @@ static __global__ void pack_scales_kernel(const uint8_t *__restrict__ sf, uint8_
 
 // Copy `rows` rows of `row_bytes` bytes each (source pitch row_bytes, densely
 // packed) into a buffer whose row pitch `dst_pitch` is a multiple of 16 bytes
-// and whose base is 256-byte aligned, so the TMA engine can describe it. The
+// (the library pads to 128) and whose base is 256-byte aligned, so the TMA
+// engine can describe it. The
 // bytes past row_bytes in each destination row are not written: the tensor
 // map keeps the logical width, and TMA zero-fills past it.
 //
 // V is the widest word that divides the source base, row_bytes and hence
 // every source row start (4 for a 4100-byte BF16 row), so every access is an
-// aligned V-byte word inside the source or destination row. Each block walks
-// whole rows (grid-stride); consecutive threads take consecutive words, so
-// both the loads and the stores of a warp are contiguous.
+// aligned V-byte word inside the source or destination row. Each warp copies
+// whole rows (grid-stride over rows): its lanes take consecutive words, and
+// every lane keeps UNROLL loads in flight before it stores them (64 bytes per
+// lane: 2 KB per warp, ~48 KB per SM at 3 blocks of 8 warps), enough to keep
+// HBM busy although the words are small.
+//
+// Launched with programmatic stream serialisation: the blocks may start while
+// the previous grid on the stream drains, and wait (griddepcontrol.wait) for
+// it before touching memory, since the source may be that grid's output and
+// the destination scratch that it read. They then let the GEMM that follows
+// launch at once; it waits for this grid to complete before it reads.
 template <int V>
 __global__ void __launch_bounds__(256) realign_rows_kernel(const uint8_t *__restrict__ src,
                                                            uint8_t *__restrict__ dst, int64_t rows,
@@ -893,22 +902,25 @@ __global__ void __launch_bounds__(256) realign_rows_kernel(const uint8_t *__rest
                                   typename std::conditional<V == 4, uint32_t,
                                                             typename std::conditional<V == 2, uint16_t,
                                                                                       uint8_t>::type>::type>::type>::type;
+    grid_dependency_wait();
+    grid_launch_dependents();
+    constexpr int UNROLL = V >= 4 ? 64 / V : 32;
     const int64_t words = row_bytes / V;
-    // independent loads in flight per thread before their stores (~64 KB per SM at 8 blocks)
-    constexpr int UNROLL = V >= 16 ? 2 : V == 8 ? 4 : 8;
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const int lane = static_cast<int>(threadIdx.x % 32u);
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x / 32u);
+    for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x / 32u) + threadIdx.x / 32u; r < rows; r += warps) {
         const W *s = reinterpret_cast<const W *>(src + r * row_bytes);
         W *d = reinterpret_cast<W *>(dst + r * dst_pitch);
-        for (int64_t i0 = threadIdx.x; i0 < words; i0 += UNROLL * 256) {
+        for (int64_t i0 = lane; i0 < words; i0 += UNROLL * 32) {
             W v[UNROLL];
 #pragma unroll
             for (int u = 0; u < UNROLL; ++u)
-                if (i0 + u * 256 < words)
-                    v[u] = __ldg(s + i0 + u * 256);
+                if (i0 + u * 32 < words)
+                    v[u] = __ldg(s + i0 + u * 32);
 #pragma unroll
             for (int u = 0; u < UNROLL; ++u)
-                if (i0 + u * 256 < words)
-                    d[i0 + u * 256] = v[u];
+                if (i0 + u * 32 < words)
+                    d[i0 + u * 32] = v[u];
         }
     }
 }
