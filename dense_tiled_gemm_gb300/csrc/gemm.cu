@@ -50,6 +50,7 @@ int default_k_slabs(int cg, int kind)
 
 struct Variant {
     int cg;
+    int mc;            // CTA pairs per cluster sharing A tiles (1 or 2)
     int bn;
     int ks;            // K slabs (128 bytes of K each) per ring stage
     int kind;          // KIND_F16, KIND_F8, KIND_MXF8 or KIND_MXF4
@@ -58,11 +59,11 @@ struct Variant {
     bool b_mn_ok;      // MN-major B needs 64-column TMA boxes per CTA (16-bit only)
 };
 
-template <int CG, int BN, int KS, int KIND>
+template <int CG, int BN, int KS, int KIND, int MC = 1>
 constexpr Variant variant(bool b_mn_ok)
 {
-    return {CG, BN, KS, KIND, TileConfig<CG, BN, KS, KIND>::STAGE_BYTES,
-            reinterpret_cast<const void *>(&gemm_tcgen05_kernel<CG, BN, KS, KIND>), b_mn_ok};
+    return {CG, MC, BN, KS, KIND, TileConfig<CG, BN, KS, KIND>::STAGE_BYTES,
+            reinterpret_cast<const void *>(&gemm_tcgen05_kernel<CG, BN, KS, KIND, MC>), b_mn_ok};
 }
 
 const Variant kVariants[] = {
@@ -72,6 +73,9 @@ const Variant kVariants[] = {
     variant<2, 256, 2, KIND_F8>(false),  variant<2, 224, 2, KIND_F8>(false),  variant<1, 256, 2, KIND_F8>(false),
     variant<2, 224, 1, KIND_MXF8>(false), variant<2, 224, 2, KIND_MXF8>(false),
     variant<2, 224, 1, KIND_MXF4>(false), variant<2, 224, 2, KIND_MXF4>(false),
+    // two pairs per cluster sharing A (gemm_options_t.cluster_pairs = 2)
+    variant<2, 256, 1, KIND_F16, 2>(true), variant<2, 256, 2, KIND_F16, 2>(true),
+    variant<2, 256, 1, KIND_F8, 2>(false), variant<2, 256, 2, KIND_F8, 2>(false),
 };
 constexpr int NUM_VARIANTS = sizeof(kVariants) / sizeof(kVariants[0]);
 
@@ -222,12 +226,13 @@ gemm_status_t device_state(DeviceState **out)
                 d.max_units[v] = per_sm * d.sms;
             } else {
                 cudaLaunchConfig_t cfg = {};
-                cfg.gridDim = dim3(2 * d.sms);
+                const int cs = var.cg * var.mc;
+                cfg.gridDim = dim3(static_cast<unsigned>(cs * d.sms));
                 cfg.blockDim = dim3(NUM_THREADS);
                 cfg.dynamicSmemBytes = SMEM_LIMIT;
                 cudaLaunchAttribute attr[1];
                 attr[0].id = cudaLaunchAttributeClusterDimension;
-                attr[0].val.clusterDim.x = 2;
+                attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
                 attr[0].val.clusterDim.y = 1;
                 attr[0].val.clusterDim.z = 1;
                 cfg.attrs = attr;
@@ -282,8 +287,10 @@ gemm_status_t validate(const void *A, const void *B, const void *C, int64_t M, i
             return GEMM_ERR_INVALID_ARG;
         if (o->block_n != 0 && o->block_n != 224 && o->block_n != 256)
             return GEMM_ERR_UNSUPPORTED;
-        if (o->k_stage < 0 || o->stream_k < 0 || o->reserved != 0)
+        if (o->k_stage < 0 || o->stream_k < 0 || o->cluster_pairs < 0)
             return GEMM_ERR_INVALID_ARG;
+        if (o->cluster_pairs > 2)
+            return GEMM_ERR_UNSUPPORTED;
         if (o->stream_k > 2)
             return GEMM_ERR_UNSUPPORTED;
         const int sk = kind_slab_k(kind_for(dtype_in, scaled));
@@ -295,7 +302,7 @@ gemm_status_t validate(const void *A, const void *B, const void *C, int64_t M, i
 
 struct Plan {
     int variant;
-    int num_m, num_n, num_tiles, num_kb;
+    int num_m, num_n, num_tiles, num_kb;   // num_n, num_tiles: scheduling units (two tiles each with mc = 2)
     int grid_ctas;
     int group_m;
     int sk_tiles;          // trailing tiles split along K
@@ -315,7 +322,7 @@ struct PlanKey {
     int32_t dtype_in, dtype_out, layoutB, scaled;
     int32_t misalign;   // bit 0: A, bit 1: B, bit 2: C not describable to the TMA engine
     int32_t cta_group, block_n, max_clusters, group_m, k_stage, stream_k;
-    int32_t pad;
+    int32_t cluster_pairs;
 };
 
 struct MapKey {
@@ -423,6 +430,8 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
     const int sk_elems = kind_slab_k(kind);
     const int64_t k_bytes = row_bytes(kind, K);
     const int mode = o ? o->stream_k : 0;
+    // pairs sharing A only on request: two pairs per cluster (cluster_pairs = 2)
+    const int want_mc = (o && o->cluster_pairs) ? o->cluster_pairs : 1;
     int best = -1, best_sk = 0;
     double best_cost = 0;
     for (int v = 0; v < NUM_VARIANTS; ++v) {
@@ -437,12 +446,16 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
             continue;
         if (b_mn && !var.b_mn_ok)
             continue;
+        if (var.mc != want_mc)
+            continue;
         int units = d.max_units[v];
         if (o && o->max_clusters)
             units = std::min(units, static_cast<int>(o->max_clusters));
         if (units < 1)
             continue;
-        const int64_t tiles = ((M + 128 * var.cg - 1) / (128 * var.cg)) * ((N + var.bn - 1) / var.bn);
+        // scheduling units: one tile, or with mc = 2 two tiles side by side in N
+        const int64_t n_units = ((N + var.bn - 1) / var.bn + var.mc - 1) / var.mc;
+        const int64_t tiles = ((M + 128 * var.cg - 1) / (128 * var.cg)) * n_units;
         const int64_t kb = (K + static_cast<int64_t>(sk_elems) * var.ks - 1) / (static_cast<int64_t>(sk_elems) * var.ks);
         const Cost c = plan_cost(tiles, units, kb, k_bytes);
         const double scale = var.bn * (var.cg == 1 ? 1.15 : 1.0);
@@ -463,7 +476,7 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
         units = std::min(units, static_cast<int>(o->max_clusters));
     pl->variant = best;
     pl->num_m = static_cast<int>((M + 128 * var.cg - 1) / (128 * var.cg));
-    pl->num_n = static_cast<int>((N + var.bn - 1) / var.bn);
+    pl->num_n = static_cast<int>(((N + var.bn - 1) / var.bn + var.mc - 1) / var.mc);
     const int64_t tiles = static_cast<int64_t>(pl->num_m) * pl->num_n;
     if (tiles > INT_MAX)
         return GEMM_ERR_UNSUPPORTED;
@@ -472,7 +485,7 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
     pl->num_kb = static_cast<int>((K + stage_k - 1) / stage_k);
     pl->sk_tiles = best_sk;
     // with stream-K every unit takes a share; otherwise no more units than tiles
-    pl->grid_ctas = static_cast<int>(best_sk ? units : std::min<int64_t>(tiles, units)) * var.cg;
+    pl->grid_ctas = static_cast<int>(best_sk ? units : std::min<int64_t>(tiles, units)) * var.cg * var.mc;
     pl->ws_bytes = best_sk ? sk_workspace_bytes(pl->grid_ctas, var.bn) : 0;
     pl->group_m = (o && o->group_m) ? o->group_m : 8;
     pl->realign_a = misaligned(A, row_bytes(kind, K), 1);
@@ -505,6 +518,7 @@ PlanKey plan_key(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, i
         k.group_m = o->group_m;
         k.k_stage = o->k_stage;
         k.stream_k = o->stream_k;
+        k.cluster_pairs = o->cluster_pairs;
     }
     return k;
 }
@@ -618,7 +632,7 @@ gemm_status_t realign(const void *src, int64_t rows, int64_t cols, int eb, int s
     return realign_into(src, rows, cols, ld, eb, sms, st, *out);
 }
 
-template <int CG, int BN, int KS, int KIND>
+template <int CG, int BN, int KS, int KIND, int MC = 1>
 cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap *maps, const KernelParams &kp,
                            cudaStream_t st)
 {
@@ -635,39 +649,43 @@ cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap *maps
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (CG == 2) {
+    if (CG * MC > 1) {
         attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.x = CG * MC;
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<CG, BN, KS, KIND>, maps[0], maps[1], maps[2], maps[3],
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<CG, BN, KS, KIND, MC>, maps[0], maps[1], maps[2], maps[3],
                               maps[4], kp);
 }
 
 cudaError_t launch_any(const Variant &v, int grid_ctas, uint32_t smem, const CUtensorMap *maps,
                        const KernelParams &kp, cudaStream_t st)
 {
-#define DTG_LAUNCH(CG, BN, KS, KIND)                                                               \
-    if (v.cg == CG && v.bn == BN && v.ks == KS && v.kind == KIND)                                  \
-        return launch_variant<CG, BN, KS, KIND>(grid_ctas, smem, maps, kp, st);
-    DTG_LAUNCH(2, 256, 1, KIND_F16)
-    DTG_LAUNCH(2, 224, 1, KIND_F16)
-    DTG_LAUNCH(1, 256, 1, KIND_F16)
-    DTG_LAUNCH(2, 256, 2, KIND_F16)
-    DTG_LAUNCH(2, 224, 2, KIND_F16)
-    DTG_LAUNCH(1, 256, 2, KIND_F16)
-    DTG_LAUNCH(2, 256, 1, KIND_F8)
-    DTG_LAUNCH(2, 224, 1, KIND_F8)
-    DTG_LAUNCH(1, 256, 1, KIND_F8)
-    DTG_LAUNCH(2, 256, 2, KIND_F8)
-    DTG_LAUNCH(2, 224, 2, KIND_F8)
-    DTG_LAUNCH(1, 256, 2, KIND_F8)
-    DTG_LAUNCH(2, 224, 1, KIND_MXF8)
-    DTG_LAUNCH(2, 224, 2, KIND_MXF8)
-    DTG_LAUNCH(2, 224, 1, KIND_MXF4)
-    DTG_LAUNCH(2, 224, 2, KIND_MXF4)
+#define DTG_LAUNCH(CG, BN, KS, KIND, MC)                                                           \
+    if (v.cg == CG && v.bn == BN && v.ks == KS && v.kind == KIND && v.mc == MC)                    \
+        return launch_variant<CG, BN, KS, KIND, MC>(grid_ctas, smem, maps, kp, st);
+    DTG_LAUNCH(2, 256, 1, KIND_F16, 1)
+    DTG_LAUNCH(2, 224, 1, KIND_F16, 1)
+    DTG_LAUNCH(1, 256, 1, KIND_F16, 1)
+    DTG_LAUNCH(2, 256, 2, KIND_F16, 1)
+    DTG_LAUNCH(2, 224, 2, KIND_F16, 1)
+    DTG_LAUNCH(1, 256, 2, KIND_F16, 1)
+    DTG_LAUNCH(2, 256, 1, KIND_F8, 1)
+    DTG_LAUNCH(2, 224, 1, KIND_F8, 1)
+    DTG_LAUNCH(1, 256, 1, KIND_F8, 1)
+    DTG_LAUNCH(2, 256, 2, KIND_F8, 1)
+    DTG_LAUNCH(2, 224, 2, KIND_F8, 1)
+    DTG_LAUNCH(1, 256, 2, KIND_F8, 1)
+    DTG_LAUNCH(2, 224, 1, KIND_MXF8, 1)
+    DTG_LAUNCH(2, 224, 2, KIND_MXF8, 1)
+    DTG_LAUNCH(2, 224, 1, KIND_MXF4, 1)
+    DTG_LAUNCH(2, 224, 2, KIND_MXF4, 1)
+    DTG_LAUNCH(2, 256, 1, KIND_F16, 2)
+    DTG_LAUNCH(2, 256, 2, KIND_F16, 2)
+    DTG_LAUNCH(2, 256, 1, KIND_F8, 2)
+    DTG_LAUNCH(2, 256, 2, KIND_F8, 2)
 #undef DTG_LAUNCH
     return cudaErrorInvalidValue;
 }
@@ -715,7 +733,9 @@ bool encode_maps(const Plan &pl, Operand a, Operand b, const void *sfa, const vo
     const uint32_t box_k = var.kind == KIND_F16 ? 64 : 128;
     std::memset(maps, 0, 5 * sizeof(CUtensorMap));
     const CUtensorMapDataType in_dt = tma_dtype(dtype_in);
-    bool ok = encode_2d(&maps[0], in_dt, a.ptr, width, M, a.ld * eb, box_k, BLOCK_M_CTA, CU_TENSOR_MAP_SWIZZLE_128B);
+    // with two pairs sharing A each CTA loads half of its 128 rows
+    bool ok = encode_2d(&maps[0], in_dt, a.ptr, width, M, a.ld * eb, box_k, BLOCK_M_CTA / var.mc,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (!b_mn)
         ok = ok && encode_2d(&maps[1], in_dt, b.ptr, width, N, b.ld * eb, box_k, var.bn / var.cg,
                              CU_TENSOR_MAP_SWIZZLE_128B);
@@ -992,7 +1012,7 @@ gemm_status_t plan_query(int64_t M, int64_t N, int64_t K, int dtype_in, int dtyp
     plan->block_k = kind_slab_k(var.kind) * var.ks;
     const Layout lay = layout_for(var, dtype_out);
     plan->stages = static_cast<int32_t>(lay.stages);
-    plan->num_tiles = pl.num_tiles;
+    plan->num_tiles = static_cast<int32_t>(static_cast<int64_t>(pl.num_m) * ((N + var.bn - 1) / var.bn));
     plan->grid_ctas = pl.grid_ctas;
     plan->group_m = pl.group_m;
     plan->realign_a = pl.realign_a;
@@ -1002,6 +1022,7 @@ gemm_status_t plan_query(int64_t M, int64_t N, int64_t K, int dtype_in, int dtyp
     plan->num_sms = d->sms;
     plan->sk_tiles = pl.sk_tiles;
     plan->workspace_bytes = static_cast<int32_t>(pl.ws_bytes);
+    plan->cluster_pairs = var.mc;
     return GEMM_OK;
 }
 

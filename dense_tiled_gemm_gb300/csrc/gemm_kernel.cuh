@@ -395,7 +395,17 @@ __device__ __forceinline__ void store_row_direct(const KernelParams &p, int row,
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int CG, int BN, int KS, int KIND>
+// MC = CTA pairs per cluster that share their A tiles (1 or 2; 2 needs CG = 2).
+// With MC = 2 a cluster of four CTAs takes two tiles side by side in N: pair
+// p (ranks 2p, 2p + 1) computes tile column 2 * n_unit + p, and both pairs
+// use the same 256 rows of A. Each CTA loads 64 of its 128 A rows per slab
+// and multicasts them to the CTA with the same row half in the other pair, so
+// every A row is read from L2 once per cluster instead of once per pair. The
+// completion of a multicast pair load lands on the barrier of each destination
+// CTA's pair leader, so each leader still expects exactly the bytes its two
+// CTAs receive; a ring slot is free again only when both pairs' products have
+// read it (each pair's commit arrives on every CTA's empty barrier).
+template <int CG, int BN, int KS, int KIND, int MC = 1>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_b,
@@ -404,6 +414,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ CUtensorMap tmap_sfb, const KernelParams p)
 {
     using Cfg = TileConfig<CG, BN, KS, KIND>;
+    static_assert(MC == 1 || (MC == 2 && CG == 2 && !Cfg::SCALED), "A is shared by CTA pairs of plain products only");
+    constexpr int CS = CG * MC;   // CTAs per cluster
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_u32(smem_raw);
     if (base & 1023u) {
@@ -417,9 +429,12 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
 
     const uint32_t warp = threadIdx.x / 32u;
     const uint32_t lane = threadIdx.x % 32u;
-    const uint32_t rank = (CG == 2) ? cluster_cta_rank() : 0u;
-    const int cluster_id = static_cast<int>(blockIdx.x) / CG;
-    const int num_clusters = static_cast<int>(gridDim.x) / CG;
+    const uint32_t rank = (CS > 1) ? cluster_cta_rank() : 0u;
+    const uint32_t half = rank % CG;      // this CTA's 128-row half of the pair's tile
+    const uint32_t pair = rank / CG;      // the pair of the cluster (0 when MC = 1)
+    const uint32_t leader = rank - half;  // the pair's even CTA: its barriers count both CTAs' bytes
+    const int cluster_id = static_cast<int>(blockIdx.x) / CS;
+    const int num_clusters = static_cast<int>(gridDim.x) / CS;
 
     const uint32_t staging_off = stages * Cfg::STAGE_BYTES;
     const uint32_t bar_off = staging_off + 4u * p.staging_bufs * p.staging_bytes;
@@ -434,7 +449,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < stages; ++s) {
             mbar_init(full_bar(s), 1);    // producer's arrive.expect_tx (+ bytes of both CTAs)
-            mbar_init(empty_bar(s), 1);   // one tcgen05.commit
+            mbar_init(empty_bar(s), MC);  // one tcgen05.commit of every pair that reads or shares the slot
         }
         for (uint32_t b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);             // one tcgen05.commit
@@ -448,7 +463,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
         tmem_relinquish<CG>();
     }
     tc_fence_before_sync();
-    if constexpr (CG == 2)
+    if constexpr (CS > 1)
         cluster_sync();
     else
         __syncthreads();
@@ -486,8 +501,9 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const Job jb = sch.job(i);
                 int m_blk, n_blk;
                 tile_coords(p, jb.tile, m_blk, n_blk);
-                const int a_row = m_blk * (BLOCK_M_CTA * CG) + static_cast<int>(rank) * BLOCK_M_CTA;
-                const int b_off = n_blk * BN + static_cast<int>(rank) * Cfg::BN_CTA;
+                n_blk = n_blk * MC + static_cast<int>(pair);   // MC = 2: the pair's tile of the two
+                const int a_row = m_blk * (BLOCK_M_CTA * CG) + static_cast<int>(half) * BLOCK_M_CTA;
+                const int b_off = n_blk * BN + static_cast<int>(half) * Cfg::BN_CTA;
                 for (int kb = jb.kb0; kb < jb.kb1; ++kb) {
                     wait_bounded<CG == 2>(w, empty_bar(s), ph ^ 1u, SITE_PRODUCER_EMPTY);
                     if (!w.aborted && !(i == 0 && kb == withhold)) {
@@ -516,14 +532,22 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                                             sf_atom_row(n_blk, kb, p.num_k_blocks, Cfg::SF_GROUPS * Cfg::SFB_ATOMS));
                             }
                         } else {
-                            // both CTAs' boxes complete on the even CTA's full barrier
-                            const uint32_t bar = map_to_cta(full_bar(s), 0);
-                            if (rank == 0)
+                            // both CTAs' boxes complete on the pair leader's full barrier
+                            const uint32_t bar = map_to_cta(full_bar(s), leader);
+                            if (half == 0)
                                 mbar_arrive_expect_tx(full_bar(s), 2u * Cfg::STAGE_TX);
 #pragma unroll
                             for (int j = 0; j < KS; ++j) {
                                 const int kj = x0 + j * Cfg::SLAB_X;
-                                tma_load_2d_pair(a_dst + j * Cfg::A_SLAB, &tmap_a, bar, kj, a_row);
+                                if constexpr (MC == 1) {
+                                    tma_load_2d_pair(a_dst + j * Cfg::A_SLAB, &tmap_a, bar, kj, a_row);
+                                } else {
+                                    // this CTA's 64-row share of the half's A rows, into the same
+                                    // offset of both pairs' CTAs of this half (the A map's box is 64 rows)
+                                    const uint16_t mask = static_cast<uint16_t>((1u << half) | (1u << (half + CG)));
+                                    tma_load_2d_pair_mc(a_dst + j * Cfg::A_SLAB + pair * (Cfg::A_SLAB / 2), &tmap_a, bar,
+                                                        kj, a_row + static_cast<int>(pair) * (BLOCK_M_CTA / 2), mask);
+                                }
                                 const uint32_t bj = b_dst + j * Cfg::B_SLAB;
                                 if (KIND != KIND_F16 || !p.b_mn_major)
                                     tma_load_2d_pair(bj, &tmap_b, bar, kj, b_off);
@@ -550,8 +574,9 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 }
             }
             // Leave no bulk copy into shared memory in flight: wait for the last
-            // fill of every slot (the peer CTA's copies land on these barriers too).
-            if (CG == 1 || rank == 0)
+            // fill of every slot (the peer CTA's copies, and with MC = 2 the other
+            // pair's shares of A, land on these barriers too).
+            if (CG == 1 || half == 0)
                 for (uint32_t s2 = 0; s2 < stages; ++s2)
                     if ((pend_mask >> s2) & 1u)
                         wait_drain<CG == 2>(full_bar(s2), (pend_par >> s2) & 1u, w.limit_ns, w.id, w.status,
@@ -561,7 +586,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
         // ------------------------------------------------------------ MMA issuer
         // The whole warp walks the job list and waits; one elected lane issues
         // each product, copy and commit.
-        if (CG == 1 || rank == 0) {
+        if (CG == 1 || half == 0) {
             auto sync_abort = [&]() {
                 __syncwarp();
                 w.aborted = __any_sync(0xffffffffu, w.aborted);
@@ -632,7 +657,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         if constexpr (CG == 1)
                             mma_commit(empty_bar(s));
                         else
-                            mma_commit_pair(empty_bar(s), 0x3);
+                            mma_commit_pair(empty_bar(s), static_cast<uint16_t>((1u << CS) - 1u));   // every CTA of the cluster
                     }
                     if (++s == stages) {
                         s = 0;
@@ -643,7 +668,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     if constexpr (CG == 1)
                         mma_commit(tfull_bar(acc));
                     else
-                        mma_commit_pair(tfull_bar(acc), 0x3);
+                        mma_commit_pair(tfull_bar(acc), static_cast<uint16_t>(3u << leader));    // this pair
                 }
                 if (++acc == 2) {
                     acc = 0;
@@ -654,7 +679,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
             if constexpr (CG == 1)
                 mma_commit(done_bar);
             else
-                mma_commit_pair(done_bar, 0x1);
+                mma_commit_pair(done_bar, static_cast<uint16_t>(1u << leader));
             wait_drain<false>(done_bar, 0, w.limit_ns, w.id, w.status, SITE_MMA_DONE);
         }
     } else {
@@ -673,6 +698,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const Job jb = sch.job(i);
             int m_blk, n_blk;
             tile_coords(p, jb.tile, m_blk, n_blk);
+            n_blk = n_blk * MC + static_cast<int>(pair);
             wait_bounded<CG == 2>(w, tfull_bar(acc), acc_ph, SITE_EPI_TMEM_FULL);
             // An owner needs every writer's partial for its rows first. The
             // writers did their segments at the start of their work lists.
@@ -682,7 +708,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (lane == 0)
                     for (int v = cluster_id - 1; v >= w_first; --v)
                         if (sch.has_range(v) &&
-                            !wait_flag_bounded(w, &p.flags[(static_cast<size_t>(v) * CG + rank) * 4u + quarter],
+                            !wait_flag_bounded(w, &p.flags[(static_cast<size_t>(v) * CS + rank) * 4u + quarter],
                                                SITE_EPI_PARTIAL))
                             break;
                 w.aborted = __shfl_sync(0xffffffffu, w.aborted ? 1 : 0, 0) != 0;
@@ -691,7 +717,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const bool skip = __any_sync(0xffffffffu, w.aborted);   // warp-uniform
             w.aborted = skip;
             tc_fence_after_sync();
-            const int row0 = m_blk * (BLOCK_M_CTA * CG) + static_cast<int>(rank) * BLOCK_M_CTA +
+            const int row0 = m_blk * (BLOCK_M_CTA * CG) + static_cast<int>(half) * BLOCK_M_CTA +
                              static_cast<int>(quarter) * 32;
             const int col0 = n_blk * BN;
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + acc * ACC_STRIDE;
@@ -712,7 +738,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         if constexpr (CG == 1)
                             mbar_arrive_local(tempty_bar(acc));
                         else
-                            mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
+                            mbar_arrive_cluster(map_to_cta(tempty_bar(acc), leader));
                     }
                 }
                 const int gcol = col0 + c * EPI_COLS;
@@ -732,7 +758,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     for (int u = cluster_id - 1; u >= w_first; --u) {
                         if (!sch.has_range(u))
                             continue;
-                        const float4 *src = partial_chunk(u * CG + static_cast<int>(rank), c);
+                        const float4 *src = partial_chunk(u * CS + static_cast<int>(rank), c);
 #pragma unroll
                         for (int j4 = 0; j4 < 8; ++j4) {
                             const float4 x = __ldcg(src + 32 * j4);
@@ -782,7 +808,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (lane == 0)
                     for (int u = cluster_id - 1; u >= w_first; --u)
                         if (sch.has_range(u))
-                            p.flags[(static_cast<size_t>(u) * CG + rank) * 4u + quarter] = 0ull;
+                            p.flags[(static_cast<size_t>(u) * CS + rank) * 4u + quarter] = 0ull;
             }
             if (++acc == 2) {
                 acc = 0;
@@ -796,8 +822,8 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
     // ---------------------------------------------------------------- teardown
     __syncwarp();
     tc_fence_before_sync();
-    if constexpr (CG == 2)
-        cluster_sync();   // the peer no longer touches this CTA's barriers or TMEM
+    if constexpr (CS > 1)
+        cluster_sync();   // no other CTA of the cluster touches this CTA's barriers, ring or TMEM
     else
         __syncthreads();
     if (p.trace != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {

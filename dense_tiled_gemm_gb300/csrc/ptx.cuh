@@ -178,6 +178,19 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
                  : "memory");
 }
 
+// Paired-CTA multicast form: the box lands at the same shared-memory offset
+// in every CTA of `cta_mask`, and each destination's bytes complete on the
+// barrier at bar_cluster's offset in that destination's pair leader (the even
+// CTA of its pair), whichever CTA issued the copy.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar_cluster,
+                                                    int32_t c0, int32_t c1, uint16_t cta_mask)
+{
+    asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "h"(cta_mask)
+                 : "memory");
+}
+
 // 2-D tiled store of one box from this CTA's shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t c0,
                                              int32_t c1)

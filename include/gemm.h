@@ -181,7 +181,14 @@ gemm_status_t gemm_mx(const void *A, const void *B, const uint8_t *SFA, const ui
  *                 tile whole (data-parallel), 2 forces stream-K on the last
  *                 tiles (see gemm_schedule_jobs). Other values give
  *                 GEMM_ERR_INVALID_ARG (negative) or GEMM_ERR_UNSUPPORTED.
- *   reserved      must be 0.
+ *   cluster_pairs CTA pairs per thread-block cluster (cta_group 2 only):
+ *                 1 keeps each pair on its own; 2 clusters two pairs on
+ *                 tiles side by side in N, which share their A tiles: each
+ *                 CTA loads half of its A rows and multicasts them to the
+ *                 other pair, so A is read from L2 once per two tiles. Only
+ *                 the FP16/BF16 and FP8 products with 256-wide tiles offer
+ *                 it. Other values give GEMM_ERR_INVALID_ARG (negative) or
+ *                 GEMM_ERR_UNSUPPORTED.
  *   clock_trace   NULL, or a device pointer to 4 writable, 8-byte aligned
  *                 uint64 words. The launch's first CTA then writes the
  *                 global timer (ns) and its SM cycle counter as it starts
@@ -199,7 +206,7 @@ typedef struct {
     int32_t timeout_ms;
     int32_t k_stage;
     int32_t stream_k;
-    int32_t reserved;
+    int32_t cluster_pairs;
     uint64_t *clock_trace;
 } gemm_options_t;
 
@@ -237,9 +244,11 @@ typedef struct {
     int32_t direct_store;  /* 1 if C is written with ordinary stores */
     int32_t smem_bytes;    /* dynamic shared memory per CTA */
     int32_t num_sms;       /* multiprocessors on the current device */
-    int32_t sk_tiles;      /* trailing tiles split along K (stream-K); 0 = none */
+    int32_t sk_tiles;      /* leading scheduling units split along K (stream-K); 0 = none.
+                              A unit is one tile, or two side by side in N when
+                              cluster_pairs is 2 */
     int32_t workspace_bytes; /* stream-K partial sums and flags, taken per call */
-    int32_t reserved;
+    int32_t cluster_pairs;   /* CTA pairs per cluster sharing A (1 or 2) */
 } gemm_plan_t;
 
 /* Fill *plan for a problem on the current device. Same validation and

@@ -65,7 +65,7 @@ def test_struct_sizes():
     assert ctypes.sizeof(binding.GemmOptions) == 40
     assert binding.GemmOptions.clock_trace.offset == 32
     assert ctypes.sizeof(binding.GemmPlan) == 64
-    assert re.search(r"int32_t reserved;\s*uint64_t \*clock_trace;\s*\} gemm_options_t;", header_text())
+    assert re.search(r"int32_t cluster_pairs;\s*uint64_t \*clock_trace;\s*\} gemm_options_t;", header_text())
 
 
 def test_prototypes_use_the_enum_types():
@@ -138,7 +138,7 @@ def test_invalid_options_rejected_on_host():
     for field, val, expect in (("cta_group", 3, 1), ("cta_group", -1, 1), ("block_n", 128, 2),
                                ("max_clusters", -2, 1), ("group_m", -1, 1), ("timeout_ms", -1, 1),
                                ("k_stage", 96, 2), ("k_stage", -64, 1), ("stream_k", 3, 2),
-                               ("stream_k", -1, 1), ("reserved", 1, 1)):
+                               ("stream_k", -1, 1), ("cluster_pairs", -1, 1), ("cluster_pairs", 3, 2)):
         o = binding.GemmOptions()
         setattr(o, field, val)
         rc = binding.lib.gemm_ex(FAKE, FAKE, FAKE, 64, 64, 64, 0, 0, 0, 0, ctypes.byref(o), None)
