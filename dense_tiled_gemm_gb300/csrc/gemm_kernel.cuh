@@ -703,11 +703,23 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
             // An owner needs every writer's partial for its rows first. The
             // writers did their segments at the start of their work lists.
             int w_first = cluster_id;
+            // Which of the units cluster_id - 1, cluster_id - 2, ... (down to w_first)
+            // left a partial: worked out once per owner job (each test takes two
+            // 64-bit divisions), bit i for unit cluster_id - 1 - i; beyond 32 units
+            // back (tiny problems spread over many units) the test is redone per use.
+            uint32_t wmask = 0;
+            auto wrote = [&](int u) {
+                const int i = cluster_id - 1 - u;
+                return i < 32 ? ((wmask >> i) & 1u) != 0 : sch.has_range(u);
+            };
             if (jb.kind == JOB_OWNER && !w.aborted) {
                 w_first = sch.first_writer();
+                for (int i = 0; i < 32 && cluster_id - 1 - i >= w_first; ++i)
+                    if (sch.has_range(cluster_id - 1 - i))
+                        wmask |= 1u << i;
                 if (lane == 0)
                     for (int v = cluster_id - 1; v >= w_first; --v)
-                        if (sch.has_range(v) &&
+                        if (wrote(v) &&
                             !wait_flag_bounded(w, &p.flags[(static_cast<size_t>(v) * CS + rank) * 4u + quarter],
                                                SITE_EPI_PARTIAL))
                             break;
@@ -756,7 +768,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (jb.kind == JOB_OWNER) {
                     // add the writers' partial sums, nearest k-range first
                     for (int u = cluster_id - 1; u >= w_first; --u) {
-                        if (!sch.has_range(u))
+                        if (!wrote(u))
                             continue;
                         const float4 *src = partial_chunk(u * CS + static_cast<int>(rank), c);
 #pragma unroll
@@ -807,7 +819,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 __syncwarp();
                 if (lane == 0)
                     for (int u = cluster_id - 1; u >= w_first; --u)
-                        if (sch.has_range(u))
+                        if (wrote(u))
                             p.flags[(static_cast<size_t>(u) * CS + rank) * 4u + quarter] = 0ull;
             }
             if (++acc == 2) {
