@@ -34,6 +34,7 @@ static __device__ unsigned long long g_status[4];
 namespace {
 
 constexpr int MAX_DEVICES = 64;
+constexpr int STREAM_SCRATCH_ENTRIES = 8;
 constexpr uint64_t DEFAULT_TIMEOUT_MS = 2000;
 // K per ring stage, unless gemm_options_t.k_stage says otherwise: 128 for CTA
 // pairs (8 MMAs per barrier wait; the MMA issuer's wait costs ~60-100 cycles
@@ -129,6 +130,20 @@ struct DeviceState {
     } slots[2];
     unsigned next_slot = 0;
     cudaStream_t h2d = nullptr;
+    // Per-stream scratch for re-pitched operands, packed scales and stream-K
+    // partial sums. A call reuses its stream's buffer, which stream order makes
+    // safe, so no allocation (a stream operation that would stop the next
+    // kernel from launching early) sits between two calls' kernels. Entries are
+    // keyed by cudaStreamGetId, which no later stream reuses; a buffer grows
+    // only on its own stream. Nothing is evicted: calls on further streams take
+    // per-call scratch, and gemm_release_workspace frees every buffer.
+    std::mutex scratch_mu;
+    struct StreamScratch {
+        unsigned long long stream_id = 0;
+        bool used = false;
+        void *ptr = nullptr;
+        size_t bytes = 0;
+    } scratch[STREAM_SCRATCH_ENTRIES];
 };
 
 std::mutex g_mu;
@@ -618,20 +633,6 @@ gemm_status_t realign_into(const void *src, int64_t rows, int64_t cols, int64_t 
     return GEMM_OK;
 }
 
-// realign_into stream-ordered scratch taken with cudaMallocAsync.
-gemm_status_t realign(const void *src, int64_t rows, int64_t cols, int eb, int sms, cudaStream_t st,
-                      void **out, int64_t *ld_out)
-{
-    const int64_t ld = padded_pitch(cols, eb);
-    if (cudaMallocAsync(out, static_cast<size_t>(rows * ld * eb), st) != cudaSuccess) {
-        cudaGetLastError();
-        *out = nullptr;
-        return GEMM_ERR_OUT_OF_MEMORY;
-    }
-    *ld_out = ld;
-    return realign_into(src, rows, cols, ld, eb, sms, st, *out);
-}
-
 template <int CG, int BN, int KS, int KIND, int MC = 1>
 cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap *maps, const KernelParams &kp,
                            cudaStream_t st)
@@ -868,6 +869,71 @@ gemm_status_t pack_scales(const uint8_t *sf, int64_t rows, int64_t K, const SfGe
     return GEMM_OK;
 }
 
+// Scratch of `need` bytes for one call on `st`: the stream's cached buffer
+// (grown, when too small, by a stream-ordered free and allocation on `st`), or,
+// inside a stream capture or beyond STREAM_SCRATCH_ENTRIES streams, a
+// stream-ordered allocation that the caller frees after its launch
+// (*per_call = true; in a capture it becomes the graph's own memory).
+gemm_status_t acquire_scratch(DeviceState &d, cudaStream_t st, size_t need, void **out, bool *per_call)
+{
+    *out = nullptr;
+    *per_call = false;
+    if (need == 0)
+        return GEMM_OK;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    unsigned long long id = 0;
+    const bool cacheable = cudaStreamIsCapturing(st, &cap) == cudaSuccess && cap == cudaStreamCaptureStatusNone &&
+                           cudaStreamGetId(st, &id) == cudaSuccess;
+    if (!cacheable)
+        cudaGetLastError();
+    if (cacheable) {
+        std::lock_guard<std::mutex> lock(d.scratch_mu);
+        DeviceState::StreamScratch *e = nullptr, *empty = nullptr;
+        for (DeviceState::StreamScratch &x : d.scratch) {
+            if (x.used && x.stream_id == id) {
+                e = &x;
+                break;
+            }
+            if (!x.used && !empty)
+                empty = &x;
+        }
+        if (!e && empty) {
+            e = empty;
+            e->used = true;
+            e->stream_id = id;
+            e->ptr = nullptr;
+            e->bytes = 0;
+        }
+        if (e) {
+            if (e->bytes < need) {
+                // grow by at least a quarter, in 2 MiB steps
+                const size_t step = size_t(2) << 20;
+                const size_t want = std::max(need, e->bytes + e->bytes / 4);
+                const size_t bytes = (want + step - 1) / step * step;
+                if (e->ptr)
+                    cudaFreeAsync(e->ptr, st);   // after every earlier call on this stream
+                e->ptr = nullptr;
+                e->bytes = 0;
+                if (cudaMallocAsync(&e->ptr, bytes, st) != cudaSuccess) {
+                    cudaGetLastError();
+                    e->ptr = nullptr;
+                    return GEMM_ERR_OUT_OF_MEMORY;
+                }
+                e->bytes = bytes;
+            }
+            *out = e->ptr;
+            return GEMM_OK;
+        }
+    }
+    if (cudaMallocAsync(out, need, st) != cudaSuccess) {
+        cudaGetLastError();
+        *out = nullptr;
+        return GEMM_ERR_OUT_OF_MEMORY;
+    }
+    *per_call = true;
+    return GEMM_OK;
+}
+
 gemm_status_t run(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C, int64_t M,
                   int64_t N, int64_t K, int dtype_in, int dtype_out, int layoutA, int layoutB,
                   const gemm_options_t *opts, cudaStream_t st, int32_t withhold_kb = -1)
@@ -894,42 +960,55 @@ gemm_status_t run(const void *A, const void *B, const uint8_t *SFA, const uint8_
     const int64_t a_width = row_bytes(var.kind, K) / eb;
     const int64_t b_rows = b_mn ? K : N, b_width = b_mn ? N : a_width;
 
-    Operand a{A, a_width}, b{B, b_width};
-    void *a_tmp = nullptr, *b_tmp = nullptr, *ws = nullptr, *sf_tmp = nullptr;
+    // One scratch area per call: stream-K partial sums and flags, then the
+    // re-pitched A and B, then the packed scales, each on a 256-byte boundary.
+    auto up256 = [](size_t v) { return (v + 255) / 256 * 256; };
+    const int64_t lda_pad = padded_pitch(a_width, eb), ldb_pad = padded_pitch(b_width, eb);
+    const size_t a_off = up256(pl.ws_bytes);
+    const size_t a_bytes = pl.realign_a ? static_cast<size_t>(M) * lda_pad * eb : 0;
+    const size_t b_off = a_off + up256(a_bytes);
+    const size_t b_bytes = pl.realign_b ? static_cast<size_t>(b_rows) * ldb_pad * eb : 0;
+    const size_t sf_off = b_off + up256(b_bytes);
+    SfGeometry ga{}, gb{};
+    size_t sfa_bytes = 0, sfb_off = 0, sf_bytes = 0;
+    if (scaled) {
+        ga = sf_geometry(var, pl, M, false);
+        gb = sf_geometry(var, pl, N, true);
+        sfa_bytes = static_cast<size_t>(ga.bytes());
+        sfb_off = up256(sfa_bytes);
+        sf_bytes = sfb_off + static_cast<size_t>(gb.bytes());
+    }
+    const size_t need = scaled ? sf_off + sf_bytes : (b_bytes ? b_off + b_bytes : (a_bytes ? a_off + a_bytes : pl.ws_bytes));
+    void *scratch = nullptr;
+    bool per_call = false;
+    if ((rc = acquire_scratch(*d, st, need, &scratch, &per_call)) != GEMM_OK)
+        return rc;
+    char *base = static_cast<char *>(scratch);
     auto release = [&]() {
-        for (void *q : {a_tmp, b_tmp, ws, sf_tmp})
-            if (q)
-                cudaFreeAsync(q, st);
+        if (per_call)
+            cudaFreeAsync(scratch, st);
     };
-    if (pl.ws_bytes && cudaMallocAsync(&ws, pl.ws_bytes, st) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_OUT_OF_MEMORY;
+
+    Operand a{A, a_width}, b{B, b_width};
+    void *ws = pl.ws_bytes ? base : nullptr;
+    if (pl.realign_a) {
+        if ((rc = realign_into(A, M, a_width, lda_pad, eb, d->sms, st, base + a_off)) != GEMM_OK) {
+            release();
+            return rc;
+        }
+        a = {base + a_off, lda_pad};
     }
-    if (pl.realign_a && (rc = realign(A, M, a_width, eb, d->sms, st, &a_tmp, &a.ld)) != GEMM_OK) {
-        release();
-        return rc;
+    if (pl.realign_b) {
+        if ((rc = realign_into(B, b_rows, b_width, ldb_pad, eb, d->sms, st, base + b_off)) != GEMM_OK) {
+            release();
+            return rc;
+        }
+        b = {base + b_off, ldb_pad};
     }
-    if (a_tmp)
-        a.ptr = a_tmp;
-    if (pl.realign_b && (rc = realign(B, b_rows, b_width, eb, d->sms, st, &b_tmp, &b.ld)) != GEMM_OK) {
-        release();
-        return rc;
-    }
-    if (b_tmp)
-        b.ptr = b_tmp;
     const void *sfa = nullptr, *sfb = nullptr;
     if (scaled) {
-        const SfGeometry ga = sf_geometry(var, pl, M, false), gb = sf_geometry(var, pl, N, true);
-        const size_t a_bytes = static_cast<size_t>(ga.bytes()), b_bytes = static_cast<size_t>(gb.bytes());
-        const size_t b_off = (a_bytes + 255) / 256 * 256;
-        if (cudaMallocAsync(&sf_tmp, b_off + b_bytes, st) != cudaSuccess) {
-            cudaGetLastError();
-            sf_tmp = nullptr;
-            release();
-            return GEMM_ERR_OUT_OF_MEMORY;
-        }
-        sfa = sf_tmp;
-        sfb = static_cast<char *>(sf_tmp) + b_off;
+        sfa = base + sf_off;
+        sfb = base + sf_off + sfb_off;
         if ((rc = pack_scales(SFA, M, K, ga, d->sms, st, const_cast<void *>(sfa))) != GEMM_OK ||
             (rc = pack_scales(SFB, N, K, gb, d->sms, st, const_cast<void *>(sfb))) != GEMM_OK) {
             release();
@@ -1147,6 +1226,16 @@ gemm_status_t gemm_release_workspace(void)
         slot.ws = nullptr;
         slot.bytes = 0;
         slot.used = false;
+    }
+    {
+        std::lock_guard<std::mutex> slock(d->scratch_mu);
+        for (DeviceState::StreamScratch &e : d->scratch) {
+            if (e.ptr && cudaFree(e.ptr) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+            e = DeviceState::StreamScratch{};
+        }
     }
     g_cache[d->dev].clear();
     return GEMM_OK;

@@ -93,19 +93,28 @@ typedef enum {
  * planner may split the last tiles along K (stream-K): each unit then gets an
  * equal share of their k-blocks, and the units that end a split tile add the
  * FP32 partial sums of the others before the cast. The partial sums and their
- * flags live in a per-call workspace (plan->workspace_bytes) taken with
- * cudaMallocAsync and freed with cudaFreeAsync on the same stream. For a
+ * flags (plan->workspace_bytes) live in the library's scratch (below). For a
  * given device and problem the split points are fixed, so results are
  * reproducible from run to run. The split tiles are run first, so that the
  * whole tiles after them proceed in step across the machine.
  *
  * Alignment: the tensor-memory-access engine needs 16-byte-aligned bases and
  * row pitches. When A or B misses this (for example K*2 bytes, or K bytes for
- * FP8, not a multiple of 16), the call first copies that operand into a padded, stream-ordered
- * scratch buffer. It takes this buffer with cudaMallocAsync and frees it with
- * cudaFreeAsync on the same stream. When C misses it, the epilogue writes C
- * with ordinary stores instead of bulk tensor stores. Results do not depend
- * on either path.
+ * FP8, not a multiple of 16), the call first copies that operand into the
+ * library's scratch with rows padded to a multiple of 128 bytes. When C
+ * misses it, the epilogue writes C with ordinary stores instead of bulk
+ * tensor stores. Results do not depend on either path.
+ *
+ * Scratch: the library keeps, per device, one scratch buffer for each of up
+ * to 8 streams (told apart by cudaStreamGetId), for stream-K partial sums,
+ * re-pitched operands and repacked MX scales. A call reuses its stream's
+ * buffer, which stream order makes safe, so consecutive calls on a stream
+ * put no allocation between their kernels; a buffer that is too small is
+ * replaced by cudaFreeAsync and cudaMallocAsync on its own stream. Calls on
+ * further streams, and calls made during a stream capture (whose graph then
+ * owns the memory), take stream-ordered scratch per call (cudaMallocAsync /
+ * cudaFreeAsync on the call's stream). gemm_release_workspace frees the
+ * buffers.
  *
  * Per-call host work: the library keeps, per device, the plans and the TMA
  * tensor maps of its most recent launches (GEMM_LAUNCH_CACHE_ENTRIES of
@@ -149,10 +158,10 @@ gemm_status_t gemm(const void *A, const void *B, void *C,
  *   C, M, N, K, dtype_out, layoutA, stream: as for gemm.
  *
  * The call first repacks the scales into the kernel's per-stage layout, in
- * stream-ordered scratch (cudaMallocAsync / cudaFreeAsync on `stream`,
- * (M + N) x ceil(K / stage K) x 16 bytes), and re-pitches A or B like gemm
- * when their row pitch is not a multiple of 16 bytes. Tiles are 256 x 224,
- * computed by CTA pairs. Errors as for gemm.
+ * the library's scratch (as for gemm; (M + N) x ceil(K / stage K) x 16
+ * bytes), and re-pitches A or B like gemm when their row pitch is not a
+ * multiple of 16 bytes. Tiles are 256 x 224, computed by CTA pairs. Errors as
+ * for gemm.
  */
 gemm_status_t gemm_mx(const void *A, const void *B, const uint8_t *SFA, const uint8_t *SFB, void *C,
                       int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype_in, gemm_dtype_t dtype_out,
@@ -301,8 +310,9 @@ gemm_status_t gemm_from_host_async(const void *A_host, const void *B_host, void 
                                    gemm_layout_t layoutA, gemm_layout_t layoutB,
                                    void *stream);
 
-/* Free the gemm_from_host staging slots of the current device and empty its
- * launch cache. Synchronises the device first. */
+/* Free the gemm_from_host staging slots and the per-stream scratch buffers of
+ * the current device and empty its launch cache. Synchronises the device
+ * first. */
 gemm_status_t gemm_release_workspace(void);
 
 /* Launch-cache counters of this process, over all devices: plan lookups that
@@ -362,17 +372,19 @@ gemm_status_t gemm_selftest_withheld_load(const void *A, const void *B, void *C,
  * The pages have no counterpart to this entry point; it exists for callers
  * such as a serving runtime that has already handed all of the GPU's memory
  * to its own pool, or a latency-critical loop in which a cudaMalloc or
- * cudaFree could synchronise the device or fail. gemm itself calls
- * cudaMallocAsync/cudaFreeAsync whenever A or B must be re-pitched (a base
- * or row pitch that is not a multiple of 16 bytes, for example K*2 bytes
- * not a multiple of 16) and whenever its plan splits tiles along K (the
- * stream-K partial sums and flags). gemm_no_alloc takes the same arguments
+ * cudaFree could synchronise the device or fail. gemm itself needs scratch
+ * whenever A or B must be re-pitched (a base or row pitch that is not a
+ * multiple of 16 bytes, for example K*2 bytes not a multiple of 16) and
+ * whenever its plan splits tiles along K (the stream-K partial sums and
+ * flags), and takes it with cudaMallocAsync/cudaFreeAsync: on a stream's
+ * first such call, when that stream's buffer must grow, and per call on
+ * streams beyond its cache or during a capture. gemm_no_alloc takes the same arguments
  * and computes the same result, but it never allocates or frees: the
  * re-pitched copies and the stream-K workspace go into one fixed device
  * array that the library holds on every GPU that loads it,
  * GEMM_NO_ALLOC_SCRATCH_BYTES (32 MiB) in size, until the process exits.
  *
- *   - Limit: the padded copies (rows x row bytes rounded up to 16, A then B,
+ *   - Limit: the padded copies (rows x row bytes rounded up to 128, A then B,
  *     each started on a 256-byte boundary) must fit in
  *     GEMM_NO_ALLOC_SCRATCH_BYTES. Otherwise the call returns
  *     GEMM_ERR_UNSUPPORTED and launches nothing. When no operand needs

@@ -191,3 +191,50 @@ def test_repitch_copy_every_word_width(dtg, offset, K, dtype_in, width):
     got = C.cpu().numpy().astype(np.float64)
     bad = np.argwhere(got != C_ref)
     assert bad.size == 0, f"{len(bad)} inexact elements, first {tuple(bad[0])}"
+
+
+def _exact_inputs(M, N, K, seed):
+    A, B = workloads.make_operands(M, N, K, "f16", "k", ("int", -3, 3), seed)
+    C_ref, _ = oracle.gemm_ref(workloads.as_bits(A), workloads.as_bits(B), M, N, K, "f16", "k")
+    return A.cuda(), B.cuda(), C_ref
+
+
+def test_stream_scratch_many_streams(dtg):
+    """Re-pitched operands and stream-K partial sums on ten streams at once: eight
+    streams keep a scratch buffer of their own, the other two take per-call scratch.
+    Three calls per stream are queued before anything is waited for; every result
+    is exact, and again after the buffers are released."""
+    M, N, K = 640, 896, 1090          # K * 2 bytes not a multiple of 16: A and B re-pitched
+    cases = [_exact_inputs(M, N, K, 200 + i) for i in range(10)]
+    streams = [torch.cuda.Stream() for _ in range(10)]
+    for rnd in range(2):
+        outs = []
+        for rep in range(3):
+            for (A, B, _), st in zip(cases, streams):
+                with torch.cuda.stream(st):
+                    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+                    dtg.gemm(A, B, C, stream=st, options={"stream_k": 2})
+                    outs.append(C)
+        torch.cuda.synchronize()
+        for j, C in enumerate(outs):
+            ref = cases[j % 10][2]
+            assert np.array_equal(C.cpu().numpy().astype(np.float64), ref), (rnd, j)
+        assert dtg.gemm_last_device_status() == (dtg.GEMM_OK, 0)
+        dtg.gemm_release_workspace()
+
+
+def test_stream_scratch_grows(dtg):
+    """One stream: a small re-pitched call, a larger one (its scratch buffer grows,
+    the old one freed in stream order behind the first call), and the small one
+    again, queued back to back; all exact."""
+    st = torch.cuda.Stream()
+    small = _exact_inputs(300, 333, 258, 210)
+    large = _exact_inputs(2000, 3000, 1026, 211)
+    outs = []
+    with torch.cuda.stream(st):
+        for (A, B, ref), opts in ((small, {"stream_k": 2}), (large, {"stream_k": 2}), (small, None)):
+            outs.append((dtg.gemm(A, B, out_dtype=torch.float32, stream=st, options=opts), ref))
+    torch.cuda.synchronize()
+    for C, ref in outs:
+        assert np.array_equal(C.cpu().numpy().astype(np.float64), ref)
+    assert dtg.gemm_last_device_status() == (dtg.GEMM_OK, 0)
