@@ -229,25 +229,45 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
-def kernel_clock_mhz(trace: torch.Tensor):
-    """SM clock of each traced launch from its clock_trace words (global timer ns and
-    SM cycles of CTA 0 at its start and end): cycles / ns * 1000, in MHz."""
+# %globaltimer advances in steps, not every nanosecond: a launch of a few
+# microseconds can read a quarter above the maximum clock from one interval.
+# Below this median launch length the clock is pooled over all launches.
+SHORT_LAUNCH_NS = 20000
+
+
+def kernel_clock_mhz(trace: torch.Tensor) -> dict:
+    """SM clock of the traced launches from their clock_trace words (global timer ns
+    and SM cycles of CTA 0 at its start and end), in MHz: per launch (cycles / ns), and
+    pooled over all launches (all cycles / all ns), which averages out the timer's steps."""
     t = trace.cpu().tolist()
-    mhz = [(c1 - c0) / (n1 - n0) * 1e3 for n0, c0, n1, c1 in t if n1 > n0 and c1 > c0]
-    return mhz
+    spans = [(n1 - n0, c1 - c0) for n0, c0, n1, c1 in t if n1 > n0 and c1 > c0]
+    if not spans:
+        return {"per_launch": [], "pooled": None, "median_ns": None}
+    return {"per_launch": [c / n * 1e3 for n, c in spans],
+            "pooled": sum(c for _, c in spans) / sum(n for n, _ in spans) * 1e3,
+            "median_ns": statistics.median(n for n, _ in spans)}
 
 
-def merge_clocks(smi: dict | None, mhz: list) -> dict | None:
-    """The line's clock record: the in-kernel SM clock (median over the timed launches)
-    where the launches were traced, nvidia-smi's samples under load otherwise; throttle
-    reasons and the maximum clock always come from nvidia-smi."""
+def merge_clocks(smi: dict | None, kc: dict | None) -> dict | None:
+    """The line's clock record: the in-kernel SM clock where the launches were traced
+    (the median over the timed launches, or for launches shorter than SHORT_LAUNCH_NS
+    the pooled clock), nvidia-smi's samples under load otherwise; throttle reasons and
+    the maximum clock always come from nvidia-smi."""
     out = dict(smi) if smi else {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
                                  "samples_under_load": 0, "power_w_max": None}
     out["smi_sm_mhz_under_load"] = out.get("sm_mhz")
+    mhz = kc["per_launch"] if kc else []
     if mhz:
-        out["sm_mhz"] = statistics.median(mhz)
-        out["sm_mhz_source"] = (f"in-kernel: SM cycles over global-timer ns of CTA 0, median of {len(mhz)} "
-                                "timed launches")
+        n = len(mhz)
+        if kc["median_ns"] < SHORT_LAUNCH_NS:
+            out["sm_mhz"] = kc["pooled"]
+            out["sm_mhz_source"] = (f"in-kernel: SM cycles over global-timer ns of CTA 0, pooled over {n} "
+                                    f"timed launches (median launch {kc['median_ns'] / 1e3:.1f} us, too short "
+                                    "for the timer's steps)")
+        else:
+            out["sm_mhz"] = statistics.median(mhz)
+            out["sm_mhz_source"] = (f"in-kernel: SM cycles over global-timer ns of CTA 0, median of {n} "
+                                    "timed launches")
         out["kernel_mhz_min"] = min(mhz)
         out["kernel_mhz_max"] = max(mhz)
     else:
@@ -643,7 +663,7 @@ def run_attention(args):
     torch.cuda.synchronize(dev)
     launches = dtg.gemm_launch_count() - launches0
     clocks = sampler.stop()
-    clocks = merge_clocks(clocks, [])
+    clocks = merge_clocks(clocks, None)
     status, detail = dtg.gemm_last_device_status(stream)
     if status != dtg.GEMM_OK:
         raise RuntimeError(f"device status {dtg.gemm_status_string(status)} site {detail:#x}")

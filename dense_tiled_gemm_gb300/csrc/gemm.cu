@@ -49,6 +49,11 @@ int default_k_slabs(int cg, int kind)
     return kind_scaled(kind) ? 1 : cg == 2 ? 2 : 1;
 }
 
+template <int CG, int BN, int KS, int KIND, int MC>
+cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap *maps, const KernelParams &kp,
+                           cudaStream_t st);
+using LaunchFn = cudaError_t (*)(int, uint32_t, const CUtensorMap *, const KernelParams &, cudaStream_t);
+
 struct Variant {
     int cg;
     int mc;            // CTA pairs per cluster sharing A tiles (1 or 2)
@@ -57,6 +62,7 @@ struct Variant {
     int kind;          // KIND_F16, KIND_F8, KIND_MXF8 or KIND_MXF4
     int stage_bytes;   // one ring slot: A and B tiles (and scales) of one stage, per CTA
     const void *fn;
+    LaunchFn launch;   // launch_variant of the same template arguments
     bool b_mn_ok;      // MN-major B needs 64-column TMA boxes per CTA (16-bit only)
 };
 
@@ -64,7 +70,8 @@ template <int CG, int BN, int KS, int KIND, int MC = 1>
 constexpr Variant variant(bool b_mn_ok)
 {
     return {CG, MC, BN, KS, KIND, TileConfig<CG, BN, KS, KIND>::STAGE_BYTES,
-            reinterpret_cast<const void *>(&gemm_tcgen05_kernel<CG, BN, KS, KIND, MC>), b_mn_ok};
+            reinterpret_cast<const void *>(&gemm_tcgen05_kernel<CG, BN, KS, KIND, MC>),
+            &launch_variant<CG, BN, KS, KIND, MC>, b_mn_ok};
 }
 
 const Variant kVariants[] = {
@@ -74,6 +81,9 @@ const Variant kVariants[] = {
     variant<2, 256, 2, KIND_F8>(false),  variant<2, 224, 2, KIND_F8>(false),  variant<1, 256, 2, KIND_F8>(false),
     variant<2, 224, 1, KIND_MXF8>(false), variant<2, 224, 2, KIND_MXF8>(false),
     variant<2, 224, 1, KIND_MXF4>(false), variant<2, 224, 2, KIND_MXF4>(false),
+    // narrow single-CTA tiles: more units for problems of few tiles
+    variant<1, 128, 1, KIND_F16>(true), variant<1, 64, 1, KIND_F16>(true),
+    variant<1, 128, 1, KIND_F8>(false), variant<1, 64, 1, KIND_F8>(false),
     // two pairs per cluster sharing A (gemm_options_t.cluster_pairs = 2)
     variant<2, 256, 1, KIND_F16, 2>(true), variant<2, 256, 2, KIND_F16, 2>(true),
     variant<2, 256, 1, KIND_F8, 2>(false), variant<2, 256, 2, KIND_F8, 2>(false),
@@ -300,7 +310,7 @@ gemm_status_t validate(const void *A, const void *B, const void *C, int64_t M, i
         if (o->cta_group < 0 || o->cta_group > 2 || o->max_clusters < 0 || o->group_m < 0 ||
             o->timeout_ms < 0 || o->block_n < 0)
             return GEMM_ERR_INVALID_ARG;
-        if (o->block_n != 0 && o->block_n != 224 && o->block_n != 256)
+        if (o->block_n != 0 && o->block_n != 64 && o->block_n != 128 && o->block_n != 224 && o->block_n != 256)
             return GEMM_ERR_UNSUPPORTED;
         if (o->k_stage < 0 || o->stream_k < 0 || o->cluster_pairs < 0)
             return GEMM_ERR_INVALID_ARG;
@@ -406,25 +416,43 @@ size_t sk_workspace_bytes(int grid_ctas, int bn)
 // tiles when there are fewer than two waves.
 int sk_tiles_for(int64_t T, int64_t U) { return static_cast<int>(T < 2 * U ? T : U + T % U); }
 
-// Relative time of a plan, in whole-tile times of a block_n-wide tile:
-// data-parallel waves, or DP waves + an equal stream-K share + the owner's
-// reads of partial sums. A partial slot of 128 x block_n FP32 read from L2 at
-// ~100 GB/s per SM takes about 600 / (K bytes) of a tile's MMA time.
+// Predicted time of a plan in microseconds, fitted to CUDA-graph timings of
+// every variant (128 x 64 to 256 x 256 tiles, each with and without stream-K)
+// on 15 shapes from 512^3 to 2560^3 with K up to 16384, at ~1.9 GHz:
+//  - one tile on one SM costs the larger of its products at 80% of the tensor
+//    rate (block_n x K bytes / 64 cycles) and its operand bytes,
+//    (128 / mc + block_n / cg) rows x K bytes, at ~55 bytes per SM cycle from
+//    L2: narrow tiles are bound by L2, not by the tensor core;
+//  - a launch pays ~2.6 us (ring fill, teardown) plus its last tile's
+//    epilogue, ~0.01 us per column, which nothing overlaps;
+//  - a stream-K owner adds its writers' partial sums, ~1.5 us plus ~1 us per
+//    writer and 32-column chunk. With one writer and data-parallel tiles after
+//    it, the next tile's main loop hides up to one tile time of that; otherwise
+//    (fewer tiles than two waves) the whole fix-up adds to the launch.
 struct Cost {
     double dp, sk;
     int sk_tiles;
 };
 
-Cost plan_cost(int64_t T, int64_t U, int64_t KB, int64_t k_bytes)
+Cost plan_cost(int64_t T, int64_t U, int64_t KB, int64_t k_bytes, int cg, int bn, int mc)
 {
+    constexpr double kMmaEff = 0.8, kL2BytesPerCycle = 55.0, kCyclesPerUs = 1900.0;
+    constexpr double kLaunchUs = 2.6, kEpilogueUsPerCol = 0.01, kFixUs = 1.5, kFixChunkUs = 1.0;
+    const double kb = static_cast<double>(k_bytes);
+    const double mma = bn * kb / 64.0 / kMmaEff;
+    const double l2 = (128.0 / mc + static_cast<double>(bn) / cg) * kb / kL2BytesPerCycle;
+    const double tile = std::max(mma, l2) / kCyclesPerUs;
+    const double fixed = kLaunchUs + kEpilogueUsPerCol * bn;
     Cost c;
-    c.dp = static_cast<double>((T + U - 1) / U);
+    c.dp = static_cast<double>((T + U - 1) / U) * tile + fixed;
     const int64_t S = sk_tiles_for(T, U);
     c.sk_tiles = static_cast<int>(S);
-    const int64_t L = (S * KB + U - 1) / U;                    // k-blocks per unit
-    const int64_t writers = L >= KB ? 1 : (KB + L - 1) / L;    // other units per split tile
-    const double F = 600.0 / static_cast<double>(k_bytes);
-    c.sk = static_cast<double>((T - S) / U) + static_cast<double>(L) / KB + writers * F;
+    const int64_t L = (S * KB + U - 1) / U;                        // k-blocks per unit
+    const int64_t writers = L >= KB ? 1 : (KB + L - 1) / L - 1;    // per split tile
+    const double fix = kFixUs + static_cast<double>(writers * (bn / 32)) * kFixChunkUs;
+    const int64_t dp_after = (T - S) / U;                          // whole tiles after the owner's
+    c.sk = (static_cast<double>(dp_after) + static_cast<double>(L) / static_cast<double>(KB)) * tile + fixed +
+           (dp_after >= 1 && writers == 1 ? std::max(0.0, fix - tile) : fix);
     return c;
 }
 
@@ -433,9 +461,8 @@ bool misaligned(const void *p, int64_t row_elems, int elem_bytes)
     return (reinterpret_cast<uintptr_t>(p) % 16) != 0 || (row_elems * elem_bytes) % 16 != 0;
 }
 
-// Choose the tile shape with the fewest output columns per SM over the whole
-// problem: waves = ceil(tiles / co-resident units), cost = waves x block_n.
-// Single-CTA tiles pay ~15% for their higher shared-memory read rate per flop.
+// Choose the variant (tile shape, CTA group) and schedule (data-parallel or
+// stream-K) of least predicted time (plan_cost).
 gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, int dtype_in,
                         int dtype_out, int layoutB, const void *A, const void *B, const void *C,
                         const gemm_options_t *o, Plan *pl, bool scaled = false)
@@ -472,11 +499,10 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
         const int64_t n_units = ((N + var.bn - 1) / var.bn + var.mc - 1) / var.mc;
         const int64_t tiles = ((M + 128 * var.cg - 1) / (128 * var.cg)) * n_units;
         const int64_t kb = (K + static_cast<int64_t>(sk_elems) * var.ks - 1) / (static_cast<int64_t>(sk_elems) * var.ks);
-        const Cost c = plan_cost(tiles, units, kb, k_bytes);
-        const double scale = var.bn * (var.cg == 1 ? 1.15 : 1.0);
+        const Cost c = plan_cost(tiles, units, kb, k_bytes, var.cg, var.bn, var.mc);
         // stream-K only where it saves more than 3%, or when asked for
         const bool sk = mode == 2 || (mode == 0 && tiles % units != 0 && c.sk < 0.97 * c.dp);
-        const double cost = (sk ? c.sk : c.dp) * scale;
+        const double cost = sk ? c.sk : c.dp;
         if (best < 0 || cost < best_cost) {
             best = v;
             best_cost = cost;
@@ -633,7 +659,7 @@ gemm_status_t realign_into(const void *src, int64_t rows, int64_t cols, int64_t 
     return GEMM_OK;
 }
 
-template <int CG, int BN, int KS, int KIND, int MC = 1>
+template <int CG, int BN, int KS, int KIND, int MC>
 cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap *maps, const KernelParams &kp,
                            cudaStream_t st)
 {
@@ -664,31 +690,7 @@ cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap *maps
 cudaError_t launch_any(const Variant &v, int grid_ctas, uint32_t smem, const CUtensorMap *maps,
                        const KernelParams &kp, cudaStream_t st)
 {
-#define DTG_LAUNCH(CG, BN, KS, KIND, MC)                                                           \
-    if (v.cg == CG && v.bn == BN && v.ks == KS && v.kind == KIND && v.mc == MC)                    \
-        return launch_variant<CG, BN, KS, KIND, MC>(grid_ctas, smem, maps, kp, st);
-    DTG_LAUNCH(2, 256, 1, KIND_F16, 1)
-    DTG_LAUNCH(2, 224, 1, KIND_F16, 1)
-    DTG_LAUNCH(1, 256, 1, KIND_F16, 1)
-    DTG_LAUNCH(2, 256, 2, KIND_F16, 1)
-    DTG_LAUNCH(2, 224, 2, KIND_F16, 1)
-    DTG_LAUNCH(1, 256, 2, KIND_F16, 1)
-    DTG_LAUNCH(2, 256, 1, KIND_F8, 1)
-    DTG_LAUNCH(2, 224, 1, KIND_F8, 1)
-    DTG_LAUNCH(1, 256, 1, KIND_F8, 1)
-    DTG_LAUNCH(2, 256, 2, KIND_F8, 1)
-    DTG_LAUNCH(2, 224, 2, KIND_F8, 1)
-    DTG_LAUNCH(1, 256, 2, KIND_F8, 1)
-    DTG_LAUNCH(2, 224, 1, KIND_MXF8, 1)
-    DTG_LAUNCH(2, 224, 2, KIND_MXF8, 1)
-    DTG_LAUNCH(2, 224, 1, KIND_MXF4, 1)
-    DTG_LAUNCH(2, 224, 2, KIND_MXF4, 1)
-    DTG_LAUNCH(2, 256, 1, KIND_F16, 2)
-    DTG_LAUNCH(2, 256, 2, KIND_F16, 2)
-    DTG_LAUNCH(2, 256, 1, KIND_F8, 2)
-    DTG_LAUNCH(2, 256, 2, KIND_F8, 2)
-#undef DTG_LAUNCH
-    return cudaErrorInvalidValue;
+    return v.launch(grid_ctas, smem, maps, kp, st);
 }
 
 // Packed-scale geometry of one operand: row blocks of R rows (128 for A, the

@@ -173,8 +173,11 @@ gemm_status_t gemm_mx(const void *A, const void *B, const uint8_t *SFA, const ui
  *   cta_group     1: each output tile is 128 x block_n and one CTA owns it.
  *                 2: tiles are 256 x block_n, and a cluster of two CTAs
  *                 shares each one (paired tensor-core issue).
- *   block_n       the tile width: 256 or 224 for cta_group 2, 256 for
- *                 cta_group 1. 224 is valid only for a K-major B.
+ *   block_n       the tile width: 256 or 224 for cta_group 2; 256, 128 or 64
+ *                 for cta_group 1 (128 and 64 for the FP16/BF16 and FP8
+ *                 products only). 224 is valid only for a K-major B. A width
+ *                 no variant offers for the other settings gives
+ *                 GEMM_ERR_UNSUPPORTED.
  *   max_clusters  upper bound on the persistent grid, counted in CTAs
  *                 (cta_group 1) or in pairs (cta_group 2). A small value
  *                 makes each CTA loop over many tiles.

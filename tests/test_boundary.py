@@ -135,7 +135,7 @@ def test_other_entry_points_validate_on_host(fn, kwargs, expect):
 
 
 def test_invalid_options_rejected_on_host():
-    for field, val, expect in (("cta_group", 3, 1), ("cta_group", -1, 1), ("block_n", 128, 2),
+    for field, val, expect in (("cta_group", 3, 1), ("cta_group", -1, 1), ("block_n", 96, 2),
                                ("max_clusters", -2, 1), ("group_m", -1, 1), ("timeout_ms", -1, 1),
                                ("k_stage", 96, 2), ("k_stage", -64, 1), ("stream_k", 3, 2),
                                ("stream_k", -1, 1), ("cluster_pairs", -1, 1), ("cluster_pairs", 3, 2)):

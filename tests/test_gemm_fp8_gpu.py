@@ -122,6 +122,15 @@ def test_output_types(dtg, dtype_out, dtype_in, opts):
     case(dtg, 384, 640, 640, dtype_in, dtype_out, ("normal", 1.0), 5, options=opts)
 
 
+@pytest.mark.parametrize("dtype_in", FP8)
+@pytest.mark.parametrize("opts", [{"cta_group": 1, "block_n": 128}, {"cta_group": 1, "block_n": 64},
+                                  {"cta_group": 1, "block_n": 64, "stream_k": 2}],
+                         ids=["cta1_n128", "cta1_n64", "cta1_n64_sk"])
+def test_narrow_integer_exact(dtg, dtype_in, opts):
+    """Narrow single-CTA tiles, with K ragged at the 128-byte slab."""
+    exact_case(dtg, 384, 448, 1000, dtype_in, options=opts, seed=7)
+
+
 @pytest.mark.parametrize("opts", [{"cta_group": 1, "max_clusters": 1},
                                   {"cta_group": 2, "max_clusters": 1},
                                   {"cta_group": 2, "max_clusters": 3, "group_m": 2},

@@ -127,6 +127,42 @@ def test_many_tiles_per_cta(dtg, opts):
     exact_case(dtg, 1024, 1024, 448, "f16", "k", options=opts, seed=4)
 
 
+# ---------------------------------------------------------------- narrow single-CTA tiles
+NARROW = [{"cta_group": 1, "block_n": 128}, {"cta_group": 1, "block_n": 64}]
+NARROW_IDS = ["cta1_n128", "cta1_n64"]
+
+
+@pytest.mark.parametrize("opts", NARROW, ids=NARROW_IDS)
+@pytest.mark.parametrize("dtype_in", ["f16", "bf16"])
+@pytest.mark.parametrize("layout_b", ["k", "mn"])
+def test_narrow_integer_exact(dtg, opts, dtype_in, layout_b):
+    exact_case(dtg, 512, 512, 1024, dtype_in, layout_b, options=opts, seed=3)
+
+
+@pytest.mark.parametrize("opts", NARROW, ids=NARROW_IDS)
+@pytest.mark.parametrize("shape", [(1, 1, 1), (129, 130, 65), (300, 70, 1000), (1000, 999, 257)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("layout_b", ["k", "mn"])
+def test_narrow_ragged(dtg, opts, shape, layout_b):
+    M, N, K = shape
+    case(dtg, M, N, K, "bf16", "f32", layout_b, ("uniform", -2.0, 2.0), seed=M + N + K, options=opts)
+
+
+@pytest.mark.parametrize("dtype_out", ["f16", "bf16"])
+@pytest.mark.parametrize("opts", NARROW, ids=NARROW_IDS)
+def test_narrow_16bit_out(dtg, dtype_out, opts):
+    case(dtg, 384, 640, 320, "bf16" if dtype_out == "bf16" else "f16", dtype_out, "k",
+         ("normal", 1.0), 5, options=opts)
+
+
+@pytest.mark.parametrize("opts", [dict(NARROW[0], stream_k=2), dict(NARROW[1], stream_k=2),
+                                  dict(NARROW[0], max_clusters=3), dict(NARROW[1], max_clusters=5, group_m=2)],
+                         ids=["cta1_n128_sk", "cta1_n64_sk", "cta1_n128_three", "cta1_n64_five"])
+def test_narrow_stream_k_and_many_tiles(dtg, opts):
+    """Stream-K splits and a handful of CTAs walking many narrow tiles."""
+    exact_case(dtg, 1024, 1024, 448, "f16", "k", options=opts, seed=4)
+
+
 # ---------------------------------------------------------------- 128-deep ring stages
 K128 = [{"cta_group": 2, "k_stage": 128}, {"cta_group": 2, "block_n": 224, "k_stage": 128},
         {"cta_group": 1, "k_stage": 128}, {"cta_group": 2, "k_stage": 128, "max_clusters": 2}]
