@@ -30,8 +30,16 @@ _DT_OUT = {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16, torch.float32: GE
 _LAYOUT = {"k": GEMM_K_MAJOR, "mn": GEMM_MN_MAJOR}
 
 
-def _stream_ptr(stream) -> int:
+# torch's current stream of a device as a raw cudaStream_t, without building a
+# Stream object (about 0.2 us against 2.9 us for current_stream().cuda_stream on
+# the GB300 host); the public call where a torch build lacks it
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_ptr(stream, dev: int | None = None) -> int:
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device() if dev is None else dev)
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
@@ -97,8 +105,8 @@ def _on_device(dev: int, fn, *args):
         return fn(*args)
 
 
-def _gemm_call(a, b, c, M, N, K, din, dout, lb, opts, stream):
-    st = _stream_ptr(stream)
+def _gemm_call(a, b, c, M, N, K, din, dout, lb, opts, stream, dev):
+    st = _stream_ptr(stream, dev)
     if opts is None:
         return binding.lib.gemm(a, b, c, M, N, K, din, dout, GEMM_K_MAJOR, lb, st), "gemm"
     return binding.lib.gemm_ex(a, b, c, M, N, K, din, dout, GEMM_K_MAJOR, lb, ctypes.byref(opts), st), "gemm_ex"
@@ -115,8 +123,9 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *,
     ``options``: dict or GemmOptions of gemm_ex overrides.
     """
     M, N, K, C, din = _prepare(A, B, C, layout_b, out_dtype, "cuda")
-    status, what = _on_device(A.get_device(), _gemm_call, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
-                              din, _DT_OUT[C.dtype], _LAYOUT[layout_b], _options(options), stream)
+    dev = A.get_device()
+    status, what = _on_device(dev, _gemm_call, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                              din, _DT_OUT[C.dtype], _LAYOUT[layout_b], _options(options), stream, dev)
     if status != GEMM_OK:
         raise GemmError(status, what)
     return C

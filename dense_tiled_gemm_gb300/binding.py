@@ -31,7 +31,8 @@ class GemmOptions(ctypes.Structure):
                 ("max_clusters", ctypes.c_int32), ("group_m", ctypes.c_int32),
                 ("timeout_ms", ctypes.c_int32), ("k_stage", ctypes.c_int32),
                 ("stream_k", ctypes.c_int32), ("cluster_pairs", ctypes.c_int32),
-                ("clock_trace", ctypes.c_void_p)]
+                ("clock_trace", ctypes.c_void_p), ("epilogue_warps", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class GemmPlan(ctypes.Structure):
@@ -42,7 +43,8 @@ class GemmPlan(ctypes.Structure):
                 ("realign_a", ctypes.c_int32), ("realign_b", ctypes.c_int32),
                 ("direct_store", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("num_sms", ctypes.c_int32), ("sk_tiles", ctypes.c_int32),
-                ("workspace_bytes", ctypes.c_int32), ("cluster_pairs", ctypes.c_int32)]
+                ("workspace_bytes", ctypes.c_int32), ("cluster_pairs", ctypes.c_int32),
+                ("epilogue_warps", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

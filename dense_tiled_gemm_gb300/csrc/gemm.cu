@@ -50,9 +50,9 @@ int default_k_slabs(int cg, int kind)
 }
 
 template <int CG, int BN, int KS, int KIND, int MC>
-cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap *maps, const KernelParams &kp,
-                           cudaStream_t st);
-using LaunchFn = cudaError_t (*)(int, uint32_t, const CUtensorMap *, const KernelParams &, cudaStream_t);
+cudaError_t launch_variant(int grid_ctas, int threads, uint32_t smem, const CUtensorMap *maps,
+                           const KernelParams &kp, cudaStream_t st);
+using LaunchFn = cudaError_t (*)(int, int, uint32_t, const CUtensorMap *, const KernelParams &, cudaStream_t);
 
 struct Variant {
     int cg;
@@ -316,6 +316,10 @@ gemm_status_t validate(const void *A, const void *B, const void *C, int64_t M, i
             return GEMM_ERR_INVALID_ARG;
         if (o->cluster_pairs > 2)
             return GEMM_ERR_UNSUPPORTED;
+        if (o->epilogue_warps < 0 || o->reserved != 0)
+            return GEMM_ERR_INVALID_ARG;
+        if (o->epilogue_warps != 0 && o->epilogue_warps != 4 && o->epilogue_warps != 8)
+            return GEMM_ERR_UNSUPPORTED;
         if (o->stream_k > 2)
             return GEMM_ERR_UNSUPPORTED;
         const int sk = kind_slab_k(kind_for(dtype_in, scaled));
@@ -331,6 +335,7 @@ struct Plan {
     int grid_ctas;
     int group_m;
     int sk_tiles;          // trailing tiles split along K
+    int epi_warps;         // epilogue warps of the launch: 4 or 8
     size_t ws_bytes;       // stream-K workspace: flags, then partial sums
     bool realign_a, realign_b, direct_store;
 };
@@ -347,7 +352,7 @@ struct PlanKey {
     int32_t dtype_in, dtype_out, layoutB, scaled;
     int32_t misalign;   // bit 0: A, bit 1: B, bit 2: C not describable to the TMA engine
     int32_t cta_group, block_n, max_clusters, group_m, k_stage, stream_k;
-    int32_t cluster_pairs;
+    int32_t cluster_pairs, epilogue_warps;
 };
 
 struct MapKey {
@@ -405,7 +410,7 @@ std::atomic<uint64_t> g_plan_hits{0}, g_plan_misses{0}, g_map_hits{0}, g_map_mis
 
 // Stream-K workspace of a launch: one flag per (CTA, epilogue warp), then one
 // partial-sum slot per CTA (128 rows x block_n FP32).
-size_t sk_flag_bytes(int grid_ctas) { return (static_cast<size_t>(grid_ctas) * 4 * 8 + 255) / 256 * 256; }
+size_t sk_flag_bytes(int grid_ctas) { return (static_cast<size_t>(grid_ctas) * EPI_WARPS_MAX * 8 + 255) / 256 * 256; }
 size_t sk_workspace_bytes(int grid_ctas, int bn)
 {
     return sk_flag_bytes(grid_ctas) + static_cast<size_t>(grid_ctas) * BLOCK_M_CTA * bn * 4;
@@ -525,6 +530,15 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
     const int64_t stage_k = static_cast<int64_t>(sk_elems) * var.ks;
     pl->num_kb = static_cast<int>((K + stage_k - 1) / stage_k);
     pl->sk_tiles = best_sk;
+    // Eight epilogue warps where a unit's work is at most two tiles, so that its
+    // last epilogue (which nothing overlaps) is a large share of its time: 2048^3
+    // measured 5.8% faster and 1024^3 3.2%. Four where main loops dominate: eight
+    // cost 0.5-1% at 8192^3 and beyond, and on the ragged 3000 x 5000 x 2050 workload.
+    const double unit_tiles =
+        best_sk ? static_cast<double>((tiles - best_sk) / units) +
+                      static_cast<double>((static_cast<int64_t>(best_sk) * pl->num_kb + units - 1) / units) / pl->num_kb
+                : static_cast<double>((tiles + units - 1) / units);
+    pl->epi_warps = (o && o->epilogue_warps) ? o->epilogue_warps : (unit_tiles <= 2.0 ? 8 : 4);
     // with stream-K every unit takes a share; otherwise no more units than tiles
     pl->grid_ctas = static_cast<int>(best_sk ? units : std::min<int64_t>(tiles, units)) * var.cg * var.mc;
     pl->ws_bytes = best_sk ? sk_workspace_bytes(pl->grid_ctas, var.bn) : 0;
@@ -560,6 +574,7 @@ PlanKey plan_key(int64_t M, int64_t N, int64_t K, int dtype_in, int dtype_out, i
         k.k_stage = o->k_stage;
         k.stream_k = o->stream_k;
         k.cluster_pairs = o->cluster_pairs;
+        k.epilogue_warps = o->epilogue_warps;
     }
     return k;
 }
@@ -629,22 +644,19 @@ gemm_status_t realign_into(const void *src, int64_t rows, int64_t cols, int64_t 
     // that every source row starts on a word boundary
     const uint64_t align = static_cast<uint64_t>(reinterpret_cast<uintptr_t>(src)) | static_cast<uint64_t>(row_bytes);
     const int v = (align % 16 == 0) ? 16 : (align % 8 == 0) ? 8 : (align % 4 == 0) ? 4 : (align % 2 == 0) ? 2 : 1;
-    // one warp per row at a time, up to 3 blocks of 8 warps per SM: room beside
-    // them for the GEMM CTA (192 threads x 176 registers) that the copy lets
-    // launch early (programmatic dependent launch)
+    // one warp per row at a time, up to 3 blocks of 8 warps per SM
     const unsigned blocks = static_cast<unsigned>(
         std::max<int64_t>(std::min<int64_t>((rows + 7) / 8, static_cast<int64_t>(sms) * 3), 1));
     const uint8_t *s = static_cast<const uint8_t *>(src);
     uint8_t *d = static_cast<uint8_t *>(dst);
+    // In plain stream order: launched early beside the previous GEMM (programmatic
+    // stream serialisation), the copy measured 1.5 us slower per call back to back
+    // on the ragged 3000 x 5000 x 2050 workload, and no faster in a CUDA graph.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(blocks);
     cfg.blockDim = dim3(256);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 0;
     cudaError_t e;
     switch (v) {
     case 16: e = cudaLaunchKernelEx(&cfg, realign_rows_kernel<16>, s, d, rows, row_bytes, pitch); break;
@@ -660,12 +672,12 @@ gemm_status_t realign_into(const void *src, int64_t rows, int64_t cols, int64_t 
 }
 
 template <int CG, int BN, int KS, int KIND, int MC>
-cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap *maps, const KernelParams &kp,
-                           cudaStream_t st)
+cudaError_t launch_variant(int grid_ctas, int threads, uint32_t smem, const CUtensorMap *maps,
+                           const KernelParams &kp, cudaStream_t st)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_ctas));
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     // Programmatic stream serialisation lets this grid's CTAs start their setup
@@ -687,10 +699,10 @@ cudaError_t launch_variant(int grid_ctas, uint32_t smem, const CUtensorMap *maps
                               maps[4], kp);
 }
 
-cudaError_t launch_any(const Variant &v, int grid_ctas, uint32_t smem, const CUtensorMap *maps,
+cudaError_t launch_any(const Variant &v, int grid_ctas, int epi_warps, uint32_t smem, const CUtensorMap *maps,
                        const KernelParams &kp, cudaStream_t st)
 {
-    return v.launch(grid_ctas, smem, maps, kp, st);
+    return v.launch(grid_ctas, (EPI_WARP0 + epi_warps) * 32, smem, maps, kp, st);
 }
 
 // Packed-scale geometry of one operand: row blocks of R rows (128 for A, the
@@ -845,7 +857,7 @@ gemm_status_t encode_and_launch(const DeviceState &d, const PlanKey &pk, const P
     kp.trace = x.trace;
     kp.withhold_kb = x.withhold_kb;
 
-    if (launch_any(var, pl.grid_ctas, lay.smem, maps, kp, st) != cudaSuccess) {
+    if (launch_any(var, pl.grid_ctas, pl.epi_warps, lay.smem, maps, kp, st) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -1104,6 +1116,7 @@ gemm_status_t plan_query(int64_t M, int64_t N, int64_t K, int dtype_in, int dtyp
     plan->sk_tiles = pl.sk_tiles;
     plan->workspace_bytes = static_cast<int32_t>(pl.ws_bytes);
     plan->cluster_pairs = var.mc;
+    plan->epilogue_warps = pl.epi_warps;
     return GEMM_OK;
 }
 

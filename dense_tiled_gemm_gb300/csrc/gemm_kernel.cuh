@@ -83,8 +83,13 @@ constexpr int SF_ATOM_BYTES = 512;
 constexpr int SF_ATOM_ROWS = 32;
 constexpr int SF_ROW_BYTES = 16;
 constexpr int MX_MAX_STAGES = 8;
-constexpr int NUM_THREADS = 192;     // producer warp, MMA warp, 4 epilogue warps
+constexpr int NUM_THREADS = 320;     // at most: producer warp, MMA warp, 8 epilogue warps
 constexpr int EPI_WARP0 = 2;
+// A launch runs 4 or 8 epilogue warps (192 or 320 threads): 8 shorten each
+// tile's epilogue, which pays where a unit's last epilogue is a large share of
+// its time (one or two tiles per unit), and cost a little in main loops that
+// overlap an epilogue.
+constexpr int EPI_WARPS_MAX = 8;
 constexpr int TMEM_COLS = 512;       // two accumulators at columns 0 and 256
 constexpr int ACC_STRIDE = 256;
 constexpr int EPI_COLS = 32;         // accumulator columns per epilogue chunk
@@ -115,7 +120,7 @@ struct KernelParams {
     uint32_t direct_store;     // 1: write C with ordinary stores (unaligned C)
     uint32_t stages;           // ring depth (2 .. MAX_STAGES)
     uint32_t staging_bytes;    // one epilogue staging buffer: 32 rows x 32 columns of C
-    uint32_t staging_bufs;     // staging buffers per epilogue warp: 2 or 4
+    uint32_t staging_bufs;     // staging buffers per TMEM lane quarter: 2 or 4, shared by its epilogue warps
     void *C;                   // used by the direct-store path
     int32_t sk_tiles;          // trailing tiles scheduled stream-K (0: all tiles data-parallel)
     float4 *partials;          // stream-K partial sums: one slot per CTA (128 rows x block_n FP32)
@@ -182,7 +187,8 @@ struct TileConfig {
 
 // Dynamic shared memory, from a 1024-byte aligned base:
 //   ring      stages x {KS slabs of A 128 x 128 B, KS slabs of B BN_CTA x 128 B} (128-byte swizzle)
-//   staging   4 epilogue warps x 2 or 4 buffers x staging_bytes (2 KB for 16-bit C, 4 KB for FP32 C)
+//   staging   4 lane quarters x 2 or 4 buffers x staging_bytes (2 KB for 16-bit C, 4 KB for FP32 C),
+//             split between a quarter's epilogue warps (one or two)
 //   barriers  full[stages], empty[stages], tmem_full[2], tmem_empty[2], mma_done
 //   TMEM base address written by tcgen05.alloc
 __host__ __device__ constexpr uint32_t smem_bytes_for(uint32_t stage_bytes, uint32_t stages,
@@ -453,7 +459,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
         }
         for (uint32_t b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);             // one tcgen05.commit
-            mbar_init(tempty_bar(b), 4u * CG);      // every epilogue warp of the tile
+            mbar_init(tempty_bar(b), (blockDim.x / 32u - EPI_WARP0) * CG);   // every epilogue warp of the tile
         }
         mbar_init(done_bar, 1);
         fence_barrier_init();
@@ -684,10 +690,18 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        const uint32_t ew = warp - EPI_WARP0;                       // 0 .. epilogue warps - 1
+        const uint32_t per_quarter = (blockDim.x / 32u - EPI_WARP0) / 4u;   // 1 or 2 warps
         const uint32_t quarter = warp & 3u;      // the TMEM lane quarter this warp may access
-        const uint32_t staging = base + staging_off + (warp - EPI_WARP0) * p.staging_bufs * p.staging_bytes;
+        // The quarter's warps split its staging buffers and its chunks: with two,
+        // warps 2-5 take chunks [0, C_SPLIT) and warps 6-9 the rest.
+        const uint32_t wbufs = p.staging_bufs / per_quarter;
+        const uint32_t staging = base + staging_off + ew * wbufs * p.staging_bytes;
         const uint64_t c_policy = l2_evict_first_policy();   // C is written once: keep A and B in L2
         constexpr int CHUNKS = BN / EPI_COLS;
+        constexpr int C_SPLIT = (CHUNKS + 1) / 2;
+        const int c_begin = (per_quarter == 2u && ew >= 4u) ? C_SPLIT : 0;
+        const int c_end = (per_quarter == 2u && ew < 4u) ? C_SPLIT : CHUNKS;
         // Stream-K partial slot of CTA `cta`, this warp's 32 rows, chunk c: 32 lanes x 8 float4,
         // laid out so that each float4 store or load of the warp covers 512 contiguous bytes.
         auto partial_chunk = [&](int cta, int c) {
@@ -720,7 +734,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (lane == 0)
                     for (int v = cluster_id - 1; v >= w_first; --v)
                         if (wrote(v) &&
-                            !wait_flag_bounded(w, &p.flags[(static_cast<size_t>(v) * CS + rank) * 4u + quarter],
+                            !wait_flag_bounded(w, &p.flags[(static_cast<size_t>(v) * CS + rank) * EPI_WARPS_MAX + ew],
                                                SITE_EPI_PARTIAL))
                             break;
                 w.aborted = __shfl_sync(0xffffffffu, w.aborted ? 1 : 0, 0) != 0;
@@ -734,13 +748,13 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
             const int col0 = n_blk * BN;
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + acc * ACC_STRIDE;
 #pragma unroll 1
-            for (int c = 0; c < CHUNKS; ++c) {
+            for (int c = c_begin; c < c_end; ++c) {
                 uint32_t v[32];
                 if (!skip) {
                     tmem_ld_32x32b_x32(t_row + static_cast<uint32_t>(c * EPI_COLS), v);
                     tmem_ld_wait_regs(v);
                 }
-                if (c == CHUNKS - 1 && i + 1 < num_jobs) {
+                if (c == c_end - 1 && i + 1 < num_jobs) {
                     // accumulator fully read: hand it back to the MMA issuer (after this
                     // unit's last tile nothing waits for it; teardown's cluster barrier
                     // orders the reads before TMEM is freed)
@@ -788,10 +802,12 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const uint32_t buf = staging + sb * p.staging_bytes;
                 if (lane == 0) {
                     // the store that last used `buf` has read it
-                    if (p.staging_bufs == 4)
+                    if (wbufs == 4)
                         bulk_wait_group_read<3>();
-                    else
+                    else if (wbufs == 2)
                         bulk_wait_group_read<1>();
+                    else
+                        bulk_wait_group_read<0>();
                 }
                 __syncwarp();
                 stage_row(buf, lane, v, p.out_dtype);
@@ -801,14 +817,14 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                     tma_store_2d_hint(&tmap_c, buf, gcol, row0, c_policy);
                     bulk_commit_group();
                 }
-                sb = (sb + 1u) & (p.staging_bufs - 1u);
+                sb = (sb + 1u) & (wbufs - 1u);
             }
             if (jb.kind == JOB_WRITER && !skip) {
                 // publish: every lane's partial stores, then the flag
                 __syncwarp();
                 if (lane == 0) {
                     __threadfence();
-                    st_release_gpu(&p.flags[static_cast<size_t>(blockIdx.x) * 4u + quarter], p.launch_id);
+                    st_release_gpu(&p.flags[static_cast<size_t>(blockIdx.x) * EPI_WARPS_MAX + ew], p.launch_id);
                 }
             }
             if (jb.kind == JOB_OWNER && !skip) {
@@ -820,7 +836,7 @@ gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 if (lane == 0)
                     for (int u = cluster_id - 1; u >= w_first; --u)
                         if (wrote(u))
-                            p.flags[(static_cast<size_t>(u) * CS + rank) * 4u + quarter] = 0ull;
+                            p.flags[(static_cast<size_t>(u) * CS + rank) * EPI_WARPS_MAX + ew] = 0ull;
             }
             if (++acc == 2) {
                 acc = 0;
@@ -924,11 +940,10 @@ static __global__ void pack_scales_kernel(const uint8_t *__restrict__ sf, uint8_
 // lane: 2 KB per warp, ~48 KB per SM at 3 blocks of 8 warps), enough to keep
 // HBM busy although the words are small.
 //
-// Launched with programmatic stream serialisation: the blocks may start while
-// the previous grid on the stream drains, and wait (griddepcontrol.wait) for
-// it before touching memory, since the source may be that grid's output and
-// the destination scratch that it read. They then let the GEMM that follows
-// launch at once; it waits for this grid to complete before it reads.
+// Launched in plain stream order, so the previous grid has completed when it
+// starts (its griddepcontrol.wait returns at once then, and guards a launch
+// that lets it start early). It lets the GEMM that follows launch at once; that
+// GEMM waits for this grid to complete before it reads.
 template <int V>
 __global__ void __launch_bounds__(256) realign_rows_kernel(const uint8_t *__restrict__ src,
                                                            uint8_t *__restrict__ dst, int64_t rows,

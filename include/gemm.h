@@ -208,7 +208,16 @@ gemm_status_t gemm_mx(const void *A, const void *B, const uint8_t *SFA, const ui
  *                 that ([3]-[1]) / ([2]-[0]) is the SM clock, in GHz, that
  *                 the launch ran at. The words are written by the kernel,
  *                 asynchronously on the call's stream; the caller owns them.
- *                 It does not change the plan or the result.
+ *                 It does not change the plan or the result. The global
+ *                 timer advances in steps, so for a launch of a few
+ *                 microseconds pool the words of many launches.
+ *   epilogue_warps warps per CTA that drain the accumulators: 4, or 8 (two
+ *                 per TMEM lane quarter, each taking half of a tile's
+ *                 columns). The default (0) takes 8 where a CTA's work is
+ *                 at most two tiles, whose last epilogue nothing overlaps,
+ *                 and 4 otherwise. Other values give GEMM_ERR_INVALID_ARG
+ *                 (negative) or GEMM_ERR_UNSUPPORTED.
+ *   reserved      must be 0 (GEMM_ERR_INVALID_ARG otherwise).
  */
 typedef struct {
     int32_t cta_group;
@@ -220,6 +229,8 @@ typedef struct {
     int32_t stream_k;
     int32_t cluster_pairs;
     uint64_t *clock_trace;
+    int32_t epilogue_warps;
+    int32_t reserved;       /* must be 0 */
 } gemm_options_t;
 
 /* gemm with overrides. opts may be NULL. An unsupported override combination
@@ -261,6 +272,7 @@ typedef struct {
                               cluster_pairs is 2 */
     int32_t workspace_bytes; /* stream-K partial sums and flags, taken per call */
     int32_t cluster_pairs;   /* CTA pairs per cluster sharing A (1 or 2) */
+    int32_t epilogue_warps;  /* epilogue warps per CTA (4 or 8) */
 } gemm_plan_t;
 
 /* Fill *plan for a problem on the current device. Same validation and

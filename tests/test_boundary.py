@@ -61,11 +61,15 @@ def test_enums_match_header():
 
 
 def test_struct_sizes():
-    # gemm_options_t: 8 int32 fields and the clock-trace pointer; gemm_plan_t: 16 int32 fields
-    assert ctypes.sizeof(binding.GemmOptions) == 40
+    # gemm_options_t: 8 int32 fields, the clock-trace pointer, 2 int32 fields;
+    # gemm_plan_t: 17 int32 fields
+    assert ctypes.sizeof(binding.GemmOptions) == 48
     assert binding.GemmOptions.clock_trace.offset == 32
-    assert ctypes.sizeof(binding.GemmPlan) == 64
-    assert re.search(r"int32_t cluster_pairs;\s*uint64_t \*clock_trace;\s*\} gemm_options_t;", header_text())
+    assert binding.GemmOptions.epilogue_warps.offset == 40
+    assert ctypes.sizeof(binding.GemmPlan) == 68
+    assert re.search(r"int32_t cluster_pairs;\s*uint64_t \*clock_trace;\s*int32_t epilogue_warps;\s*"
+                     r"int32_t reserved;[^\n]*\n\} gemm_options_t;", header_text())
+    assert re.search(r"int32_t epilogue_warps;[^\n]*\n\} gemm_plan_t;", header_text())
 
 
 def test_prototypes_use_the_enum_types():
@@ -138,7 +142,8 @@ def test_invalid_options_rejected_on_host():
     for field, val, expect in (("cta_group", 3, 1), ("cta_group", -1, 1), ("block_n", 96, 2),
                                ("max_clusters", -2, 1), ("group_m", -1, 1), ("timeout_ms", -1, 1),
                                ("k_stage", 96, 2), ("k_stage", -64, 1), ("stream_k", 3, 2),
-                               ("stream_k", -1, 1), ("cluster_pairs", -1, 1), ("cluster_pairs", 3, 2)):
+                               ("stream_k", -1, 1), ("cluster_pairs", -1, 1), ("cluster_pairs", 3, 2),
+                               ("epilogue_warps", -4, 1), ("epilogue_warps", 6, 2), ("reserved", 1, 1)):
         o = binding.GemmOptions()
         setattr(o, field, val)
         rc = binding.lib.gemm_ex(FAKE, FAKE, FAKE, 64, 64, 64, 0, 0, 0, 0, ctypes.byref(o), None)

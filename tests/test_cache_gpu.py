@@ -244,3 +244,19 @@ def test_stream_scratch_grows(dtg):
     for C, ref in outs:
         assert np.array_equal(C.cpu().numpy().astype(np.float64), ref)
     assert dtg.gemm_last_device_status() == (dtg.GEMM_OK, 0)
+
+
+def test_default_stream_is_torchs_current(dtg):
+    """With no stream given, a call goes to torch's current stream of A's device, also
+    inside a torch.cuda.stream context."""
+    s = torch.cuda.Stream()
+    assert dtg._stream_ptr(None) == torch.cuda.current_stream().cuda_stream
+    with torch.cuda.stream(s):
+        assert dtg._stream_ptr(None) == s.cuda_stream
+        assert dtg._stream_ptr(None, torch.cuda.current_device()) == s.cuda_stream
+        A, B = _ops(384, 256, 320, seed=9)
+        C = dtg.gemm(A, B)
+    s.synchronize()
+    ref = dtg.gemm(A, B)
+    torch.cuda.synchronize()
+    assert torch.equal(C, ref)

@@ -163,6 +163,41 @@ def test_narrow_stream_k_and_many_tiles(dtg, opts):
     exact_case(dtg, 1024, 1024, 448, "f16", "k", options=opts, seed=4)
 
 
+# ---------------------------------------------------------------- epilogue warps
+EPI = [({"epilogue_warps": 8, "stream_k": 2}, "k"), ({"epilogue_warps": 4, "stream_k": 2}, "k"),
+       ({"epilogue_warps": 8, "block_n": 224, "stream_k": 2}, "k"),
+       ({"epilogue_warps": 8, "cta_group": 1, "block_n": 64, "stream_k": 2}, "k"),
+       ({"epilogue_warps": 8, "cta_group": 1, "block_n": 256, "max_clusters": 3}, "mn"),
+       ({"epilogue_warps": 8, "max_clusters": 3, "group_m": 2}, "mn"),
+       ({"epilogue_warps": 4, "cta_group": 1, "block_n": 128}, "k")]
+
+
+@pytest.mark.parametrize("opts,layout_b", EPI, ids=["cta2_8_sk", "cta2_4_sk", "n224_8_sk", "cta1_n64_8_sk",
+                                                    "cta1_8_three", "cta2_8_three", "cta1_n128_4"])
+def test_epilogue_warps_integer_exact(dtg, opts, layout_b):
+    """Four and eight epilogue warps: stream-K flags and partial chunks per warp,
+    an odd chunk count split 4/3, and accumulator phases wrapping over many tiles."""
+    exact_case(dtg, 1024, 1024, 448, "f16", layout_b, options=opts, seed=6)
+
+
+@pytest.mark.parametrize("dtype_out", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("warps", [4, 8])
+def test_epilogue_warps_output_types(dtg, dtype_out, warps):
+    """One (FP32) or two (16-bit) staging buffers per warp with eight warps, and a
+    ragged tile edge."""
+    case(dtg, 300, 700, 320, "bf16" if dtype_out == "bf16" else "f16", dtype_out, "k",
+         ("normal", 1.0), 8, options={"epilogue_warps": warps})
+
+
+def test_planner_epilogue_warps(dtg):
+    """Eight warps where a CTA's work is at most two tiles, four where main loops dominate."""
+    assert dtg.gemm_plan(2048, 2048, 2048)["epilogue_warps"] == 8
+    assert dtg.gemm_plan(1024, 1024, 1024)["epilogue_warps"] == 8
+    assert dtg.gemm_plan(8192, 8192, 8192)["epilogue_warps"] == 4
+    assert dtg.gemm_plan(4096, 4096, 8192)["epilogue_warps"] == 4
+    assert dtg.gemm_plan(2048, 2048, 2048, options={"epilogue_warps": 4})["epilogue_warps"] == 4
+
+
 # ---------------------------------------------------------------- 128-deep ring stages
 K128 = [{"cta_group": 2, "k_stage": 128}, {"cta_group": 2, "block_n": 224, "k_stage": 128},
         {"cta_group": 1, "k_stage": 128}, {"cta_group": 2, "k_stage": 128, "max_clusters": 2}]
