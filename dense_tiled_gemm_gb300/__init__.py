@@ -63,35 +63,38 @@ def _check(status: int, what: str):
 def _prepare(A, B, C, layout_b, out_dtype, device_kind):
     """Check A, B (and C, or allocate it) for a GEMM on `device_kind` tensors.
     Returns M, N, K, C and the input type code. Type errors come first."""
-    din = _DT_IN.get(A.dtype)
-    if din is None or B.dtype not in _DT_IN:
+    adt, bdt = A.dtype, B.dtype
+    din = _DT_IN.get(adt)
+    if din is None or bdt not in _DT_IN:
         name, t = ("A", A) if din is None else ("B", B)
         raise TypeError(f"{name} must be float16, bfloat16, float8_e4m3fn or float8_e5m2, got {t.dtype}")
-    if A.dtype != B.dtype:
+    if adt != bdt:
         raise TypeError("A and B must have the same dtype")
     want_cuda = device_kind == "cuda"
     if not (A.is_contiguous() and B.is_contiguous()):
         raise ValueError("A and B must be contiguous")
     if A.is_cuda != want_cuda or B.is_cuda != want_cuda:
         raise ValueError(f"A and B must be {device_kind} tensors")
-    if A.dim() != 2 or B.dim() != 2:
+    sa, sb = A.shape, B.shape
+    if len(sa) != 2 or len(sb) != 2:
         raise ValueError("A and B must be 2-D")
-    M, K = A.shape
+    M, K = sa
     if layout_b == "k":
-        N, Kb = B.shape
+        N, Kb = sb
     elif layout_b == "mn":
-        Kb, N = B.shape
+        Kb, N = sb
     else:
         raise ValueError("layout_b must be 'k' (B is N x K) or 'mn' (B is K x N)")
     if Kb != K:
         raise ValueError(f"K mismatch: A has {K}, B has {Kb}")
     if C is None:
-        default_out = torch.bfloat16 if A.dtype in _FP8 else A.dtype
+        default_out = torch.bfloat16 if adt in _FP8 else adt
         C = torch.empty((M, N), dtype=out_dtype or default_out, device=A.device,
                         pin_memory=(not want_cuda and torch.cuda.is_available()))
-    elif (C.dtype not in _DT_OUT or C.dim() != 2 or C.shape[0] != M or C.shape[1] != N
-          or not C.is_contiguous()):
-        raise ValueError("C must be a contiguous (M, N) float16/bfloat16/float32 tensor")
+    else:
+        sc = C.shape
+        if C.dtype not in _DT_OUT or len(sc) != 2 or sc[0] != M or sc[1] != N or not C.is_contiguous():
+            raise ValueError("C must be a contiguous (M, N) float16/bfloat16/float32 tensor")
     if C.is_cuda != want_cuda:
         raise ValueError(f"C must be a {device_kind} tensor")
     return M, N, K, C, din
@@ -124,8 +127,13 @@ def gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, *,
     """
     M, N, K, C, din = _prepare(A, B, C, layout_b, out_dtype, "cuda")
     dev = A.get_device()
-    status, what = _on_device(dev, _gemm_call, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
-                              din, _DT_OUT[C.dtype], _LAYOUT[layout_b], _options(options), stream, dev)
+    args = (A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, din, _DT_OUT[C.dtype], _LAYOUT[layout_b],
+            _options(options), stream, dev)
+    if dev == torch.cuda.current_device():
+        status, what = _gemm_call(*args)
+    else:
+        with torch.cuda.device(dev):
+            status, what = _gemm_call(*args)
     if status != GEMM_OK:
         raise GemmError(status, what)
     return C
