@@ -231,8 +231,11 @@ class ClockSampler:
 
 # %globaltimer advances in steps, not every nanosecond: a launch of a few
 # microseconds can read a quarter above the maximum clock from one interval.
-# Below this median launch length the clock is pooled over all launches.
+# Below SHORT_LAUNCH_NS of median launch length the clock is pooled over all
+# launches; below TOO_SHORT_NS even that read 35% above the maximum clock
+# (256^3, ~3 us launches), so no in-kernel clock is reported.
 SHORT_LAUNCH_NS = 20000
+TOO_SHORT_NS = 5000
 
 
 def kernel_clock_mhz(trace: torch.Tensor) -> dict:
@@ -257,6 +260,17 @@ def merge_clocks(smi: dict | None, kc: dict | None) -> dict | None:
                                  "samples_under_load": 0, "power_w_max": None}
     out["smi_sm_mhz_under_load"] = out.get("sm_mhz")
     mhz = kc["per_launch"] if kc else []
+    max_mhz = out.get("sm_max_mhz")
+    pooled_ok = bool(mhz) and (max_mhz is None or kc["pooled"] <= 1.02 * max_mhz)
+    if mhz and (kc["median_ns"] < TOO_SHORT_NS or not pooled_ok):
+        out["kernel_mhz_min"] = min(mhz)
+        out["kernel_mhz_max"] = max(mhz)
+        out["sm_mhz_source"] = (f"in-kernel clock not used: median launch {kc['median_ns'] / 1e3:.1f} us, too short "
+                                "for the global timer's steps; " +
+                                ("nvidia-smi samples drawing > 300 W" if out.get("sm_mhz") is not None
+                                 else "no nvidia-smi sample under load"))
+        mhz = []
+        return out
     if mhz:
         n = len(mhz)
         if kc["median_ns"] < SHORT_LAUNCH_NS:

@@ -29,10 +29,10 @@ def test_long_launches_report_the_median():
 
 
 def test_short_launches_report_the_pooled_clock():
-    spans = [2_600 + 37 * (i % 11) for i in range(400)]
+    spans = [6_600 + 37 * (i % 11) for i in range(400)]
     kc = bench.kernel_clock_mhz(_trace(spans, 1_950.0, step_ns=1_000))
     per = kc["per_launch"]
-    assert max(per) > 2_400.0                 # single intervals read far above the true clock
+    assert max(per) > 2_070.0                 # single intervals read above the maximum clock
     out = bench.merge_clocks(None, kc)
     assert abs(out["sm_mhz"] - 1_950.0) < 20.0, out["sm_mhz"]
     assert "pooled over 400" in out["sm_mhz_source"]
@@ -47,3 +47,21 @@ def test_no_trace_leaves_the_smi_record():
     empty = bench.kernel_clock_mhz(torch.zeros(3, 4, dtype=torch.int64))
     assert empty == {"per_launch": [], "pooled": None, "median_ns": None}
     assert bench.merge_clocks(None, empty)["sm_mhz"] is None
+
+
+def test_launches_too_short_give_no_in_kernel_clock():
+    spans = [2_600 + 37 * (i % 11) for i in range(400)]
+    kc = bench.kernel_clock_mhz(_trace(spans, 1_950.0, step_ns=1_000))
+    smi = {"sm_mhz": None, "sm_max_mhz": 2_070.0, "reasons": [], "samples": 3, "samples_under_load": 0,
+           "power_w_max": 150.0}
+    out = bench.merge_clocks(smi, kc)
+    assert out["sm_mhz"] is None and "not used" in out["sm_mhz_source"]
+
+
+def test_pooled_clock_above_the_maximum_is_dropped():
+    spans = [9_000] * 100
+    kc = bench.kernel_clock_mhz(_trace(spans, 2_600.0))       # a clock no GB300 SM reaches
+    smi = {"sm_mhz": 1_800.0, "sm_max_mhz": 2_070.0, "reasons": [], "samples": 5, "samples_under_load": 5,
+           "power_w_max": 900.0}
+    out = bench.merge_clocks(smi, kc)
+    assert out["sm_mhz"] == 1_800.0 and "not used" in out["sm_mhz_source"]
