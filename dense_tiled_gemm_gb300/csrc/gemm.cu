@@ -423,17 +423,23 @@ int sk_tiles_for(int64_t T, int64_t U) { return static_cast<int>(T < 2 * U ? T :
 
 // Predicted time of a plan in microseconds, fitted to CUDA-graph timings of
 // every variant (128 x 64 to 256 x 256 tiles, each with and without stream-K)
-// on 15 shapes from 512^3 to 2560^3 with K up to 16384, at ~1.9 GHz:
+// on 15 shapes from 512^3 to 2560^3 with K up to 16384, and of the planner's
+// plan, data-parallel plans and 224-wide plans on 7 shapes from 3072^3 to
+// 8192^3, at 1.7-1.9 GHz:
 //  - one tile on one SM costs the larger of its products at 80% of the tensor
 //    rate (block_n x K bytes / 64 cycles) and its operand bytes,
-//    (128 / mc + block_n / cg) rows x K bytes, at ~55 bytes per SM cycle from
-//    L2: narrow tiles are bound by L2, not by the tensor core;
+//    (128 / mc + block_n / cg) rows x K bytes, from L2 at ~55 bytes per SM
+//    cycle for single CTAs and ~45 for CTA pairs: narrow tiles are bound by L2,
+//    not by the tensor core, and 224-wide pair tiles do less work per byte
+//    than 256-wide ones;
 //  - a launch pays ~2.6 us (ring fill, teardown) plus its last tile's
-//    epilogue, ~0.01 us per column, which nothing overlaps;
-//  - a stream-K owner adds its writers' partial sums, ~1.5 us plus ~1 us per
-//    writer and 32-column chunk. With one writer and data-parallel tiles after
-//    it, the next tile's main loop hides up to one tile time of that; otherwise
-//    (fewer tiles than two waves) the whole fix-up adds to the launch.
+//    epilogue, ~0.006 us per column, which nothing overlaps;
+//  - a stream-K owner adds its writers' partial sums: in effect ~6 us plus
+//    ~1.5 us per writer and 32-column chunk, more than the fix-up's own time
+//    in a trace, as it also slows the main loop beside it. With one writer
+//    and data-parallel tiles after it, the next tile's main loop hides up to
+//    one tile time of that; otherwise (fewer tiles than two waves) the whole
+//    fix-up adds to the launch.
 struct Cost {
     double dp, sk;
     int sk_tiles;
@@ -441,11 +447,13 @@ struct Cost {
 
 Cost plan_cost(int64_t T, int64_t U, int64_t KB, int64_t k_bytes, int cg, int bn, int mc)
 {
-    constexpr double kMmaEff = 0.8, kL2BytesPerCycle = 55.0, kCyclesPerUs = 1900.0;
-    constexpr double kLaunchUs = 2.6, kEpilogueUsPerCol = 0.01, kFixUs = 1.5, kFixChunkUs = 1.0;
+    constexpr double kMmaEff = 0.8, kCyclesPerUs = 1900.0;
+    constexpr double kL2BytesPerCycleCta = 55.0, kL2BytesPerCyclePair = 45.0;
+    constexpr double kLaunchUs = 2.6, kEpilogueUsPerCol = 0.006, kFixUs = 6.0, kFixChunkUs = 1.5;
     const double kb = static_cast<double>(k_bytes);
     const double mma = bn * kb / 64.0 / kMmaEff;
-    const double l2 = (128.0 / mc + static_cast<double>(bn) / cg) * kb / kL2BytesPerCycle;
+    const double l2 = (128.0 / mc + static_cast<double>(bn) / cg) * kb /
+                      (cg == 1 ? kL2BytesPerCycleCta : kL2BytesPerCyclePair);
     const double tile = std::max(mma, l2) / kCyclesPerUs;
     const double fixed = kLaunchUs + kEpilogueUsPerCol * bn;
     Cost c;

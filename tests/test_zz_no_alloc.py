@@ -82,12 +82,12 @@ def test_no_alloc_rejects_operands_beyond_its_array(lib):
 
 def test_no_alloc_stream_k_workspace(lib):
     """Stream-K partial sums go into the fixed array after the re-pitched copies.
-    3000 x 5000 x 2050 (A re-pitched, 12.3 MB; partials ~20 MB) fits: same plan and
-    the same bits as gemm. 6000 x 5000 x 2050 (A re-pitched, 24.7 MB) leaves no room
+    3000 x 5000 x 2050 (A re-pitched, 12.7 MB; partials ~20 MB) fits: same plan and
+    the same bits as gemm. 4000 x 5000 x 2050 (A re-pitched, 16.9 MB) leaves no room
     for the partials: the call keeps every tile whole and stays within the bound."""
     import ctypes
     import dense_tiled_gemm_gb300 as dtg
-    for M, fits in ((3000, True), (6000, False)):
+    for M, fits in ((3000, True), (4000, False)):
         N, K = 5000, 2050
         assert dtg.gemm_plan(M, N, K, dtype_in=torch.bfloat16, dtype_out=torch.float32,
                              layout_b="mn")["sk_tiles"] > 0
