@@ -88,6 +88,13 @@ typedef enum {
  *             (GEMM_MN_MAJOR gives GEMM_ERR_UNSUPPORTED).
  *   stream    cudaStream_t as void*.
  *
+ * Tile choice: the library runs the tile shape (256 x 256 or 256 x 224 per CTA
+ * pair; 128 x 256, 128 x 128 or 128 x 64 per single CTA), the schedule below
+ * and the epilogue width that its time model predicts fastest for the
+ * problem. Narrow single-CTA tiles serve problems of few tiles, which wide
+ * tiles would leave most SMs idle for. gemm_plan reports the choice and
+ * gemm_ex overrides it.
+ *
  * Tail scheduling: the grid is persistent, one unit (CTA or CTA pair) per
  * resident slot. When the tile count leaves the last wave part-empty, the
  * planner may split the last tiles along K (stream-K): each unit then gets an
