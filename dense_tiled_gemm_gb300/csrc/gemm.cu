@@ -538,15 +538,19 @@ gemm_status_t make_plan(const DeviceState &d, int64_t M, int64_t N, int64_t K, i
     const int64_t stage_k = static_cast<int64_t>(sk_elems) * var.ks;
     pl->num_kb = static_cast<int>((K + stage_k - 1) / stage_k);
     pl->sk_tiles = best_sk;
-    // Eight epilogue warps where a unit's work is at most two tiles, so that its
-    // last epilogue (which nothing overlaps) is a large share of its time: 2048^3
-    // measured 5.8% faster and 1024^3 3.2%. Four where main loops dominate: eight
-    // cost 0.5-1% at 8192^3 and beyond, and on the ragged 3000 x 5000 x 2050 workload.
+    // Eight epilogue warps where a unit's last epilogue (which nothing overlaps)
+    // is a large share of its time: work of at most two tiles (2048^3 measured
+    // 5.8% faster, 1024^3 3.2%), or of at most four with a 16-bit C (4096^3 and
+    // 4096 x 4096 x 8192: 0.5-0.7% faster in short runs, 0.7-1.8% under the
+    // power cap). Four elsewhere: eight cost 0.5-1% at 8192^3 and beyond, and
+    // with an FP32 C, which leaves each of the eight one staging buffer (1.1%
+    // on the ragged 3000 x 5000 x 2050 workload).
     const double unit_tiles =
         best_sk ? static_cast<double>((tiles - best_sk) / units) +
                       static_cast<double>((static_cast<int64_t>(best_sk) * pl->num_kb + units - 1) / units) / pl->num_kb
                 : static_cast<double>((tiles + units - 1) / units);
-    pl->epi_warps = (o && o->epilogue_warps) ? o->epilogue_warps : (unit_tiles <= 2.0 ? 8 : 4);
+    const bool wide_epilogue = unit_tiles <= 2.0 || (unit_tiles <= 4.0 && dtype_out != GEMM_F32);
+    pl->epi_warps = (o && o->epilogue_warps) ? o->epilogue_warps : (wide_epilogue ? 8 : 4);
     // with stream-K every unit takes a share; otherwise no more units than tiles
     pl->grid_ctas = static_cast<int>(best_sk ? units : std::min<int64_t>(tiles, units)) * var.cg * var.mc;
     pl->ws_bytes = best_sk ? sk_workspace_bytes(pl->grid_ctas, var.bn) : 0;

@@ -220,9 +220,10 @@ gemm_status_t gemm_mx(const void *A, const void *B, const uint8_t *SFA, const ui
  *                 microseconds pool the words of many launches.
  *   epilogue_warps warps per CTA that drain the accumulators: 4, or 8 (two
  *                 per TMEM lane quarter, each taking half of a tile's
- *                 columns). The default (0) takes 8 where a CTA's work is
- *                 at most two tiles, whose last epilogue nothing overlaps,
- *                 and 4 otherwise. Other values give GEMM_ERR_INVALID_ARG
+ *                 columns). The default (0) takes 8 where a CTA's last
+ *                 epilogue, which nothing overlaps, is a large share of its
+ *                 work (at most two tiles, or four with a 16-bit C), and 4
+ *                 otherwise. Other values give GEMM_ERR_INVALID_ARG
  *                 (negative) or GEMM_ERR_UNSUPPORTED.
  *   reserved      must be 0 (GEMM_ERR_INVALID_ARG otherwise).
  */

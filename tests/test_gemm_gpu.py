@@ -190,11 +190,14 @@ def test_epilogue_warps_output_types(dtg, dtype_out, warps):
 
 
 def test_planner_epilogue_warps(dtg):
-    """Eight warps where a CTA's work is at most two tiles, four where main loops dominate."""
+    """Eight warps where a CTA's work is at most two tiles, or four with a 16-bit C;
+    four where main loops dominate or C is FP32."""
     assert dtg.gemm_plan(2048, 2048, 2048)["epilogue_warps"] == 8
     assert dtg.gemm_plan(1024, 1024, 1024)["epilogue_warps"] == 8
+    assert dtg.gemm_plan(4096, 4096, 8192)["epilogue_warps"] == 8
     assert dtg.gemm_plan(8192, 8192, 8192)["epilogue_warps"] == 4
-    assert dtg.gemm_plan(4096, 4096, 8192)["epilogue_warps"] == 4
+    assert dtg.gemm_plan(3000, 5000, 2050, dtype_in=torch.bfloat16, dtype_out=torch.float32,
+                         layout_b="mn")["epilogue_warps"] == 4
     assert dtg.gemm_plan(2048, 2048, 2048, options={"epilogue_warps": 4})["epilogue_warps"] == 4
 
 
