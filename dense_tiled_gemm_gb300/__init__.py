@@ -20,7 +20,7 @@ from .binding import (GEMM_BF16, GEMM_E2M1, GEMM_E4M3, GEMM_E5M2, GEMM_F16, GEMM
 
 __all__ = ["gemm", "gemm_ex", "gemm_mx", "attention", "gemm_plan", "gemm_from_host", "gemm_from_host_async",
            "gemm_release_workspace", "gemm_cache_stats", "gemm_cache_clear", "gemm_selftest_withheld_load",
-           "gemm_last_device_status", "gemm_selftest_wait_timeout", "gemm_status_string",
+           "gemm_last_device_status", "gemm_selftest_wait_timeout", "gemm_status_string", "gemm_no_alloc_scratch",
            "gemm_launch_count", "gemm_schedule_jobs", "GemmError", "GemmOptions", "GemmPlan"]
 
 _DT_IN = {torch.float16: GEMM_F16, torch.bfloat16: GEMM_BF16,
@@ -335,6 +335,13 @@ def gemm_schedule_jobs(num_tiles: int, units: int, k_blocks: int, sk_tiles: int,
     _check(binding.lib.gemm_schedule_jobs(num_tiles, units, k_blocks, sk_tiles, unit, jobs, n.value,
                                           ctypes.byref(n)), "gemm_schedule_jobs")
     return [(j.tile, j.kb_begin, j.kb_end, j.kind) for j in jobs[:n.value]]
+
+
+def gemm_no_alloc_scratch() -> tuple[int, int]:
+    """(device address, size in bytes) of the current device's gemm_no_alloc array."""
+    ptr, size = ctypes.c_void_p(0), ctypes.c_size_t(0)
+    _check(binding.lib.gemm_no_alloc_scratch(ctypes.byref(ptr), ctypes.byref(size)), "gemm_no_alloc_scratch")
+    return int(ptr.value or 0), int(size.value)
 
 
 def gemm_no_alloc(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, *, layout_b: str = "k",

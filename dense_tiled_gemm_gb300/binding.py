@@ -112,6 +112,10 @@ def _declare(lib):
     lib.gemm_schedule_jobs.restype = c_int
     lib.gemm_schedule_jobs.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(GemmJob), i32,
                                        ctypes.POINTER(i32)]
+    lib.gemm_no_alloc.restype = c_int
+    lib.gemm_no_alloc.argtypes = gemm_args + [vp]
+    lib.gemm_no_alloc_scratch.restype = c_int
+    lib.gemm_no_alloc_scratch.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_size_t)]
     return lib
 
 
@@ -123,9 +127,3 @@ def load(path: str = LIB_PATH):
 
 
 lib = load()
-
-# gemm_no_alloc: the same arguments as gemm; declared here for the binding below.
-lib.gemm_no_alloc.restype = ctypes.c_int
-lib.gemm_no_alloc.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
-                              ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
-                              ctypes.c_int, ctypes.c_int, ctypes.c_void_p]

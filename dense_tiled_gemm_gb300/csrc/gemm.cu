@@ -1537,3 +1537,18 @@ extern "C" gemm_status_t gemm_no_alloc(const void *A, const void *B, void *C, in
     return run_no_alloc(A, B, C, M, N, K, dtype_in, dtype_out, layoutA, layoutB,
                         static_cast<cudaStream_t>(stream));
 }
+
+extern "C" gemm_status_t gemm_no_alloc_scratch(void **ptr, size_t *bytes)
+{
+    if (!ptr || !bytes)
+        return GEMM_ERR_INVALID_ARG;
+    *ptr = nullptr;
+    *bytes = 0;
+    void *p = nullptr;
+    const gemm_status_t rc = no_alloc_scratch(&p);
+    if (rc != GEMM_OK)
+        return rc;
+    *ptr = p;
+    *bytes = GEMM_NO_ALLOC_SCRATCH_BYTES;
+    return GEMM_OK;
+}

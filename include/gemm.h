@@ -435,6 +435,19 @@ gemm_status_t gemm_no_alloc(const void *A, const void *B, void *C,
                             void *stream);
 
 /*
+ * gemm_no_alloc_scratch: the current device's fixed array of gemm_no_alloc,
+ * for tests and debuggers that check what the calls write into it.
+ * *ptr receives its device address and *bytes its size
+ * (GEMM_NO_ALLOC_SCRATCH_BYTES). The address is looked up as on a first
+ * gemm_no_alloc call on the device. The array belongs to the library: a
+ * caller may read it, or fill it between calls that are not in flight,
+ * since no call depends on its previous contents.
+ * Errors: GEMM_ERR_INVALID_ARG (ptr or bytes NULL), GEMM_ERR_NO_DEVICE,
+ * GEMM_ERR_CUDA.
+ */
+gemm_status_t gemm_no_alloc_scratch(void **ptr, size_t *bytes);
+
+/*
  * gemm_schedule_jobs: the work list that unit `unit` of a launch walks, as
  * computed by the kernel itself (no GPU needed). Tiles [0, sk_tiles) (the
  * first in the swizzled raster order) are laid end to end in k-blocks

@@ -107,3 +107,61 @@ def test_no_alloc_stream_k_workspace(lib):
             ok, ratio, n_bad, first = tolerance.check(C_new.double().cpu().numpy(),
                                                       C_gemm.double().cpu().numpy(), C_abs, "f32")
             assert ok, f"{n_bad} elements differ beyond the bound, first {first}"
+
+
+class _DeviceBytes:
+    """A raw device range as a CUDA array, so that torch can view it without a copy."""
+
+    def __init__(self, ptr: int, n: int):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "|u1", "data": (ptr, False), "version": 3}
+
+
+def _used_bytes(plan, M, N, K, layout_b, eb=2):
+    """The part of the array a call uses, from the layout gemm.h documents: the padded
+    copies (row bytes rounded up to 128), A then B, each from a 256-byte boundary,
+    then the stream-K workspace."""
+    up = lambda v, m: -(-v // m) * m
+    a_bytes = M * up(K * eb, 128) if plan["realign_a"] else 0
+    b_rows, b_cols = (K, N) if layout_b == "mn" else (N, K)
+    b_off = up(a_bytes, 256)
+    b_bytes = b_rows * up(b_cols * eb, 128) if plan["realign_b"] else 0
+    if plan["sk_tiles"]:
+        return up(b_off + b_bytes, 256) + plan["workspace_bytes"]
+    return b_off + b_bytes
+
+
+@pytest.mark.parametrize("M,N,K,layout_b,opts_sk", [(3000, 5000, 2050, "mn", True), (1000, 1000, 1090, "k", False)],
+                         ids=["repitched_a_stream_k", "repitched_a_and_b"])
+def test_no_alloc_writes_only_the_used_part_of_its_array(lib, M, N, K, layout_b, opts_sk):
+    """The fixed array, viewed through gemm_no_alloc_scratch and filled with a pattern:
+    a call writes inside the part its plan uses and leaves every byte after it as it was."""
+    import dense_tiled_gemm_gb300 as dtg
+    ptr, size = dtg.gemm_no_alloc_scratch()
+    assert ptr != 0 and size == 32 * 1024 * 1024
+    arr = torch.as_tensor(_DeviceBytes(ptr, size), device="cuda")
+    plan = dtg.gemm_plan(M, N, K, dtype_in=torch.bfloat16, dtype_out=torch.float32, layout_b=layout_b)
+    assert plan["realign_a"] == 1 and (plan["sk_tiles"] > 0) == opts_sk
+    used = _used_bytes(plan, M, N, K, layout_b)
+    assert 0 < used <= size
+    A, B = workloads.make_operands(M, N, K, "bf16", layout_b, ("uniform", -2.0, 2.0), 60 + M)
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    Ad, Bd = A.cuda(), B.cuda()
+    torch.cuda.synchronize()
+    arr.fill_(0xA5)
+    torch.cuda.synchronize()
+    assert _call(lib.gemm_no_alloc, Ad, Bd, C, M, N, K, "bf16", "f32", layout_b) == 0
+    torch.cuda.synchronize()
+    assert bool((arr[used:] == 0xA5).all()), "a write past the used part of the array"
+    assert not bool((arr[:used] == 0xA5).all()), "the used part was not written"
+    rows = workloads.sample_rows(M, 16, M)
+    C_ref, C_abs = oracle.gemm_ref(workloads.as_bits(A), workloads.as_bits(B), M, N, K, "bf16", layout_b, rows=rows)
+    ok, ratio, n_bad, first = tolerance.check(C.cpu().numpy().astype(np.float64)[rows], C_ref, C_abs, "f32")
+    assert ok, f"{n_bad} out of bound (worst {ratio:.3g}) first {first}"
+
+
+def test_no_alloc_scratch_rejects_null_outputs(lib):
+    import ctypes
+    size = ctypes.c_size_t(0)
+    assert lib.gemm_no_alloc_scratch(None, ctypes.byref(size)) == 1      # GEMM_ERR_INVALID_ARG
+    ptr = ctypes.c_void_p(0)
+    assert lib.gemm_no_alloc_scratch(ctypes.byref(ptr), None) == 1
